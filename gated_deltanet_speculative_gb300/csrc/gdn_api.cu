@@ -1,0 +1,219 @@
+// gdn_api.cu -- the C ABI (include/gdn.h): host-side validation, launch
+// configuration and status codes.  Nothing here allocates device memory;
+// every buffer and stream belongs to the caller.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "gdn_commit.cuh"
+#include "gdn_launch.h"
+
+namespace {
+
+__device__ int g_device_error;   // OR of GDN_DERR_* bits raised by the kernels
+
+constexpr int kMaxDevices = 64;
+
+// Per-device address of g_device_error, looked up once per device.
+int *error_word() {
+    static int *addr[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_device_error) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<int *>(a);
+    }
+    return addr[dev];
+}
+
+bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+int check_dims(const gdn_dims *d) {
+    if (!d) return GDN_ENULL;
+    if (d->n_k_heads <= 0 || d->n_v_heads <= 0 || d->n_v_heads > 65535) return GDN_EINVAL;
+    if (d->n_v_heads % d->n_k_heads != 0 || d->n_v_heads / d->n_k_heads > 8) return GDN_EINVAL;
+    if (d->d_k != d->d_v || (d->d_k != 32 && d->d_k != 64 && d->d_k != 128)) return GDN_EINVAL;
+    if (d->conv_width != 4) return GDN_EINVAL;
+    if (!std::isfinite(d->q_scale)) return GDN_EINVAL;
+    if (!(d->eps_l2 >= 0.0f) || !std::isfinite(d->eps_l2)) return GDN_EINVAL;
+    if (!(d->eps_rms >= 0.0f) || !std::isfinite(d->eps_rms)) return GDN_EINVAL;
+    return GDN_OK;
+}
+
+int check_weights(const gdn_weights *w) {
+    if (!w || !w->conv_w || !w->A_log || !w->dt_bias || !w->norm_w) return GDN_ENULL;
+    if (!aligned(w->conv_w, 16) || !aligned(w->norm_w, 16) || !aligned(w->A_log, 4) || !aligned(w->dt_bias, 4))
+        return GDN_EALIGN;
+    return GDN_OK;
+}
+
+int check_cache(const gdn_cache *c) {
+    if (!c || !c->state || !c->tail) return GDN_ENULL;
+    if (c->n_slots <= 0) return GDN_EINVAL;
+    if (!aligned(c->state, 16) || !aligned(c->tail, 16)) return GDN_EALIGN;
+    return GDN_OK;
+}
+
+int check_rows(const gdn_rows *r) {
+    if (!r || !r->mixed || !r->z || !r->a || !r->b || !r->y) return GDN_ENULL;
+    if (!aligned(r->mixed, 16) || !aligned(r->z, 16) || !aligned(r->y, 16) || !aligned(r->a, 2) ||
+        !aligned(r->b, 2))
+        return GDN_EALIGN;
+    return GDN_OK;
+}
+
+#define GDN_TRY(expr)                 \
+    do {                              \
+        const int rc_ = (expr);       \
+        if (rc_ != GDN_OK) return rc_; \
+    } while (0)
+
+gdn::RowParams row_params(const gdn_dims *d, const gdn_weights *w, const gdn_cache *c, const gdn_rows *r,
+                          const int32_t *slot, int *err) {
+    gdn::RowParams p = {};
+    p.Hk = d->n_k_heads;
+    p.Hv = d->n_v_heads;
+    p.G = d->n_v_heads / d->n_k_heads;
+    p.CH = 2 * d->n_k_heads * d->d_k + d->n_v_heads * d->d_v;
+    p.q_scale = d->q_scale;
+    p.eps_l2 = d->eps_l2;
+    p.eps_rms = d->eps_rms;
+    p.conv_w = static_cast<const uint16_t *>(w->conv_w);
+    p.A_log = w->A_log;
+    p.dt_bias = w->dt_bias;
+    p.norm_w = static_cast<const uint16_t *>(w->norm_w);
+    p.state = c->state;
+    p.tail = static_cast<uint16_t *>(c->tail);
+    p.n_slots = c->n_slots;
+    p.mixed = static_cast<const uint16_t *>(r->mixed);
+    p.z = static_cast<const uint16_t *>(r->z);
+    p.a = static_cast<const uint16_t *>(r->a);
+    p.b = static_cast<const uint16_t *>(r->b);
+    p.y = static_cast<uint16_t *>(r->y);
+    p.slot = slot;
+    p.err = err;
+    return p;
+}
+
+int launch_rows(int D, int mode, const gdn::RowParams &p, int n_streams, void *stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (D) {
+        case 32: e = gdn::launch_rows_d32(mode, p, n_streams, st); break;
+        case 64: e = gdn::launch_rows_d64(mode, p, n_streams, st); break;
+        default: e = gdn::launch_rows_d128(mode, p, n_streams, st); break;
+    }
+    return e == cudaSuccess ? GDN_OK : GDN_ECUDA;
+}
+
+int rows_entry(int mode, const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
+               const int32_t *row_ptr, const int32_t *parent, int32_t n_streams, int32_t n_rows,
+               const gdn_rows *rows, float *rec_state, void *rec_tail, void *stream) {
+    GDN_TRY(check_dims(dims));
+    GDN_TRY(check_weights(w));
+    GDN_TRY(check_cache(cache));
+    GDN_TRY(check_rows(rows));
+    if (!slot) return GDN_ENULL;
+    if (n_streams <= 0 || n_streams > 65535) return GDN_EINVAL;
+    if (mode != gdn::kStep) {
+        if (!row_ptr || !rec_state || !rec_tail) return GDN_ENULL;
+        if (mode == gdn::kTree && !parent) return GDN_ENULL;
+        if (n_rows <= 0) return GDN_EINVAL;
+        if (!aligned(rec_state, 16) || !aligned(rec_tail, 16)) return GDN_EALIGN;
+    }
+    if (!aligned(slot, 4) || (row_ptr && !aligned(row_ptr, 4)) || (parent && !aligned(parent, 4)))
+        return GDN_EALIGN;
+    int *err = error_word();
+    if (!err) return GDN_ECUDA;
+    gdn::RowParams p = row_params(dims, w, cache, rows, slot, err);
+    p.row_ptr = row_ptr;
+    p.parent = parent;
+    p.n_rows = mode == gdn::kStep ? n_streams : n_rows;
+    p.rec_state = rec_state;
+    p.rec_tail = static_cast<uint16_t *>(rec_tail);
+    return launch_rows(dims->d_k, mode, p, n_streams, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_step(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
+             int32_t n_streams, const gdn_rows *rows, void *stream) {
+    return rows_entry(gdn::kStep, dims, w, cache, slot, nullptr, nullptr, n_streams, n_streams, rows, nullptr,
+                      nullptr, stream);
+}
+
+int gdn_window(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
+               const int32_t *row_ptr, int32_t n_streams, int32_t n_rows, const gdn_rows *rows, float *rec_state,
+               void *rec_tail, void *stream) {
+    return rows_entry(gdn::kWindow, dims, w, cache, slot, row_ptr, nullptr, n_streams, n_rows, rows, rec_state,
+                      rec_tail, stream);
+}
+
+int gdn_tree(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
+             const int32_t *row_ptr, const int32_t *parent, int32_t n_streams, int32_t n_rows,
+             const gdn_rows *rows, float *rec_state, void *rec_tail, void *stream) {
+    return rows_entry(gdn::kTree, dims, w, cache, slot, row_ptr, parent, n_streams, n_rows, rows, rec_state,
+                      rec_tail, stream);
+}
+
+int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot, const int32_t *keep_row,
+               int32_t n_streams, int32_t n_rows, const float *rec_state, const void *rec_tail, void *stream) {
+    GDN_TRY(check_dims(dims));
+    GDN_TRY(check_cache(cache));
+    if (!slot || !keep_row || !rec_state || !rec_tail) return GDN_ENULL;
+    if (n_streams <= 0 || n_streams > 65535 || n_rows <= 0) return GDN_EINVAL;
+    if (!aligned(slot, 4) || !aligned(keep_row, 4) || !aligned(rec_state, 16) || !aligned(rec_tail, 16))
+        return GDN_EALIGN;
+    int *err = error_word();
+    if (!err) return GDN_ECUDA;
+    gdn::CommitParams p = {};
+    p.Hv = dims->n_v_heads;
+    p.D = dims->d_k;
+    p.CH = 2 * dims->n_k_heads * dims->d_k + dims->n_v_heads * dims->d_v;
+    p.state = cache->state;
+    p.tail = static_cast<uint16_t *>(cache->tail);
+    p.n_slots = cache->n_slots;
+    p.slot = slot;
+    p.keep_row = keep_row;
+    p.n_rows = n_rows;
+    p.rec_state = rec_state;
+    p.rec_tail = static_cast<const uint16_t *>(rec_tail);
+    p.err = err;
+    const dim3 grid(p.Hv, n_streams);
+    gdn::gdn_commit_kernel<<<grid, gdn::kCommitThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ECUDA;
+}
+
+const char *gdn_status_string(int status) {
+    switch (status) {
+        case GDN_OK: return "ok";
+        case GDN_EINVAL: return "invalid size or geometry";
+        case GDN_ENULL: return "required pointer is NULL";
+        case GDN_EALIGN: return "pointer misaligned";
+        case GDN_ECUDA: return "CUDA runtime error";
+        case GDN_EWORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+int gdn_get_device_error(void *stream, int32_t *bits) {
+    if (!bits) return GDN_ENULL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int value = 0;
+    static const int zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&value, g_device_error, sizeof(int), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return GDN_ECUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return GDN_ECUDA;
+    if (cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return GDN_ECUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return GDN_ECUDA;
+    *bits = value;
+    return GDN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,8 @@
+// gdn_rows_d64.cu -- row kernels (step, window, tree) for d_k = d_v = 64.
+#include "gdn_launch.h"
+
+namespace gdn {
+cudaError_t launch_rows_d64(int mode, const RowParams &p, int n_streams, cudaStream_t st) {
+    return launch_rows<64>(mode, p, n_streams, st);
+}
+}  // namespace gdn

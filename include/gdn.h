@@ -1,0 +1,200 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) gated-DeltaNet verify path.
+ *
+ * One GDN linear-attention layer's core, after its input projection and
+ * before its output projection: causal depthwise conv1d (width 4) with a
+ * kept tail, SiLU, L2-normalised q and k, the gated delta rule
+ *     S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T,   o_t = S_t q_t,
+ *     a_t = exp(-exp(A_log) * softplus(a + dt_bias)),  b_t = sigmoid(b),
+ * and the gated RMSNorm  y = RMSNorm(o) * w_norm * SiLU(z).
+ *
+ * Sources, by page:
+ *  [P932]  TensorFold #932 "perf(qwen3_5 cuda): deliver the first token
+ *          before drafting".  Commit notes on the Qwen3.5 CUDA engine:
+ *          - "MLX affine 4-bit checkpoint on the native CUDA server": the
+ *            layer glue is the gated delta rule and a causal convolution;
+ *            windows of up to 16 rows record each row's recurrence and
+ *            convolution tail; a window's rows equal one-row steps bit for
+ *            bit.
+ *          - "The 2B's CUDA engine now reads its widths": value heads over
+ *            fewer key heads; A_log per value head.
+ *          - "A verify window's rows may form a tree": each row's parent is
+ *            given, and the convolution taps and the delta rule follow the
+ *            row's own branch; one-row steps and prompts update in place.
+ *  [P747]  TensorFold #747 "perf(qwen27 cuda): reduce repeated-prompt
+ *          TTFT", first commit note: verify rounds take every stream's
+ *          window together, up to 16 streams of 16 rows, and commit only
+ *          each stream's accepted path; the engine's kernels include the
+ *          GDN tree, replay and prompt-chain kernels; prompts that arrive
+ *          together share one prefill pass.
+ *  [P888]  TensorFold #888 "Qwen3.5/3.8 on CUDA: kept prompt states in host
+ *          memory": a kept state is a stream's DeltaNet recurrences and
+ *          conv windows, whole.
+ *
+ * Conventions shared by every entry point
+ *  - Every pointer argument named "device" is a CUDA device pointer owned by
+ *    the caller; the library allocates nothing, frees nothing and keeps no
+ *    state between calls except, per device, the address of its device error
+ *    word.  All work is enqueued on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) and the call returns without synchronising.
+ *  - bf16 is IEEE bfloat16 (raw 16-bit storage); fp32 is IEEE binary32.
+ *    Internally everything is fp32; y is rounded to bf16 (nearest even) once.
+ *  - Geometry: Hk key heads, Hv value heads (Hv % Hk == 0, G = Hv/Hk <= 8),
+ *    d_k == d_v in {32, 64, 128}, conv width 4.  CH = 2*Hk*d_k + Hv*d_v is
+ *    the number of conv channels, laid out [q | k | v], head-major inside
+ *    each block.  Value head h reads key head h / G.
+ *  - State tiles are [d_v, d_k] fp32, row-major (row = value channel).
+ *  - The conv tail of a slot is [3, CH] bf16: the three previous pre-conv
+ *    inputs of its stream, oldest first.  Conv tap w[c][3] multiplies the
+ *    current row, w[c][0] the input three rows back.  No conv bias.
+ *  - Every pointer must be 16-byte aligned (GDN_EALIGN otherwise), except
+ *    a, b, slot, row_ptr, parent, keep_row, cu_seqlens (4-byte / element
+ *    alignment).
+ *  - Errors: every size, geometry and pointer is validated on the host
+ *    BEFORE anything is enqueued; an error return leaves every buffer
+ *    untouched.  Device-resident indices (slot, row_ptr, parent, keep_row,
+ *    cu_seqlens) are checked by the kernels: an out-of-range value sets a
+ *    bit in the device error word (read with gdn_get_device_error) and the
+ *    affected stream is skipped (its outputs are left unwritten).
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define GDN_OK          0
+#define GDN_EINVAL     -1   /* a size or geometry outside the supported set */
+#define GDN_ENULL      -2   /* a required pointer is NULL */
+#define GDN_EALIGN     -3   /* a pointer misses its required alignment */
+#define GDN_ECUDA      -4   /* the CUDA runtime refused the launch */
+#define GDN_EWORKSPACE -5   /* workspace missing or smaller than required */
+
+/* ---- device error word bits (gdn_get_device_error) --------------------- */
+#define GDN_DERR_SLOT      1   /* slot[s] outside [0, n_slots) */
+#define GDN_DERR_ROWS      2   /* row_ptr not monotone, > n_rows, or > 16 rows */
+#define GDN_DERR_PARENT    4   /* parent[i] outside [-1, i) (window-local) */
+#define GDN_DERR_KEEP      8   /* keep_row[s] outside [-1, n_rows) */
+#define GDN_DERR_SEQLENS  16   /* cu_seqlens not monotone or > n_tokens */
+
+#define GDN_MAX_WINDOW 16      /* rows per stream in one window or tree */
+
+typedef struct {
+    int32_t n_k_heads;  /* Hk */
+    int32_t n_v_heads;  /* Hv, a multiple of Hk, Hv / Hk <= 8 */
+    int32_t d_k;        /* key head width, equal to d_v, in {32, 64, 128} */
+    int32_t d_v;        /* value head width */
+    int32_t conv_width; /* must be 4 */
+    float q_scale;      /* q is multiplied by this after its L2 norm */
+    float eps_l2;       /* q, k <- x / sqrt(sum x^2 + eps_l2) */
+    float eps_rms;      /* RMSNorm: o / sqrt(mean o^2 + eps_rms) */
+} gdn_dims;
+
+typedef struct {
+    const void *conv_w;    /* device, bf16 [CH, 4] */
+    const float *A_log;    /* device, fp32 [Hv] */
+    const float *dt_bias;  /* device, fp32 [Hv] */
+    const void *norm_w;    /* device, bf16 [d_v], shared by all heads */
+} gdn_weights;
+
+typedef struct {
+    float *state;          /* device, fp32 [n_slots, Hv, d_v, d_k] committed states */
+    void *tail;            /* device, bf16 [n_slots, 3, CH] committed conv tails */
+    int32_t n_slots;
+} gdn_cache;
+
+typedef struct {
+    const void *mixed;     /* device, bf16 [R, CH] conv inputs (in_proj q|k|v) */
+    const void *z;         /* device, bf16 [R, Hv, d_v] output gate */
+    const void *a;         /* device, bf16 [R, Hv] decay input */
+    const void *b;         /* device, bf16 [R, Hv] beta input */
+    void *y;               /* device, bf16 [R, Hv, d_v] output */
+} gdn_rows;
+
+/*
+ * gdn_step -- one row per stream, in place ([P932] tree note: one-row steps
+ * update in place).  Row s of `rows` belongs to stream s and advances the
+ * committed state and tail of slot[s]; y[s] is written.
+ *   slot      device int32 [n_streams], distinct values in [0, n_slots)
+ *   n_streams >= 1 (<= 65535)
+ * Launch: one CTA per (value head, stream), clusters of G CTAs.
+ */
+int gdn_step(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
+             const int32_t *slot, int32_t n_streams, const gdn_rows *rows,
+             void *stream);
+
+/*
+ * gdn_window -- chain verify windows of up to 16 rows per stream, recorded
+ * row by row ([P932] "Windows of up to 16 rows record each row's recurrence
+ * and convolution tail"; [P747] shared rounds of up to 16 streams of 16
+ * rows).  Stream s owns packed rows [row_ptr[s], row_ptr[s+1]) of `rows`;
+ * its first row follows the committed state and tail of slot[s], each later
+ * row the row before it.  The committed slot is NOT modified.
+ *   slot       device int32 [n_streams]
+ *   row_ptr    device int32 [n_streams + 1], non-decreasing, row_ptr[s+1] -
+ *              row_ptr[s] <= 16, row_ptr[n_streams] <= n_rows; a stream with
+ *              no rows is skipped
+ *   n_rows     R, rows in the packed buffers (>= 1)
+ *   rec_state  device fp32 [R, Hv, d_v, d_k]: the state after each row
+ *   rec_tail   device bf16 [R, 3, CH]: the tail after each row (the three
+ *              newest conv inputs along the row's branch, oldest first)
+ * Row r of y, rec_state and rec_tail equals, bit for bit, what gdn_step
+ * would produce for that row from the state and tail it follows.
+ */
+int gdn_window(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
+               const int32_t *slot, const int32_t *row_ptr, int32_t n_streams,
+               int32_t n_rows, const gdn_rows *rows, float *rec_state,
+               void *rec_tail, void *stream);
+
+/*
+ * gdn_tree -- tree verify windows ([P932] "A verify window's rows may form
+ * a tree (each row's parent given): the convolution taps, the delta rule
+ * and attention follow each row's own branch").  As gdn_window, plus
+ *   parent  device int32 [n_rows]: for packed row r of stream s, the
+ *           window-local index (0-based within the stream's rows) of its
+ *           parent, which must be smaller than its own index, or -1 for a
+ *           row that follows the committed slot.
+ * A row whose parent is the row before it continues from registers; any
+ * other parent's state is re-read from rec_state.  A node's outputs equal
+ * gdn_window's on the chain of rows along its root-to-node path.
+ */
+int gdn_tree(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
+             const int32_t *slot, const int32_t *row_ptr, const int32_t *parent,
+             int32_t n_streams, int32_t n_rows, const gdn_rows *rows,
+             float *rec_state, void *rec_tail, void *stream);
+
+/*
+ * gdn_commit -- keep each stream's accepted path ([P747] "commit only each
+ * stream's accepted path"; [P932] recorded rows "keep partial copies").
+ * For stream s with keep_row[s] = r >= 0 (a packed row index, normally the
+ * last accepted row of the stream's window or the chosen tree node),
+ * slot[s]'s state and tail become rec_state[r] and rec_tail[r].
+ * keep_row[s] = -1 (nothing accepted) leaves the slot bit-unchanged.
+ *   slot       device int32 [n_streams], distinct
+ *   keep_row   device int32 [n_streams], each in [-1, n_rows)
+ *   rec_state, rec_tail  as written by gdn_window / gdn_tree
+ */
+int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot,
+               const int32_t *keep_row, int32_t n_streams, int32_t n_rows,
+               const float *rec_state, const void *rec_tail, void *stream);
+
+/* Text for a status code (static storage). */
+const char *gdn_status_string(int status);
+
+/*
+ * Reads and clears the calling device's error word on `stream` (this call
+ * synchronises that stream).  *bits receives the OR of GDN_DERR_* flags
+ * raised since the last read.  Returns GDN_OK or GDN_ECUDA.
+ */
+int gdn_get_device_error(void *stream, int32_t *bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */
