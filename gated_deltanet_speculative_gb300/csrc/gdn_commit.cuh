@@ -40,7 +40,21 @@ __global__ void __launch_bounds__(kCommitThreads) gdn_commit_kernel(const Commit
     const size_t tile4 = (size_t)p.D * p.D / 4;
     const float4 *src = reinterpret_cast<const float4 *>(p.rec_state) + ((size_t)kr * p.Hv + h) * tile4;
     float4 *dst = reinterpret_cast<float4 *>(p.state) + ((size_t)sl * p.Hv + h) * tile4;
-    for (size_t i = threadIdx.x; i < tile4; i += kCommitThreads) dst[i] = __ldcs(src + i);
+    // 8 loads in flight per thread before the first store
+    constexpr int kUnroll = 8;
+    for (size_t base = 0; base < tile4; base += (size_t)kUnroll * kCommitThreads) {
+        float4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const size_t i = base + (size_t)u * kCommitThreads + threadIdx.x;
+            if (i < tile4) v[u] = __ldcs(src + i);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const size_t i = base + (size_t)u * kCommitThreads + threadIdx.x;
+            if (i < tile4) dst[i] = v[u];
+        }
+    }
 
     // this CTA's share of the tail, in 16-byte units (3*CH*2 is a multiple of 16)
     const size_t units = (size_t)3 * p.CH / 8;

@@ -56,21 +56,37 @@ constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kMaxRows = GDN_MAX_WINDOW;
 
 template <int D>
-struct RowSmem {
+struct __align__(16) RowSmem {
     float q[kMaxRows][D];
     float k[kMaxRows][D];
     float v[kMaxRows][D];
-    float o[kMaxRows][D];
+    union {
+        // staged bf16 conv inputs of this head's q | k | v channels: rows 0..2
+        // are the committed tail (oldest first), row 3 + t is window row t
+        uint16_t xin[kMaxRows + 3][3 * D];
+        float o[kMaxRows][D];   // written by the recurrence, after the conv
+    } u;
+    uint16_t z[kMaxRows][D];
     float decay[kMaxRows];
     float beta[kMaxRows];
     float kq[kMaxRows];
-    // conv ancestors m = 1, 2, 3 steps back along the branch: >= 0 is a
-    // window-local row, e < 0 is row 3 + e of the committed tail
+    // conv ancestors m = 1, 2, 3 steps back along the branch: e >= 0 is a
+    // window-local row, e < 0 is row 3 + e of the committed tail; either way
+    // the ancestor's staged row is 3 + e
     int anc[kMaxRows][3];
     int parent[kMaxRows];
     int reused[kMaxRows];   // tree: re-read later by a non-adjacent child
-    int slot, r0, n;
+    int bad;
 };
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const unsigned sa = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;\n" ::: "memory");
+}
 
 template <int CPL>
 __device__ __forceinline__ void load_cols(float (&x)[CPL], const float *src) {
@@ -130,6 +146,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
     constexpr int CPL = D / 32;                   // state columns per lane
     constexpr int NV = 2 * RPW;                   // partial sums per lane: S k and S q
     constexpr int SHIFT = 5 - Log2<NV>::value;    // lane l holds total (l >> SHIFT)
+    constexpr int SEG = D * 2 / 16;               // 16-byte chunks in one q, k or v segment
+    constexpr int CHUNKS = 3 * SEG;               // 16-byte chunks in a staged row
     static_assert(NV >= 2 && NV <= 32, "unsupported head width");
 
     __shared__ RowSmem<D> sm;
@@ -137,108 +155,133 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kh = h / p.G;
     const size_t CH = (size_t)p.CH;
+    const bool lead = (h % p.G) == 0;    // this CTA writes the q/k channels shared by its key-head group
 
-    // ---- a1: the stream's rows, each row's parent and conv ancestors -------
+    // ---- a1: the stream's slot and rows (the same few words in every thread)
+    const int sl = __ldg(p.slot + s);
+    int r0 = s, n = 1;
+    if (MODE != kStep) {
+        r0 = __ldg(p.row_ptr + s);
+        n = __ldg(p.row_ptr + s + 1) - r0;
+    }
+    {
+        int bad = (sl < 0 || sl >= p.n_slots) ? GDN_DERR_SLOT : 0;
+        if (MODE != kStep && (r0 < 0 || n < 0 || n > kMaxRows || r0 > p.n_rows - n)) bad |= GDN_DERR_ROWS;
+        if (bad || n == 0) {   // uniform over the CTA and over its cluster (same stream)
+            if (bad && h == 0 && tid == 0) raise_error(p.err, bad);
+            return;
+        }
+    }
+
+    // The committed state tile goes to registers; the loads stay in flight
+    // while the conv inputs are staged and processed.
+    const size_t tile = (size_t)D * D;
+    float *slot_tile = p.state + ((size_t)sl * p.Hv + h) * tile;
+    float S[RPW][CPL];
+    load_tile<D, RPW, CPL>(S, slot_tile, warp, lane);
+
+    // Stage the committed tail and the window's rows (this head's q | k | v
+    // channels) and the z rows into shared memory, 16 bytes per copy.
+    const uint16_t *tail = p.tail + (size_t)sl * 3 * CH;
+    for (int i = tid; i < (n + 3) * CHUNKS; i += kRowThreads) {
+        const int row = i / CHUNKS, ch = i - row * CHUNKS;
+        const int part = ch / SEG, off = (ch - part * SEG) * 8;
+        const int c = channel_of<D>(part, off, p.Hk, kh, h);
+        const uint16_t *src = row < 3 ? tail + (size_t)row * CH + c : p.mixed + (size_t)(r0 + row - 3) * CH + c;
+        cp_async16(&sm.u.xin[row][part * D + off], src);
+    }
+    for (int i = tid; i < n * SEG; i += kRowThreads) {
+        const int t = i / SEG, ch = i - t * SEG;
+        cp_async16(&sm.z[t][ch * 8], p.z + ((size_t)(r0 + t) * p.Hv + h) * D + ch * 8);
+    }
+    if (MODE == kTree && tid < n) sm.parent[tid] = __ldg(p.parent + r0 + tid);
+    cp_async_wait_all();
+    __syncthreads();
+
+    // ---- each row's parent and conv ancestors along its branch -------------
     if (tid == 0) {
         int bad = 0;
-        const int sl = p.slot[s];
-        if (sl < 0 || sl >= p.n_slots) bad |= GDN_DERR_SLOT;
-        int r0 = s, n = 1;
-        if (MODE != kStep) {
-            r0 = p.row_ptr[s];
-            const int r1 = p.row_ptr[s + 1];
-            n = r1 - r0;
-            if (r0 < 0 || r1 > p.n_rows || n < 0 || n > kMaxRows) bad |= GDN_DERR_ROWS;
+        for (int t = 0; t < n; ++t) {
+            const int par = MODE == kTree ? sm.parent[t] : t - 1;
+            if (par < -1 || par >= t) bad = GDN_DERR_PARENT;
+            sm.parent[t] = par;
+            sm.reused[t] = 0;
         }
-        if (!bad) {
-            for (int t = 0; t < n; ++t) {
-                int par = t - 1;
-                if (MODE == kTree) {
-                    par = p.parent[r0 + t];
-                    if (par < -1 || par >= t) {
-                        bad |= GDN_DERR_PARENT;
-                        break;
-                    }
+        for (int t = 0; t < n && !bad; ++t) {
+            int node = t, tail_next = 2;
+            for (int m = 0; m < 3; ++m) {
+                if (node >= 0) node = sm.parent[node];
+                if (node >= 0) {
+                    sm.anc[t][m] = node;
+                } else {
+                    sm.anc[t][m] = tail_next - 3;
+                    --tail_next;
                 }
-                sm.parent[t] = par;
-                sm.reused[t] = 0;
             }
+            if (MODE == kTree && sm.parent[t] >= 0 && sm.parent[t] != t - 1) sm.reused[sm.parent[t]] = 1;
         }
-        if (!bad) {
-            for (int t = 0; t < n; ++t) {
-                int node = t, tail_next = 2;
-                for (int m = 0; m < 3; ++m) {
-                    if (node >= 0) node = sm.parent[node];
-                    if (node >= 0) {
-                        sm.anc[t][m] = node;
-                    } else {
-                        sm.anc[t][m] = tail_next - 3;
-                        --tail_next;
-                    }
-                }
-                if (MODE == kTree && sm.parent[t] >= 0 && sm.parent[t] != t - 1) sm.reused[sm.parent[t]] = 1;
-            }
-        }
-        if (bad) {
-            if (h == 0) raise_error(p.err, bad);
-            n = 0;
-        }
-        sm.slot = sl;
-        sm.r0 = r0;
-        sm.n = n;
+        if (bad && h == 0) raise_error(p.err, bad);
+        sm.bad = bad;
     }
     __syncthreads();
-    const int n = sm.n;
-    if (n == 0) return;   // uniform over the CTA and over its cluster (same stream)
-    const int sl = sm.slot, r0 = sm.r0;
-    const bool lead = (h % p.G) == 0;   // this CTA records the shared q/k tail channels
-    const uint16_t *tail = p.tail + (size_t)sl * 3 * CH;
+    if (sm.bad) return;
 
-    // ---- a2: conv over the branch's four taps, then SiLU --------------------
-    for (int idx = tid; idx < n * 3 * D; idx += kRowThreads) {
-        const int t = idx / (3 * D);
-        const int cc = idx - t * 3 * D;
-        const int part = cc / D;
-        const int e = cc - part * D;
+    // ---- a2: conv over the branch's four taps, then SiLU (4 channels each) --
+    for (int i = tid; i < n * (3 * D / 4); i += kRowThreads) {
+        const int t = i / (3 * D / 4);
+        const int cc = (i - t * (3 * D / 4)) * 4;
+        const int part = cc / D, e = cc - part * D;
         const int c = channel_of<D>(part, e, p.Hk, kh, h);
-        uint16_t x[4];   // oldest first; x[3] is the row itself
-        x[3] = p.mixed[(size_t)(r0 + t) * CH + c];
+        const uint4 *wp = reinterpret_cast<const uint4 *>(p.conv_w + (size_t)c * 4);
+        const uint4 wa = __ldg(wp), wb = __ldg(wp + 1);
+        const uint32_t wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+        // taps, oldest first: 3, 2 and 1 steps back along the branch, then the row
+        const uint2 x0 = *reinterpret_cast<const uint2 *>(&sm.u.xin[3 + sm.anc[t][2]][cc]);
+        const uint2 x1 = *reinterpret_cast<const uint2 *>(&sm.u.xin[3 + sm.anc[t][1]][cc]);
+        const uint2 x2 = *reinterpret_cast<const uint2 *>(&sm.u.xin[3 + sm.anc[t][0]][cc]);
+        const uint2 x3 = *reinterpret_cast<const uint2 *>(&sm.u.xin[3 + t][cc]);
+        float *dst = part == 0 ? &sm.q[t][e] : (part == 1 ? &sm.k[t][e] : &sm.v[t][e]);
 #pragma unroll
-        for (int m = 0; m < 3; ++m) {
-            const int an = sm.anc[t][m];
-            x[2 - m] = an >= 0 ? p.mixed[(size_t)(r0 + an) * CH + c] : tail[(size_t)(3 + an) * CH + c];
+        for (int j = 0; j < 4; ++j) {
+            const int sh = (j & 1) * 16;
+            const uint32_t a0 = (j < 2 ? x0.x : x0.y) >> sh, a1 = (j < 2 ? x1.x : x1.y) >> sh;
+            const uint32_t a2 = (j < 2 ? x2.x : x2.y) >> sh, a3 = (j < 2 ? x3.x : x3.y) >> sh;
+            float acc = __fmul_rn(bf_bits(wv[2 * j] & 0xffffu), bf_bits(a0 & 0xffffu));
+            acc = __fmaf_rn(bf_bits(wv[2 * j] >> 16), bf_bits(a1 & 0xffffu), acc);
+            acc = __fmaf_rn(bf_bits(wv[2 * j + 1] & 0xffffu), bf_bits(a2 & 0xffffu), acc);
+            acc = __fmaf_rn(bf_bits(wv[2 * j + 1] >> 16), bf_bits(a3 & 0xffffu), acc);
+            dst[j] = silu(acc);
         }
-        const uint2 wv = *reinterpret_cast<const uint2 *>(p.conv_w + (size_t)c * 4);
-        float acc = __fmul_rn(bf_bits(wv.x & 0xffffu), bf_bits(x[0]));
-        acc = __fmaf_rn(bf_bits(wv.x >> 16), bf_bits(x[1]), acc);
-        acc = __fmaf_rn(bf_bits(wv.y & 0xffffu), bf_bits(x[2]), acc);
-        acc = __fmaf_rn(bf_bits(wv.y >> 16), bf_bits(x[3]), acc);
-        const float act = silu(acc);
-        if (part == 0) sm.q[t][e] = act;
-        else if (part == 1) sm.k[t][e] = act;
-        else sm.v[t][e] = act;
-        if (MODE != kStep && (part == 2 || lead)) {   // a6: the row's tail
-            uint16_t *rt = p.rec_tail + (size_t)(r0 + t) * 3 * CH + c;
-            rt[0] = x[1];
-            rt[CH] = x[2];
-            rt[2 * CH] = x[3];
+    }
+    // ---- a6 (tail): the three newest inputs after each row, oldest first ----
+    const int own_lo = lead ? 0 : 2 * SEG;   // chunks this CTA owns: v always, q/k if lead
+    const int per_row = CHUNKS - own_lo;
+    if (MODE != kStep) {
+        for (int i = tid; i < n * 3 * per_row; i += kRowThreads) {
+            const int t = i / (3 * per_row);
+            const int rem = i - t * 3 * per_row;
+            const int m = rem / per_row;
+            const int ch = own_lo + rem - m * per_row;
+            const int src_row = m == 2 ? 3 + t : 3 + sm.anc[t][1 - m];
+            const int part = ch / SEG, off = (ch - part * SEG) * 8;
+            const int c = channel_of<D>(part, off, p.Hk, kh, h);
+            *reinterpret_cast<uint4 *>(p.rec_tail + ((size_t)(r0 + t) * 3 + m) * CH + c) =
+                *reinterpret_cast<const uint4 *>(&sm.u.xin[src_row][part * D + off]);
         }
     }
     __syncthreads();
 
     if (MODE == kStep) {
-        // Every CTA of this key-head group has read the old tail; now shift it
-        // in place: the lead CTA moves the shared q/k channels, each CTA its v.
+        // Every CTA of this key-head group has staged the old tail; now shift
+        // it in place: the lead CTA moves the shared q/k channels, each CTA its v.
         cluster_sync_all();
-        for (int cc = tid; cc < 3 * D; cc += kRowThreads) {
-            const int part = cc / D;
-            if (part < 2 && !lead) continue;
-            const int c = channel_of<D>(part, cc - part * D, p.Hk, kh, h);
-            uint16_t *tl = p.tail + (size_t)sl * 3 * CH + c;
-            const uint16_t t1 = tl[CH], t2 = tl[2 * CH];
-            tl[0] = t1;
-            tl[CH] = t2;
-            tl[2 * CH] = p.mixed[(size_t)s * CH + c];
+        for (int i = tid; i < 3 * per_row; i += kRowThreads) {
+            const int m = i / per_row;
+            const int ch = own_lo + i - m * per_row;
+            const int part = ch / SEG, off = (ch - part * SEG) * 8;
+            const int c = channel_of<D>(part, off, p.Hk, kh, h);
+            *reinterpret_cast<uint4 *>(p.tail + ((size_t)sl * 3 + m) * CH + c) =
+                *reinterpret_cast<const uint4 *>(&sm.u.xin[m + 1][part * D + off]);
         }
     }
 
@@ -265,12 +308,6 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         sm.decay[tid] = expf(g);
         sm.beta[tid] = sigmoidf_rn(bin);
     }
-
-    // The committed state tile goes to registers while the norms finish.
-    const size_t tile = (size_t)D * D;
-    float *slot_tile = p.state + ((size_t)sl * p.Hv + h) * tile;
-    float S[RPW][CPL];
-    load_tile<D, RPW, CPL>(S, slot_tile, warp, lane);
     __syncthreads();
 
     for (int t = warp; t < n; t += kRowWarps) {   // k . q of each row
@@ -316,7 +353,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         if (lane < 16) u = __fmul_rn(bet, __fsub_rn(sm.v[t][warp * RPW + vi], __fmul_rn(dec, tot)));
         const float u_pair = __shfl_xor_sync(kFull, u, 16);
         if (lane >= 16 && (lane & ((1 << SHIFT) - 1)) == 0)
-            sm.o[t][warp * RPW + vi - RPW] = __fmaf_rn(u_pair, sm.kq[t], __fmul_rn(dec, tot));
+            sm.u.o[t][warp * RPW + vi - RPW] = __fmaf_rn(u_pair, sm.kq[t], __fmul_rn(dec, tot));
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
             const float ur = __shfl_sync(kFull, u, r << SHIFT);
@@ -335,7 +372,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
     for (int t = warp; t < n; t += kRowWarps) {
         float ov[CPL];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) ov[c] = sm.o[t][lane * CPL + c];
+        for (int c = 0; c < CPL; ++c) ov[c] = sm.u.o[t][lane * CPL + c];
         float ss = __fmul_rn(ov[0], ov[0]);
 #pragma unroll
         for (int c = 1; c < CPL; ++c) ss = __fmaf_rn(ov[c], ov[c], ss);
@@ -344,7 +381,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         const size_t base = ((size_t)(r0 + t) * p.Hv + h) * D + lane * CPL;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
-            const float zz = bf_bits(p.z[base + c]);
+            const float zz = bf_bits(sm.z[t][lane * CPL + c]);
             const float wn = bf_bits(p.norm_w[lane * CPL + c]);
             const float yv = __fmul_rn(__fmul_rn(__fmul_rn(ov[c], inv), wn), silu(zz));
             p.y[base + c] = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
