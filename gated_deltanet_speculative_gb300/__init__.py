@@ -1,12 +1,12 @@
 """GB300-native gated-DeltaNet speculative verify path.
 
 The C ABI of include/gdn.h (libgdn.so, hand-written sm_103a kernels) behind a
-thin ctypes binding: ``step``, ``window``, ``tree``, ``commit`` and
-``get_device_error`` take torch CUDA tensors and enqueue on the current
+thin ctypes binding: ``step``, ``window``, ``tree``, ``commit``,
+``prefill`` and ``get_device_error`` take torch CUDA tensors and enqueue on the current
 stream.  ``synth`` draws the seeded synthetic inputs.  Importing the package
 does not load the CUDA library; the first call does (and raises if it is
 missing).
 """
 from . import synth  # noqa: F401
-from ._binding import (Dims, GdnError, MAX_WINDOW, commit, get_device_error, load,  # noqa: F401
-                       library_path, step, tree, window)
+from ._binding import (Dims, GdnError, MAX_WINDOW, PREFILL_CHUNK, commit, get_device_error,  # noqa: F401
+                       library_path, load, prefill, prefill_workspace_size, step, tree, window)

@@ -60,6 +60,9 @@ _SIGS = {
     "gdn_tree": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _P, _I, _I,
                  ctypes.POINTER(c_rows), _P, _P, _P],
     "gdn_commit": [ctypes.POINTER(c_dims), ctypes.POINTER(c_cache), _P, _P, _I, _I, _P, _P, _P],
+    "gdn_prefill": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _I, _I,
+                    ctypes.POINTER(c_rows), _I, _P, ctypes.c_size_t, _P],
+    "gdn_prefill_workspace_size": [ctypes.POINTER(c_dims), _I, _I, _I],
     "gdn_status_string": [ctypes.c_int],
     "gdn_get_device_error": [_P, ctypes.POINTER(ctypes.c_int32)],
 }
@@ -81,7 +84,8 @@ def load(build_if_missing: bool = True):
             for name, argtypes in _SIGS.items():
                 fn = getattr(lib, name)
                 fn.argtypes = argtypes
-                fn.restype = ctypes.c_char_p if name == "gdn_status_string" else ctypes.c_int
+                fn.restype = {"gdn_status_string": ctypes.c_char_p,
+                              "gdn_prefill_workspace_size": ctypes.c_size_t}.get(name, ctypes.c_int)
             _lib = lib
     return _lib
 
@@ -211,6 +215,32 @@ def commit(dims: Dims, cache: dict, slot, keep_row, rec_state, rec_tail, stream=
     _need(rec_tail, "rec_tail", torch.bfloat16, (R, 3, dims.channels))
     _check("gdn_commit", lib.gdn_commit(ctypes.byref(dims.c()), ctypes.byref(cc), _ptr(slot), _ptr(keep_row), S, R,
                                         _ptr(rec_state), _ptr(rec_tail), _stream_ptr(stream)))
+
+
+PREFILL_CHUNK = 64
+
+
+def prefill_workspace_size(dims: Dims, n_seqs: int, n_tokens: int, chunk: int = PREFILL_CHUNK) -> int:
+    """Bytes of scratch gdn_prefill needs (0 for invalid sizes)."""
+    return int(load().gdn_prefill_workspace_size(ctypes.byref(dims.c()), int(n_seqs), int(n_tokens), int(chunk)))
+
+
+def prefill(dims: Dims, weights: dict, cache: dict, slot, cu_seqlens, rows: dict, workspace, chunk: int = PREFILL_CHUNK,
+            stream=None):
+    """Chunked prompt prefill of packed sequences; slots advanced in place.
+
+    ``workspace`` is a CUDA uint8 tensor of at least
+    ``prefill_workspace_size(dims, n_seqs, n_tokens)`` bytes."""
+    lib = load()
+    _need(slot, "slot", torch.int32)
+    S = slot.numel()
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (S + 1,))
+    T = rows["mixed"].shape[0]
+    cw, cc, cr = _weights(dims, weights), _cache(dims, cache), _rows(dims, rows, T)
+    _need(workspace, "workspace", torch.uint8)
+    _check("gdn_prefill", lib.gdn_prefill(ctypes.byref(dims.c()), ctypes.byref(cw), ctypes.byref(cc), _ptr(slot),
+                                          _ptr(cu_seqlens), S, T, ctypes.byref(cr), int(chunk), _ptr(workspace),
+                                          workspace.numel(), _stream_ptr(stream)))
 
 
 def get_device_error(stream=None) -> int:

@@ -7,6 +7,7 @@
 
 #include "gdn_commit.cuh"
 #include "gdn_launch.h"
+#include "gdn_prefill_launch.h"
 
 namespace {
 
@@ -187,6 +188,66 @@ int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot
     const dim3 grid(p.Hv, n_streams);
     gdn::gdn_commit_kernel<<<grid, gdn::kCommitThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ECUDA;
+}
+
+size_t gdn_prefill_workspace_size(const gdn_dims *dims, int32_t n_seqs, int32_t n_tokens, int32_t chunk) {
+    if (check_dims(dims) != GDN_OK || n_seqs <= 0 || n_tokens <= 0 || n_tokens > (1 << 22) ||
+        chunk != gdn::kPrefillChunk)
+        return 0;
+    const size_t max_chunks = (size_t)n_tokens / chunk + (size_t)n_seqs;
+    const size_t floats = max_chunks * dims->n_v_heads * gdn::prefill_chunk_floats(dims->d_k) +
+                          (size_t)n_tokens * dims->n_v_heads * dims->d_v;
+    return floats * sizeof(float);
+}
+
+int gdn_prefill(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
+                const int32_t *cu_seqlens, int32_t n_seqs, int32_t n_tokens, const gdn_rows *rows, int32_t chunk,
+                void *workspace, size_t workspace_bytes, void *stream) {
+    GDN_TRY(check_dims(dims));
+    GDN_TRY(check_weights(w));
+    GDN_TRY(check_cache(cache));
+    GDN_TRY(check_rows(rows));
+    if (!slot || !cu_seqlens) return GDN_ENULL;
+    if (n_seqs <= 0 || n_seqs > 65535 || n_tokens <= 0 || n_tokens > (1 << 22) || chunk != gdn::kPrefillChunk)
+        return GDN_EINVAL;
+    if (!aligned(slot, 4) || !aligned(cu_seqlens, 4)) return GDN_EALIGN;
+    const size_t need = gdn_prefill_workspace_size(dims, n_seqs, n_tokens, chunk);
+    if (!workspace || workspace_bytes < need) return GDN_EWORKSPACE;
+    if (!aligned(workspace, 16)) return GDN_EALIGN;
+    const size_t max_chunks = (size_t)n_tokens / chunk + (size_t)n_seqs;
+    if (max_chunks > 65535) return GDN_EINVAL;
+    int *err = error_word();
+    if (!err) return GDN_ECUDA;
+    gdn::PrefillParams p = {};
+    p.Hk = dims->n_k_heads;
+    p.Hv = dims->n_v_heads;
+    p.G = dims->n_v_heads / dims->n_k_heads;
+    p.CH = 2 * dims->n_k_heads * dims->d_k + dims->n_v_heads * dims->d_v;
+    p.q_scale = dims->q_scale;
+    p.eps_l2 = dims->eps_l2;
+    p.eps_rms = dims->eps_rms;
+    p.conv_w = static_cast<const uint16_t *>(w->conv_w);
+    p.A_log = w->A_log;
+    p.dt_bias = w->dt_bias;
+    p.norm_w = static_cast<const uint16_t *>(w->norm_w);
+    p.state = cache->state;
+    p.tail = static_cast<uint16_t *>(cache->tail);
+    p.n_slots = cache->n_slots;
+    p.mixed = static_cast<const uint16_t *>(rows->mixed);
+    p.z = static_cast<const uint16_t *>(rows->z);
+    p.a = static_cast<const uint16_t *>(rows->a);
+    p.b = static_cast<const uint16_t *>(rows->b);
+    p.y = static_cast<uint16_t *>(rows->y);
+    p.slot = slot;
+    p.cu_seqlens = cu_seqlens;
+    p.n_seqs = n_seqs;
+    p.n_tokens = n_tokens;
+    p.max_chunks = (int)max_chunks;
+    p.ws_chunks = static_cast<float *>(workspace);
+    p.ws_out = p.ws_chunks + max_chunks * dims->n_v_heads * gdn::prefill_chunk_floats(dims->d_k);
+    p.err = err;
+    return gdn::launch_prefill(dims->d_k, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK
+                                                                                               : GDN_ECUDA;
 }
 
 const char *gdn_status_string(int status) {

@@ -183,6 +183,36 @@ int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot
                const int32_t *keep_row, int32_t n_streams, int32_t n_rows,
                const float *rec_state, const void *rec_tail, void *stream);
 
+/*
+ * gdn_prefill -- chunked prompt prefill ([P747] "prompt chain" kernel and
+ * prompts that "arrive together share one prefill pass"; [P932] tree note:
+ * prompts update in place).  Sequence s owns packed tokens
+ * [cu_seqlens[s], cu_seqlens[s+1]) of `rows`; it starts from slot[s]'s
+ * committed state and tail (zero them for a fresh prompt; a nonzero state
+ * resumes a kept one) and leaves the state and tail after its last token
+ * in the slot.  y is written for every token.  The result equals running
+ * the tokens through gdn_step one by one, up to fp32 rounding (the chunked
+ * form reorders the sums).
+ *   cu_seqlens  device int32 [n_seqs + 1], non-decreasing, last <= n_tokens;
+ *               empty sequences leave their slot untouched
+ *   n_tokens    rows in the packed buffers (>= 1, <= 2^22)
+ *   chunk       rows per chunk; must be 64
+ *   workspace   device scratch of at least gdn_prefill_workspace_size()
+ *               bytes, 16-byte aligned; its contents on entry do not
+ *               matter and are garbage on return; GDN_EWORKSPACE if absent
+ *               or too small
+ * Three launches on `stream`: prep (chunk x head), scan (sequence x head x
+ * d_v slice) and norm (token x head).
+ */
+int gdn_prefill(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
+                const int32_t *slot, const int32_t *cu_seqlens, int32_t n_seqs,
+                int32_t n_tokens, const gdn_rows *rows, int32_t chunk,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace gdn_prefill needs for these sizes (0 if invalid). */
+size_t gdn_prefill_workspace_size(const gdn_dims *dims, int32_t n_seqs, int32_t n_tokens,
+                                  int32_t chunk);
+
 /* Text for a status code (static storage). */
 const char *gdn_status_string(int status);
 

@@ -1,0 +1,128 @@
+"""GPU parity of the chunked prefill (gdn_prefill) against the oracle's
+sequential recurrence: every token's y, and the slot's final state and conv
+tail, for ragged packed prompts, resumed prompts, and the full prompt shapes
+(one 4722-token prompt; 512/1024/2048/4096 in one pass)."""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_speculative_gb300 as gdn
+import oracle
+from gated_deltanet_speculative_gb300 import synth
+
+from harness import Case, check_state, check_y, dev, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prefill(c: Case):
+    d = c.dims_gpu()
+    w, cache, rows = c.dev_weights(), c.dev_cache(), c.dev_rows()
+    ws = torch.empty(gdn.prefill_workspace_size(d, c.S, rows["mixed"].shape[0]), dtype=torch.uint8, device="cuda")
+    ws.fill_(0xff)   # NaN poison: the kernels must not read what they did not write
+    gdn.prefill(d, w, cache, dev(c.slots), dev(c.row_ptr), rows, ws)
+    assert gdn.get_device_error() == 0
+    return {"y": host_bits(rows["y"]), "state": cache["state"].cpu().numpy(), "tail": host_bits(cache["tail"])}
+
+
+def compare(c: Case, out, threads=16):
+    for s in range(c.S):
+        lo, hi = c.stream_rows(s)
+        sl = int(c.slots[s])
+        if hi == lo:
+            assert np.array_equal(out["state"][sl].view(np.uint32), c.cache["state"][sl].view(np.uint32))
+            assert np.array_equal(out["tail"][sl], c.cache["tail"][sl])
+            continue
+        r = c.rows
+        ref = oracle.gdn_rows(c.dims_oracle(), c.w, c.cache["state"][sl], c.cache["tail"][sl], r["mixed"][lo:hi],
+                              r["z"][lo:hi], r["a"][lo:hi], r["b"][lo:hi], record=False, final=True, threads=threads)
+        check_y(out["y"][lo:hi], ref["y"], what=f"prefill y seq {s}")
+        check_state(out["state"][sl], ref["final_state"], what=f"prefill state seq {s}")
+        assert np.array_equal(out["tail"][sl], ref["final_tail"]), f"prefill tail seq {s}"
+
+
+@pytest.mark.parametrize("g", [synth.Geometry(2, 4, 32, 32), synth.Geometry(2, 4, 64, 64),
+                               synth.Geometry(2, 6, 128, 128)])
+def test_prefill_ragged_prompts_resume_from_kept_state(g):
+    """Lengths around the chunk edges (1, 2, 3, 63, 64, 65, 130) and an empty
+    prompt, each starting from a nonzero kept state and tail."""
+    c = Case(g, [1, 2, 3, 0, 63, 64, 65, 130], seed=51, n_slots=10)
+    compare(c, run_prefill(c))
+
+
+def test_prefill_27b_heads_zero_state():
+    c = Case(synth.LIKE_27B, [200, 70, 1], seed=53, zero_state=True)
+    compare(c, run_prefill(c))
+
+
+def test_prefill_single_4722_token_prompt():
+    """One 4722-token prompt, 27B-like heads, chunk 64, zero initial state."""
+    c = Case(synth.LIKE_27B, [4722], seed=4, zero_state=True)
+    compare(c, run_prefill(c))
+
+
+def test_prefill_shared_pass_of_four_prompts():
+    """512 / 1024 / 2048 / 4096 tokens packed into one pass."""
+    c = Case(synth.LIKE_27B, [512, 1024, 2048, 4096], seed=4, zero_state=True)
+    compare(c, run_prefill(c))
+
+
+def test_prefill_split_at_chunk_and_off_chunk_points_matches_whole():
+    """A prompt prefilled in two passes (split at 64, then at 100) ends in the
+    same slot state as one pass over the whole prompt, to tolerance."""
+    g = synth.Geometry(2, 4, 128, 128)
+    whole = Case(g, [300], seed=57)
+    out_whole = run_prefill(whole)
+    for cut in (64, 100):
+        d = whole.dims_gpu()
+        w = whole.dev_weights()
+        cache = whole.dev_cache()
+        slot = dev(whole.slots)
+        for lo, hi in ((0, cut), (cut, 300)):
+            rows = {k: torch.from_numpy(np.ascontiguousarray(v[lo:hi]).view(np.int16)).view(torch.bfloat16).cuda()
+                    for k, v in whole.rows.items()}
+            rows["y"] = torch.empty((hi - lo, g.n_v_heads, g.d_v), dtype=torch.bfloat16, device="cuda")
+            ws = torch.empty(gdn.prefill_workspace_size(d, 1, hi - lo), dtype=torch.uint8, device="cuda")
+            gdn.prefill(d, w, cache, slot, dev(np.array([0, hi - lo], np.int32)), rows, ws)
+        sl = int(whole.slots[0])
+        check_state(cache["state"].cpu().numpy()[sl], out_whole["state"][sl].astype(np.float64),
+                    what=f"resume at {cut}")
+        assert np.array_equal(host_bits(cache["tail"])[sl], out_whole["tail"][sl])
+
+
+def test_prefill_matches_gpu_steps():
+    """Prefill of L tokens equals L one-row gdn_step calls, to tolerance."""
+    g = synth.Geometry(2, 4, 64, 64)
+    c = Case(g, [77], seed=59)
+    out = run_prefill(c)
+    d = c.dims_gpu()
+    w = c.dev_weights()
+    sl = int(c.slots[0])
+    cache = {"state": dev(c.cache["state"][sl:sl + 1]), "tail": torch.from_numpy(
+        c.cache["tail"][sl:sl + 1].view(np.int16)).view(torch.bfloat16).cuda()}
+    slot = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ys = []
+    for t in range(77):
+        rows = {k: torch.from_numpy(np.ascontiguousarray(v[t:t + 1]).view(np.int16)).view(torch.bfloat16).cuda()
+                for k, v in c.rows.items()}
+        rows["y"] = torch.empty((1, g.n_v_heads, g.d_v), dtype=torch.bfloat16, device="cuda")
+        gdn.step(d, w, cache, slot, rows)
+        ys.append(synth.bf16_bits_to_f32(host_bits(rows["y"]))[0])
+    # both sides are rounded to bf16: allow 2e-3 plus one ulp of the larger
+    y_steps = np.stack(ys).astype(np.float64)
+    y_pre = synth.bf16_bits_to_f32(out["y"][:77]).astype(np.float64)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.maximum(np.abs(y_pre), np.abs(y_steps)), 1e-30))) - 7)
+    assert np.all(np.abs(y_pre - y_steps) <= 2e-3 + ulp)
+    check_state(cache["state"].cpu().numpy()[0], out["state"][sl].astype(np.float64), what="prefill vs steps")
+
+
+def test_prefill_bad_seqlens_sets_error_and_skips():
+    g = synth.Geometry(2, 4, 32, 32)
+    c = Case(g, [10, 5], seed=61)
+    d = c.dims_gpu()
+    w, cache, rows = c.dev_weights(), c.dev_cache(), c.dev_rows()
+    ws = torch.empty(gdn.prefill_workspace_size(d, 2, 15), dtype=torch.uint8, device="cuda")
+    gdn.prefill(d, w, cache, dev(c.slots), dev(np.array([0, 10, 99], np.int32)), rows, ws)
+    assert gdn.get_device_error() & 16
+    with pytest.raises(gdn.GdnError):
+        gdn.prefill(d, w, cache, dev(c.slots), dev(c.row_ptr), rows, ws[:100])
