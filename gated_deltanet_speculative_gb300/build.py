@@ -17,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libgdn.so")
-SOURCES = ["gdn_api.cu", "gdn_rows_d32.cu", "gdn_rows_d64.cu", "gdn_rows_d128.cu", "gdn_prefill.cu"]
+SOURCES = ["gdn_api.cu", "gdn_rows_d32.cu", "gdn_rows_d64.cu", "gdn_rows_d128.cu", "gdn_prefill.cu",
+           "gdn_prefill_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-fmad=true", "-Xcompiler", "-fPIC",
                 "-I", os.path.join(ROOT, "include")]

@@ -213,6 +213,27 @@ int gdn_prefill(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cac
 size_t gdn_prefill_workspace_size(const gdn_dims *dims, int32_t n_seqs, int32_t n_tokens,
                                   int32_t chunk);
 
+/*
+ * gdn_prefill_noalloc -- gdn_prefill without a workspace argument, for
+ * callers that cannot allocate device memory (a host runtime whose pool owns
+ * the device, a serving loop that must not pay cudaMalloc's device-wide
+ * synchronisation, a plugin interface with no scratch argument).  The
+ * source pages have no counterpart to this entry point.
+ *   The scratch is a file-scope device array of
+ *   GDN_PREFILL_NOALLOC_SCRATCH_BYTES (64 MiB), reserved on every GPU where
+ *   the library's module is loaded until the process exits.  Sizes whose
+ *   gdn_prefill_workspace_size() exceeds it return GDN_EWORKSPACE before
+ *   anything is enqueued; other arguments are validated as in gdn_prefill.
+ *   The first call on a device looks up the array's device address (make it
+ *   before any stream capture).  All calls share the array: calls whose work
+ *   overlaps on the GPU race and must be serialised by the caller.  Nothing
+ *   in the array needs to start at zero.  No cudaMalloc or cudaFree is made.
+ */
+#define GDN_PREFILL_NOALLOC_SCRATCH_BYTES (64u << 20)
+int gdn_prefill_noalloc(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
+                        const int32_t *slot, const int32_t *cu_seqlens, int32_t n_seqs,
+                        int32_t n_tokens, const gdn_rows *rows, int32_t chunk, void *stream);
+
 /* Text for a status code (static storage). */
 const char *gdn_status_string(int status);
 
