@@ -173,6 +173,21 @@ def nvsmi_id(local_rank: int) -> str:
         return vis.split(",")[local_rank] if vis else str(local_rank)
 
 
+def rank_seed(rank: int) -> int:
+    """Each rank runs its own, independent round (weak scaling)."""
+    return SEED + 1000 * rank
+
+
+def reduce_max(values, world: int, device):
+    """Max over ranks of a few timings (the only cross-rank step; timing only)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
 # ---- our arm ---------------------------------------------------------------
 
 def run_ours(args, rank, world, local_rank):
@@ -183,7 +198,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     g = GEOM
     R = N_STREAMS * WINDOW
-    seed = SEED + 1000 * rank
+    seed = rank_seed(rank)
     w = synth.layer_weights(g, seed)
     cache = synth.slot_cache(g, N_STREAMS, seed)
     rows = synth.row_inputs(g, R, seed)
@@ -269,13 +284,14 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = sum(ev2[i][0].elapsed_time(ev2[i][1]) for i in range(K)) / K
     if gdn.get_device_error() != 0:
         raise RuntimeError("device error word set during the timed steps")
+    extra = None
+    if not args.no_extra and rank == 0:
+        del rec_state, rec_tail
+        extra = run_extra(dev, stream, flush)
+        if gdn.get_device_error() != 0:
+            raise RuntimeError("device error word set during the secondary measurements")
 
-    if world > 1:
-        t = torch.tensor([step_ms, e2e_ms, statistics.mean(win_ms)], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms, e2e_ms, win_avg = t.tolist()
-    else:
-        win_avg = statistics.mean(win_ms)
+    step_ms, e2e_ms, win_avg = reduce_max([step_ms, e2e_ms, statistics.mean(win_ms)], world, dev)
     if rank != 0:
         return None
 
@@ -317,7 +333,188 @@ def run_ours(args, rank, world, local_rank):
         "clocks": sampler.summary(t0, t1) if sampler else None,
         "wall_s": {"timed": t1 - t0, "e2e": t2 - t1},
     }
+    if extra is not None:
+        line["extra"] = extra
     return line
+
+
+# ---- secondary measurements: the other rows of the path ------------------
+
+def _bf(x):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+
+
+def _timed(fn, reps, stream, flush):
+    """Mean ms per call: CUDA events around each call, L2 flushed between calls."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        flush.fill_(3)
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / reps
+
+
+def prefill_flops(g: synth.Geometry, n_tokens: int, C: int = 64) -> float:
+    """KK^T, QK^T, W, U~, WS^T, QS^T, PU, U^T K per chunk-head (the C x C solve excluded)."""
+    d = g.d_k
+    per_chunk_head = 2 * (5 * C * C * d + 3 * C * d * d)
+    return n_tokens / C * g.n_v_heads * per_chunk_head
+
+
+def prefill_bytes(g: synth.Geometry, n_tokens: int, n_seqs: int) -> int:
+    row = (g.channels + 2 * g.n_v_heads * g.d_v + 2 * g.n_v_heads) * 2      # mixed, z, y, a, b
+    return n_tokens * row + n_seqs * 2 * (g.n_v_heads * g.d_v * g.d_k * 4 + 3 * g.channels * 2)
+
+
+def decode_bytes(g: synth.Geometry, n_streams: int) -> int:
+    per = 2 * g.n_v_heads * g.d_v * g.d_k * 4 + 2 * 3 * g.channels * 2 + \
+        (g.channels + 2 * g.n_v_heads * g.d_v + 2 * g.n_v_heads) * 2
+    return n_streams * per
+
+
+def run_extra(dev, stream, flush, reps=20, only=None):
+    out = {}
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    bf16 = float(peaks.get("bf16_tflops", 1950.0))
+    fp32_alu = 152 * 128 * 2 * 2.07e9 / 1e12   # FFMA peak at the max SM clock, TFLOP/s
+
+    if only in (None, "tree"):
+        out["tree_round_16x16"] = _extra_tree(dev, stream, flush, reps, hbm)
+    if only in (None, "decode"):
+        out["decode_24_layers_2b_like"] = _extra_decode(dev, stream, flush, reps, hbm)
+    if only in (None, "prefill"):
+        out["prefill_27b_like"] = _extra_prefill(dev, stream, flush, reps, hbm, bf16, fp32_alu)
+    return out
+
+
+def _extra_tree(dev, stream, flush, reps, hbm):
+    """Tree round: 16 streams x 16-node random trees, all nodes recorded."""
+    import torch
+    import gated_deltanet_speculative_gb300 as gdn
+    g = GEOM
+    R = N_STREAMS * WINDOW
+    w = synth.layer_weights(g, 3)
+    cache = synth.slot_cache(g, N_STREAMS, 3)
+    rows = synth.row_inputs(g, R, 3)
+    rng = np.random.default_rng([3, 9])
+    parent = np.concatenate([synth.random_tree(WINDOW, rng) for _ in range(N_STREAMS)]).astype(np.int32)
+    d = gdn.Dims(g.n_k_heads, g.n_v_heads, g.d_k, g.d_v)
+    dw = {"conv_w": _bf(w["conv_w"]).to(dev), "A_log": torch.from_numpy(w["A_log"]).to(dev),
+          "dt_bias": torch.from_numpy(w["dt_bias"]).to(dev), "norm_w": _bf(w["norm_w"]).to(dev)}
+    dc = {"state": torch.from_numpy(cache["state"]).to(dev), "tail": _bf(cache["tail"]).to(dev)}
+    dr = {k: _bf(rows[k]).to(dev) for k in ("mixed", "z", "a", "b")}
+    dr["y"] = torch.empty((R, g.n_v_heads, g.d_v), dtype=torch.bfloat16, device=dev)
+    rs = torch.empty((R, g.n_v_heads, g.d_v, g.d_k), dtype=torch.float32, device=dev)
+    rt = torch.empty((R, 3, g.channels), dtype=torch.bfloat16, device=dev)
+    slot_t = torch.arange(N_STREAMS, dtype=torch.int32, device=dev)
+    rp_t = torch.from_numpy(synth.row_ptr([WINDOW] * N_STREAMS)).to(dev)
+    par_t = torch.from_numpy(parent).to(dev)
+    ms = _timed(lambda: gdn.tree(d, dw, dc, slot_t, rp_t, par_t, dr, rs, rt, stream), reps, stream, flush)
+    wb = window_bytes(g, N_STREAMS, R)
+    return {"ms": ms, "rows_per_s": R / (ms * 1e-3), "algorithmic_gbs": wb / (ms * 1e-3) / 1e9,
+            "frac_hbm": wb / (ms * 1e-3) / 1e9 / hbm,
+            "note": "parent reloads of non-adjacent children are L2/HBM re-reads, not counted"}
+
+
+def _extra_decode(dev, stream, flush, reps, hbm):
+    """Decode: 24 independent 2B-like layers stepped in order, one row per stream."""
+    import torch
+    import gated_deltanet_speculative_gb300 as gdn
+    g2 = synth.LIKE_2B
+    d2 = gdn.Dims(g2.n_k_heads, g2.n_v_heads, g2.d_k, g2.d_v)
+    dec = {}
+    for S in (1, 4, 8, 16):
+        layers = []
+        for layer in range(24):
+            w = synth.layer_weights(g2, 1 + 100 * layer)
+            cache = synth.slot_cache(g2, S, 1 + 100 * layer)
+            rows = synth.row_inputs(g2, S, 1 + 100 * layer)
+            lw = {"conv_w": _bf(w["conv_w"]).to(dev), "A_log": torch.from_numpy(w["A_log"]).to(dev),
+                  "dt_bias": torch.from_numpy(w["dt_bias"]).to(dev), "norm_w": _bf(w["norm_w"]).to(dev)}
+            lc = {"state": torch.from_numpy(cache["state"]).to(dev), "tail": _bf(cache["tail"]).to(dev)}
+            lr = {k: _bf(rows[k]).to(dev) for k in ("mixed", "z", "a", "b")}
+            lr["y"] = torch.empty((S, g2.n_v_heads, g2.d_v), dtype=torch.bfloat16, device=dev)
+            layers.append((lw, lc, lr))
+        sl = torch.arange(S, dtype=torch.int32, device=dev)
+
+        def step24():
+            for lw, lc, lr in layers:
+                gdn.step(d2, lw, lc, sl, lr, stream)
+
+        ms = _timed(step24, reps, stream, flush)
+        # the same 24 launches captured once in a CUDA graph and replayed
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            step24_on = lambda: [gdn.step(d2, lw, lc, sl, lr, side) for lw, lc, lr in layers]
+            step24_on()   # warm on the side stream before capture
+            side.synchronize()
+            with torch.cuda.graph(graph, stream=side):
+                step24_on()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        ms_g = _timed(graph.replay, reps, stream, flush)
+        b = 24 * decode_bytes(g2, S)
+        dec[str(S)] = {"ms_per_24_layer_step": ms, "rows_per_s": S / (ms * 1e-3),
+                       "algorithmic_gbs": b / (ms * 1e-3) / 1e9, "frac_hbm": b / (ms * 1e-3) / 1e9 / hbm,
+                       "graph": {"ms_per_24_layer_step": ms_g, "rows_per_s": S / (ms_g * 1e-3),
+                                 "algorithmic_gbs": b / (ms_g * 1e-3) / 1e9,
+                                 "frac_hbm": b / (ms_g * 1e-3) / 1e9 / hbm}}
+    return dec
+
+
+def _extra_prefill(dev, stream, flush, reps, hbm, bf16, fp32_alu):
+    """Prefill: (i) one 4722-token prompt; (ii) 512/1024/2048/4096 in one pass."""
+    import torch
+    import gated_deltanet_speculative_gb300 as gdn
+    g = GEOM
+    d = gdn.Dims(g.n_k_heads, g.n_v_heads, g.d_k, g.d_v)
+    pre = {}
+    for name, lengths in (("i_4722", [4722]), ("ii_512_1024_2048_4096", [512, 1024, 2048, 4096])):
+        T = sum(lengths)
+        S = len(lengths)
+        w = synth.layer_weights(g, 4)
+        cache = synth.slot_cache(g, S, 4, zero=True)
+        rows = synth.row_inputs(g, T, 4)
+        dw = {"conv_w": _bf(w["conv_w"]).to(dev), "A_log": torch.from_numpy(w["A_log"]).to(dev),
+              "dt_bias": torch.from_numpy(w["dt_bias"]).to(dev), "norm_w": _bf(w["norm_w"]).to(dev)}
+        dc = {"state": torch.from_numpy(cache["state"]).to(dev), "tail": _bf(cache["tail"]).to(dev)}
+        dr = {k: _bf(rows[k]).to(dev) for k in ("mixed", "z", "a", "b")}
+        dr["y"] = torch.empty((T, g.n_v_heads, g.d_v), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(gdn.prefill_workspace_size(d, S, T), dtype=torch.uint8, device=dev)
+        sl = torch.arange(S, dtype=torch.int32, device=dev)
+        cu = torch.from_numpy(synth.row_ptr(lengths)).to(dev)
+        state0 = dc["state"].clone()
+        tail0 = dc["tail"].clone()
+
+        def run():
+            dc["state"].copy_(state0)   # every pass starts from the zero state (tiny copy)
+            dc["tail"].copy_(tail0)
+            gdn.prefill(d, dw, dc, sl, cu, dr, ws, stream=stream)
+
+        ms = _timed(run, max(5, reps // 2), stream, flush)
+        fl = prefill_flops(g, T)
+        by = prefill_bytes(g, T, S)
+        pre[name] = {"ms": ms, "tokens_per_s": T / (ms * 1e-3), "algorithmic_tflops": fl / (ms * 1e-3) / 1e12,
+                     "frac_bf16_tensor_peak": fl / (ms * 1e-3) / 1e12 / bf16,
+                     "frac_fp32_alu_peak": fl / (ms * 1e-3) / 1e12 / fp32_alu,
+                     "algorithmic_gbs": by / (ms * 1e-3) / 1e9, "frac_hbm": by / (ms * 1e-3) / 1e9 / hbm,
+                     "algorithmic_flop": fl, "algorithmic_bytes": by,
+                     "note": "contractions on fp32 CUDA cores in this version; time includes a state reset copy"}
+        del ws, dr, dc
+    return pre
 
 
 # ---- the CPU oracle, timed on the host cores --------------------------------
@@ -398,6 +595,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--no-extra", action="store_true", help="skip the tree / decode / prefill measurements")
+    ap.add_argument("--extra-only", choices=["tree", "decode", "prefill"],
+                    help="run only this secondary measurement (3 repetitions) and print it; for profiling")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -410,6 +610,15 @@ def main():
         line = run_reference(args, rank, world)
         if line is not None:
             print(json.dumps(line), flush=True)
+        return
+
+    if args.extra_only:
+        import torch
+        torch.cuda.set_device(local_rank)
+        dev = torch.device("cuda", local_rank)
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        rec = run_extra(dev, torch.cuda.current_stream(), flush, reps=3, only=args.extra_only)
+        print(json.dumps({"extra_only": args.extra_only, **rec}), flush=True)
         return
 
     if world > 1:

@@ -85,6 +85,21 @@ struct Log2<1> {
     static constexpr int value = 0;
 };
 
+// 16-byte global -> shared copy that bypasses registers (and L1).
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const unsigned sa = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+// Wait for every cp.async this thread issued.
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *gmem) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(gmem));
+}
+
 __device__ __forceinline__ void raise_error(int *err, int bits) {
     if (err) atomicOr(err, bits);
 }

@@ -124,8 +124,8 @@ struct PrepSmem {
     static constexpr int AS = C + 4;                    // padded row of A / QK (16-byte aligned)
     static constexpr int kAQK = 2 * C * AS;             // A [C][AS], QK [C][AS]
     static constexpr int kScratchFloats = kXinFloats > kAQK ? kXinFloats : kAQK;
-    static constexpr int kVec = kScratch + kScratchFloats;   // g, beta, G [C] each
-    static constexpr int kFloats = kVec + 3 * C + 4;
+    static constexpr int kVec = kScratch + kScratchFloats;   // g, beta, G, eG, eGC [C] each
+    static constexpr int kFloats = kVec + 5 * C + 4;
     static constexpr size_t kBytes = (size_t)kFloats * 4;
 };
 
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) gdn_prefill_prep_kernel(const
     constexpr int AS = L::AS;
     float *A = smem + L::kScratch;                                     // [C][AS] after the conv
     float *QK = A + C * AS;
-    float *g = smem + L::kVec, *beta = g + C, *Gc = beta + C;
+    float *g = smem + L::kVec, *beta = g + C, *Gc = beta + C, *eG = Gc + C, *eGC = eG + C;
     __shared__ int info[5];
 
     const int h = blockIdx.x, gc = blockIdx.y, tid = threadIdx.x;
@@ -230,8 +230,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1) gdn_prefill_prep_kernel(const
             Gc[t] = run;
         }
     }
+    __syncthreads();
 
-    // A = K K^T and Q K^T, 4x4 outputs per thread
+    // A = K K^T and Q K^T: each thread owns rows t = ti + 16 r and columns
+    // s = si + 16 c (r, c < 4), so the 8 threads of a 128-bit load phase read
+    // 8 consecutive padded rows (distinct banks)
     {
         const int ti = tid / (C / 4), si = tid % (C / 4);
         float accA[4][4] = {}, accQ[4][4] = {};
@@ -239,9 +242,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1) gdn_prefill_prep_kernel(const
             float4 kt[4], ks[4], qt[4];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
-                kt[r] = *reinterpret_cast<const float4 *>(k + (ti * 4 + r) * LD + j);
-                qt[r] = *reinterpret_cast<const float4 *>(q + (ti * 4 + r) * LD + j);
-                ks[r] = *reinterpret_cast<const float4 *>(k + (si * 4 + r) * LD + j);
+                kt[r] = *reinterpret_cast<const float4 *>(k + (ti + 16 * r) * LD + j);
+                qt[r] = *reinterpret_cast<const float4 *>(q + (ti + 16 * r) * LD + j);
+                ks[r] = *reinterpret_cast<const float4 *>(k + (si + 16 * r) * LD + j);
             }
 #pragma unroll
             for (int r = 0; r < 4; ++r)
@@ -257,14 +260,17 @@ __global__ void __launch_bounds__(kPrepThreads, 1) gdn_prefill_prep_kernel(const
                     accQ[r][c] = __fmaf_rn(qt[r].w, ks[c].w, accQ[r][c]);
                 }
         }
-        __syncthreads();   // the staged xin (aliased by A, QK) is no longer read
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                A[(ti * 4 + r) * AS + si * 4 + c] = accA[r][c];
-                QK[(ti * 4 + r) * AS + si * 4 + c] = accQ[r][c];
+                A[(ti + 16 * r) * AS + si + 16 * c] = accA[r][c];
+                QK[(ti + 16 * r) * AS + si + 16 * c] = accQ[r][c];
             }
+    }
+    if (tid < C) {   // per-row exponentials of the chunk-local log decay
+        eG[tid] = expf(Gc[tid]);
+        eGC[tid] = expf(__fsub_rn(Gc[n - 1], Gc[tid]));
     }
     __syncthreads();
 
@@ -279,39 +285,56 @@ __global__ void __launch_bounds__(kPrepThreads, 1) gdn_prefill_prep_kernel(const
     }
     __syncthreads();
 
-    // forward substitution, one column per thread: X_t = Y_t - sum_{s<t} M_ts X_s
+    // Forward substitution (I + M) X = Y, one column per thread, in blocks of
+    // 16 rows: first the rows' sums over all earlier blocks (16 independent
+    // accumulators), then the 16 x 16 triangular block itself.
     if (tid < 2 * D) {
         const bool isW = tid < D;
         const int col = isW ? tid : tid - D;
         float X[C];
 #pragma unroll
-        for (int t = 0; t < C; ++t) {
-            float acc;
-            if (isW) acc = __fmul_rn(__fmul_rn(beta[t], expf(Gc[t])), k[t * LD + col]);
-            else acc = __fmul_rn(beta[t], v[t * LD + col]);
+        for (int b0 = 0; b0 < C; b0 += 16) {
+            float acc[16];
 #pragma unroll
-            for (int s = 0; s < t; s += 4) {
-                const float4 m4 = *reinterpret_cast<const float4 *>(A + t * AS + s);
-                acc = __fmaf_rn(-m4.x, X[s], acc);
-                if (s + 1 < t) acc = __fmaf_rn(-m4.y, X[s + 1], acc);
-                if (s + 2 < t) acc = __fmaf_rn(-m4.z, X[s + 2], acc);
-                if (s + 3 < t) acc = __fmaf_rn(-m4.w, X[s + 3], acc);
+            for (int i = 0; i < 16; ++i) {
+                const int t = b0 + i;
+                acc[i] = isW ? __fmul_rn(__fmul_rn(beta[t], eG[t]), k[t * LD + col])
+                             : __fmul_rn(beta[t], v[t * LD + col]);
             }
-            X[t] = acc;
+#pragma unroll
+            for (int s4 = 0; s4 < b0; s4 += 4)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float4 m4 = *reinterpret_cast<const float4 *>(A + (b0 + i) * AS + s4);
+                    acc[i] = __fmaf_rn(-m4.x, X[s4], acc[i]);
+                    acc[i] = __fmaf_rn(-m4.y, X[s4 + 1], acc[i]);
+                    acc[i] = __fmaf_rn(-m4.z, X[s4 + 2], acc[i]);
+                    acc[i] = __fmaf_rn(-m4.w, X[s4 + 3], acc[i]);
+                }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+#pragma unroll
+                for (int j = 0; j < i; ++j) acc[i] = __fmaf_rn(-A[(b0 + i) * AS + b0 + j], X[b0 + j], acc[i]);
+                X[b0 + i] = acc[i];
+            }
         }
         float *dst = blk + (isW ? B::kW : B::kU);
 #pragma unroll
         for (int t = 0; t < C; ++t) dst[t * D + col] = X[t];
     }
     // Q~ = diag(gamma) Q, K~ = diag(gamma_C / gamma) K, gamma_C
-    const float GC = Gc[n - 1];
-    for (int i = tid; i < C * D; i += kPrepThreads) {
-        const int t = i / D, e = i - t * D;
+    for (int i = tid; i < C * D / 4; i += kPrepThreads) {
+        const int t = i / (D / 4), e = (i - t * (D / 4)) * 4;
         const bool live = t < n;
-        blk[B::kQ + i] = live ? __fmul_rn(expf(Gc[t]), q[t * LD + e]) : 0.0f;
-        blk[B::kK + i] = live ? __fmul_rn(expf(__fsub_rn(GC, Gc[t])), k[t * LD + e]) : 0.0f;
+        const float4 q4 = *reinterpret_cast<const float4 *>(q + t * LD + e);
+        const float4 k4 = *reinterpret_cast<const float4 *>(k + t * LD + e);
+        const float a = live ? eG[t] : 0.0f, c = live ? eGC[t] : 0.0f;
+        *reinterpret_cast<float4 *>(blk + B::kQ + t * D + e) =
+            make_float4(__fmul_rn(a, q4.x), __fmul_rn(a, q4.y), __fmul_rn(a, q4.z), __fmul_rn(a, q4.w));
+        *reinterpret_cast<float4 *>(blk + B::kK + t * D + e) =
+            make_float4(__fmul_rn(c, k4.x), __fmul_rn(c, k4.y), __fmul_rn(c, k4.z), __fmul_rn(c, k4.w));
     }
-    if (tid == 0) blk[B::kMisc] = expf(GC);
+    if (tid == 0) blk[B::kMisc] = eG[n - 1];
 }
 
 // ---------------------------------------------------------------------------
@@ -380,25 +403,31 @@ __global__ void __launch_bounds__(NT, 1) gdn_prefill_scan_kernel(const PrefillPa
         __syncthreads();   // the previous chunk's smem readers are done
         for (int i = tid; i < C * D / 4; i += NT) {
             const int t = i / (D / 4), c4 = (i - t * (D / 4)) * 4;
-            *reinterpret_cast<float4 *>(Qs + t * LD + c4) = *reinterpret_cast<const float4 *>(blk + B::kQ + t * D + c4);
-            *reinterpret_cast<float4 *>(Ks + t * LD + c4) = *reinterpret_cast<const float4 *>(blk + B::kK + t * D + c4);
-            *reinterpret_cast<float4 *>(Ws + t * LD + c4) = *reinterpret_cast<const float4 *>(blk + B::kW + t * D + c4);
+            cp_async16(Qs + t * LD + c4, blk + B::kQ + t * D + c4);
+            cp_async16(Ks + t * LD + c4, blk + B::kK + t * D + c4);
+            cp_async16(Ws + t * LD + c4, blk + B::kW + t * D + c4);
         }
         for (int i = tid; i < C * DS / 4; i += NT) {
             const int t = i / (DS / 4), c4 = (i - t * (DS / 4)) * 4;
-            *reinterpret_cast<float4 *>(Uts + t * LS + c4) =
-                *reinterpret_cast<const float4 *>(blk + B::kU + t * D + i0 + c4);
+            cp_async16(Uts + t * LS + c4, blk + B::kU + t * D + i0 + c4);
         }
         for (int i = tid; i < C * C / 4; i += NT) {
             const int t = i / (C / 4), c4 = (i - t * (C / 4)) * 4;
-            *reinterpret_cast<float4 *>(Ps + t * (C + 4) + c4) = *reinterpret_cast<const float4 *>(blk + B::kP + t * C + c4);
+            cp_async16(Ps + t * (C + 4) + c4, blk + B::kP + t * C + c4);
         }
         if (tid == 0) gam_s[0] = blk[B::kMisc];
+        cp_async_wait_all();
+        if (c + 1 < n_chunks) {   // pull the next chunk's block toward L2 while this one computes
+            const char *nxt = reinterpret_cast<const char *>(blk + (size_t)p.Hv * B::kFloats);
+            for (int off = tid * 128; off < B::kFloats * 4; off += NT * 128) prefetch_l2(nxt + off);
+        }
         __syncthreads();
 
-        // U = U~ - W S0^T and O = Q~ S0^T: thread owns rows t0..t0+3, slice columns ic0..ic0+IC-1
+        // U = U~ - W S0^T and O = Q~ S0^T: thread owns rows t = tg + 16 r
+        // (r < 4: the 8 threads of a 128-bit phase read 8 consecutive padded
+        // rows) and slice columns ic0 .. ic0 + IC - 1
         const int tg = tid % TT, icg = tid / TT;
-        const int t0 = tg * 4, ic0 = icg * IC;
+        const int ic0 = icg * IC;
         float accU[4][IC], accO[4][IC];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
@@ -411,8 +440,8 @@ __global__ void __launch_bounds__(NT, 1) gdn_prefill_scan_kernel(const PrefillPa
             float4 w4[4], q4[4], s4[IC];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
-                w4[r] = *reinterpret_cast<const float4 *>(Ws + (t0 + r) * LD + j);
-                q4[r] = *reinterpret_cast<const float4 *>(Qs + (t0 + r) * LD + j);
+                w4[r] = *reinterpret_cast<const float4 *>(Ws + (tg + TT * r) * LD + j);
+                q4[r] = *reinterpret_cast<const float4 *>(Qs + (tg + TT * r) * LD + j);
             }
 #pragma unroll
             for (int cI = 0; cI < IC; ++cI) s4[cI] = *reinterpret_cast<const float4 *>(Ss + (ic0 + cI) * LD + j);
@@ -434,13 +463,13 @@ __global__ void __launch_bounds__(NT, 1) gdn_prefill_scan_kernel(const PrefillPa
         for (int r = 0; r < 4; ++r)
 #pragma unroll
             for (int cI = 0; cI < IC; ++cI)
-                Us[(t0 + r) * LS + ic0 + cI] = __fsub_rn(Uts[(t0 + r) * LS + ic0 + cI], accU[r][cI]);
+                Us[(tg + TT * r) * LS + ic0 + cI] = __fsub_rn(Uts[(tg + TT * r) * LS + ic0 + cI], accU[r][cI]);
         __syncthreads();
 
         // O += P U (P is lower triangular), then O to the workspace
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const int t = t0 + r;
+            const int t = tg + TT * r;
             for (int s2 = 0; s2 <= t; ++s2) {
                 const float pv = Ps[t * (C + 4) + s2];
 #pragma unroll

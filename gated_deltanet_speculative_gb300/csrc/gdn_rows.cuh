@@ -79,15 +79,6 @@ struct __align__(16) RowSmem {
     int bad;
 };
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-    const unsigned sa = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;\n" ::: "memory");
-}
-
 template <int CPL>
 __device__ __forceinline__ void load_cols(float (&x)[CPL], const float *src) {
     if constexpr (CPL == 4) {
