@@ -20,7 +20,7 @@ _lib = None
 _lock = threading.Lock()
 
 STATUS = {0: "GDN_OK", -1: "GDN_EINVAL", -2: "GDN_ENULL", -3: "GDN_EALIGN", -4: "GDN_ECUDA", -5: "GDN_EWORKSPACE"}
-DERR = {1: "slot", 2: "rows", 4: "parent", 8: "keep_row", 16: "cu_seqlens"}
+DERR = {1: "slot", 2: "rows", 4: "parent", 8: "keep_row", 16: "cu_seqlens", 32: "timeout"}
 MAX_WINDOW = 16
 
 

@@ -12,14 +12,30 @@ template <int D, int C, int DS, int NT>
 cudaError_t launch(const PrefillParams &p, cudaStream_t st) {
     using Prep = PrepSmem<D, C>;
     using Scan = ScanSmem<D, C, DS>;
-    cudaError_t e = cudaFuncSetAttribute(gdn_prefill_prep_kernel<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Prep::kBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gdn_prefill_scan_kernel<D, C, DS, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Scan::kBytes);
-    if (e != cudaSuccess) return e;
-    gdn_prefill_prep_kernel<D, C><<<dim3(p.Hv, p.max_chunks), kPrepThreads, Prep::kBytes, st>>>(p);
-    gdn_prefill_scan_kernel<D, C, DS, NT><<<dim3(D / DS, p.Hv, p.n_seqs), NT, Scan::kBytes, st>>>(p);
+    constexpr bool TC = (D == 128 && C == 64);   // tensor-core prep and scan for d = 128
+    cudaError_t e;
+    if constexpr (TC) {
+        e = cudaFuncSetAttribute(gdn_prefill_prep_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kPrepTcSmem);
+        if (e != cudaSuccess) return e;
+        gdn_prefill_prep_tc_kernel<C><<<dim3(p.Hv, p.max_chunks), kPrepTcThreads, kPrepTcSmem, st>>>(p);
+    } else {
+        e = cudaFuncSetAttribute(gdn_prefill_prep_kernel<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)Prep::kBytes);
+        if (e != cudaSuccess) return e;
+        gdn_prefill_prep_kernel<D, C><<<dim3(p.Hv, p.max_chunks), kPrepThreads, Prep::kBytes, st>>>(p);
+    }
+    if constexpr (TC) {
+        e = cudaFuncSetAttribute(gdn_prefill_scan_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kScanTcSmem);
+        if (e != cudaSuccess) return e;
+        gdn_prefill_scan_tc_kernel<C><<<dim3(p.Hv, p.n_seqs), kScanTcThreads, kScanTcSmem, st>>>(p);
+    } else {
+        e = cudaFuncSetAttribute(gdn_prefill_scan_kernel<D, C, DS, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)Scan::kBytes);
+        if (e != cudaSuccess) return e;
+        gdn_prefill_scan_kernel<D, C, DS, NT><<<dim3(D / DS, p.Hv, p.n_seqs), NT, Scan::kBytes, st>>>(p);
+    }
     const size_t items = (size_t)p.n_tokens * p.Hv;
     const unsigned blocks = (unsigned)((items + kNormThreads / 32 - 1) / (kNormThreads / 32));
     gdn_prefill_norm_kernel<D><<<blocks, kNormThreads, 0, st>>>(p);

@@ -24,6 +24,7 @@
 #pragma once
 
 #include "gdn_common.cuh"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 
@@ -51,6 +52,7 @@ struct PrefillParams {
 };
 
 constexpr int kPrefillChunk = 64;
+constexpr uint32_t kPrepWaitLimit = 1u << 22;
 constexpr int kPrepThreads = 256;
 constexpr int kNormThreads = 256;
 
@@ -65,6 +67,57 @@ struct ChunkBlock {
     static constexpr int kMisc = 4 * C * D + C * C;   // gamma_C, pad
     static constexpr int kFloats = kMisc + 4;
 };
+
+// The same block as laid out for the tensor-core scan (d = 128, C = 64), in
+// bytes.  bf16 operands are pre-split (x = hi + lo, both bf16) and stored in
+// the K-major no-swizzle layout of gdn_tc.cuh, hi block then lo block:
+//   W    rows t (64), K = j (128)     B operand of U^T = S0 W^T
+//   Q~   rows t (64), K = j (128)     B operand of O^T = S0 Q~^T
+//   P    rows t (64), K = s (64)      B operand of O^T += U^T P^T
+//   K~^T rows j (128), K = t (64)     B operand of S = gamma_C S0 + U^T K~
+//   U~^T fp32 [128 i][64 t]           added to -S0 W^T in fp32
+//   gamma_C
+struct TcBlock {
+    static constexpr int kW = 0;
+    static constexpr int kQ = 32768;
+    static constexpr int kP = 65536;
+    static constexpr int kK = 81920;
+    static constexpr int kGroup1 = 65536;      // bytes of W | Q~
+    static constexpr int kGroup2 = 49152;      // bytes of P | K~^T
+    static constexpr int kOpBytes = 114688;
+    static constexpr int kUt = 114688;
+    static constexpr int kMisc = 147456;
+    static constexpr int kBytes = 147472;
+};
+static_assert(TcBlock::kBytes == ChunkBlock<128, 64>::kFloats * 4, "tensor-core block must match the fp32 block size");
+
+// Store x at element (r, k) of a K-major bf16 operand (K columns) as hi in
+// `hi_base` and lo in `lo_base`.
+__device__ __forceinline__ void store_split(unsigned char *hi_base, unsigned char *lo_base, int r, int k, int K,
+                                            float x) {
+    uint16_t h, l;
+    tc::split_bf16(x, h, l);
+    const uint32_t off = tc::kmajor_offset(r, k, K);
+    *reinterpret_cast<uint16_t *>(hi_base + off) = h;
+    *reinterpret_cast<uint16_t *>(lo_base + off) = l;
+}
+
+// Store 8 consecutive k (k0 multiple of 8) of row r as two 16-byte writes.
+__device__ __forceinline__ void store_split8(unsigned char *hi_base, unsigned char *lo_base, int r, int k0, int K,
+                                             const float (&x)[8]) {
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint16_t h0, l0, h1, l1;
+        tc::split_bf16(x[2 * j], h0, l0);
+        tc::split_bf16(x[2 * j + 1], h1, l1);
+        hw[j] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        lw[j] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+    }
+    const uint32_t off = tc::kmajor_offset(r, k0, K);
+    *reinterpret_cast<uint4 *>(hi_base + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4 *>(lo_base + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
 
 // Locate global chunk gc: its sequence, first token, rows, and the
 // sequence's first token.  Returns false past the last chunk or on bad
@@ -175,23 +228,32 @@ __global__ void __launch_bounds__(kPrepThreads, 1) gdn_prefill_prep_kernel(const
     }
     __syncthreads();
 
-    // conv + SiLU (rows >= n are zero)
-    for (int i = tid; i < C * 3 * D; i += kPrepThreads) {
-        const int t = i / (3 * D), cc = i - t * 3 * D;
+    // conv + SiLU, one channel per thread down the chunk with a sliding
+    // window of the four taps (rows >= n are zero)
+    for (int cc = tid; cc < 3 * D; cc += kPrepThreads) {
         const int part = cc / D, e = cc - part * D;
-        float act = 0.0f;
-        if (t < n) {
-            const int c = pchannel<D>(part, e, p.Hk, kh, h);
-            const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + (size_t)c * 4));
-            const uint16_t *x = xin + (size_t)t * 3 * D + cc;   // staged row t is 3 back from row t
-            float acc = __fmul_rn(bf_bits(wv.x & 0xffffu), bf_bits(x[0]));
-            acc = __fmaf_rn(bf_bits(wv.x >> 16), bf_bits(x[3 * D]), acc);
-            acc = __fmaf_rn(bf_bits(wv.y & 0xffffu), bf_bits(x[6 * D]), acc);
-            acc = __fmaf_rn(bf_bits(wv.y >> 16), bf_bits(x[9 * D]), acc);
-            act = silu(acc);
+        const int c = pchannel<D>(part, e, p.Hk, kh, h);
+        const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + (size_t)c * 4));
+        const float w0 = bf_bits(wv.x & 0xffffu), w1 = bf_bits(wv.x >> 16);
+        const float w2 = bf_bits(wv.y & 0xffffu), w3 = bf_bits(wv.y >> 16);
+        const uint16_t *x = xin + cc;   // staged row t + 3 is row t itself
+        float x0 = bf_bits(x[0]), x1 = bf_bits(x[3 * D]), x2 = bf_bits(x[6 * D]);
+        float *dst = (part == 0 ? q : (part == 1 ? k : v)) + e;
+        for (int t = 0; t < C; ++t) {
+            float act = 0.0f;
+            if (t < n) {
+                const float x3 = bf_bits(x[(size_t)(t + 3) * 3 * D]);
+                float acc = __fmul_rn(w0, x0);
+                acc = __fmaf_rn(w1, x1, acc);
+                acc = __fmaf_rn(w2, x2, acc);
+                acc = __fmaf_rn(w3, x3, acc);
+                act = __fdividef(acc, 1.0f + __expf(-acc));   // SiLU; prefill matches steps to tolerance
+                x0 = x1;
+                x1 = x2;
+                x2 = x3;
+            }
+            dst[t * LD] = act;
         }
-        float *dst = part == 0 ? q : (part == 1 ? k : v);
-        dst[t * LD + e] = act;
     }
     __syncthreads();
 
@@ -223,12 +285,18 @@ __global__ void __launch_bounds__(kPrepThreads, 1) gdn_prefill_prep_kernel(const
         beta[tid] = bb;
     }
     __syncthreads();
-    if (tid == 0) {
-        float run = 0.0f;
-        for (int t = 0; t < C; ++t) {
-            run = __fadd_rn(run, g[t]);
-            Gc[t] = run;
+    if (warp == 0) {   // inclusive prefix sum of the log decays, two rows per lane
+        const float a0 = g[2 * lane], a1 = g[2 * lane + 1];
+        float run = __fadd_rn(a0, a1);
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_up_sync(kFull, run, off);
+            if (lane >= off) run = __fadd_rn(run, o);
         }
+        const float excl = __shfl_up_sync(kFull, run, 1);
+        const float before = lane == 0 ? 0.0f : excl;
+        Gc[2 * lane] = __fadd_rn(before, a0);
+        Gc[2 * lane + 1] = run;
     }
     __syncthreads();
 
@@ -268,6 +336,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) gdn_prefill_prep_kernel(const
                 QK[(ti + 16 * r) * AS + si + 16 * c] = accQ[r][c];
             }
     }
+
     if (tid < C) {   // per-row exponentials of the chunk-local log decay
         eG[tid] = expf(Gc[tid]);
         eGC[tid] = expf(__fsub_rn(Gc[n - 1], Gc[tid]));
@@ -279,7 +348,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) gdn_prefill_prep_kernel(const
     for (int i = tid; i < C * C; i += kPrepThreads) {
         const int t = i / C, s = i - t * C;
         const bool live = t < n && s < n;
-        const float gam = live ? expf(__fsub_rn(Gc[t], Gc[s])) : 0.0f;
+        const float gam = live ? __expf(__fsub_rn(Gc[t], Gc[s])) : 0.0f;
         A[t * AS + s] = (live && s < t) ? __fmul_rn(__fmul_rn(beta[t], gam), A[t * AS + s]) : 0.0f;
         blk[B::kP + i] = (live && s <= t) ? __fmul_rn(gam, QK[t * AS + s]) : 0.0f;
     }
@@ -544,6 +613,700 @@ __global__ void __launch_bounds__(NT, 1) gdn_prefill_scan_kernel(const PrefillPa
             tl[2 * CH] = nw[2];
         }
     }
+}
+
+// ---------------------------------------------------------------------------
+// prep on the tensor cores (d = 128, C = 64): one CTA of 256 threads per
+// (value head, global chunk).  The chunk's WY/UT quantities in the form the
+// tensor-core scan consumes (TcBlock):
+//   gates first; conv + SiLU with v written straight into the (diag(b) V)^T
+//   operand; L2 norms of q and k;
+//   MMA 1:  [K; Q] (128 x 128) * K^T        -> A = K K^T and Q K^T
+//   M = strict_lower(diag(b) Gamma o A),  P = lower(Gamma o Q K^T)
+//   T = (I + M)^-1 in 16 x 16 blocks on the CUDA cores (fp32)
+//   MMA 2:  (diag(b gamma) K)^T * T^T -> W^T,   (diag(b) V)^T * T^T -> U~^T
+// Every MMA operand is split into bf16 hi + lo and multiplied three times
+// (hi hi + hi lo + lo hi), accumulating in fp32.
+//
+// Shared memory (bytes):
+//   q, k fp32 [64][132]                         0 .. 67584    (q's part holds T fp32 later)
+//   region B                                    67584 .. +131072:
+//     B + 0      staged conv inputs (51456), then the [K; Q] operand hi | lo
+//                (65536), then A / QK fp32 [64][68] x 2 (34816) and the T
+//                operand hi | lo (16384, at B + 34816)
+//     B + 65536  (diag(b gamma) K)^T operand hi | lo (32768)
+//     B + 98304  (diag(b) V)^T operand hi | lo (32768)
+//   vectors g, beta, G, eG, eGC [64] each
+// ---------------------------------------------------------------------------
+// One block row of T = (I + M)^-1 (16 x 16 blocks, C = 64): for every
+// block column bj < BI,  T[BI][bj] = -T[BI][BI] * sum_{kb = bj}^{BI-1} M[BI][kb] T[kb][bj].
+// Thread (rr, cc) = (tid / 16, tid % 16) owns row rr, column cc of each block.
+template <int BI>
+__device__ __forceinline__ void prep_inverse_block_row(const float *M, float *T, int tid) {
+    constexpr int AS = 68;
+    const int rr = tid / 16, cc = tid % 16;
+    float z[BI];
+#pragma unroll
+    for (int bj = 0; bj < BI; ++bj) z[bj] = 0.0f;
+    const float *mrow = M + (BI * 16 + rr) * AS;
+#pragma unroll
+    for (int kk = 0; kk < BI * 16; ++kk) {
+        const float m = mrow[kk];
+#pragma unroll
+        for (int bj = 0; bj < BI; ++bj)
+            if (kk >= bj * 16) z[bj] = __fmaf_rn(m, T[kk * AS + bj * 16 + cc], z[bj]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int bj = 0; bj < BI; ++bj) T[(BI * 16 + rr) * AS + bj * 16 + cc] = z[bj];   // stash Z
+    __syncthreads();
+    float t[BI];
+#pragma unroll
+    for (int bj = 0; bj < BI; ++bj) t[bj] = 0.0f;
+    const float *trow = T + (BI * 16 + rr) * AS + BI * 16;
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+        const float d = kk <= rr ? trow[kk] : 0.0f;
+#pragma unroll
+        for (int bj = 0; bj < BI; ++bj) t[bj] = __fmaf_rn(d, T[(BI * 16 + kk) * AS + bj * 16 + cc], t[bj]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int bj = 0; bj < BI; ++bj) T[(BI * 16 + rr) * AS + bj * 16 + cc] = -t[bj];
+    __syncthreads();
+}
+
+constexpr int kPrepTcThreads = 256;
+constexpr int kPrepTcLD = 132;
+constexpr size_t kPrepTcQK = 2 * 64 * kPrepTcLD * 4;
+constexpr size_t kPrepTcSmem = kPrepTcQK + 131072 + 5 * 64 * 4;
+
+template <int C>
+__global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(const PrefillParams p) {
+    constexpr int D = 128, LD = kPrepTcLD, AS = C + 4;
+    static_assert(C == 64, "the tensor-core block layout is for C = 64");
+    extern __shared__ __align__(1024) unsigned char psm[];
+    float *q = reinterpret_cast<float *>(psm);
+    float *k = q + C * LD;
+    unsigned char *B = psm + kPrepTcQK;
+    uint16_t *xin = reinterpret_cast<uint16_t *>(B);               // [C+3][3D]
+    unsigned char *kq_hi = B, *kq_lo = B + 32768;                 // [K; Q] operand
+    float *A = reinterpret_cast<float *>(B);                       // [C][AS] after MMA 1
+    float *QK = A + C * AS;
+    unsigned char *t_hi = B + 34816, *t_lo = t_hi + 8192;          // T operand [C][C]
+    unsigned char *y_hi = B + 65536, *y_lo = y_hi + 16384;         // (b gamma K)^T [D][C]
+    unsigned char *v_hi = B + 98304, *v_lo = v_hi + 16384;         // (b V)^T [D][C]
+    float *T = q;                                                  // [C][AS] once q is consumed
+    unsigned char *w_stage = B + 0;                                // W hi | lo after MMA 2 (A / QK, T op dead)
+    float *g = reinterpret_cast<float *>(B + 131072);
+    float *beta = g + C, *Gc = beta + C, *eG = Gc + C, *eGC = eG + C;
+    __shared__ int info[4];
+    __shared__ __align__(8) uint64_t bar_mma;
+    __shared__ uint32_t tmem_base;
+
+    const int h = blockIdx.x, gc = blockIdx.y, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int kh = h / p.G;
+    const size_t CH = (size_t)p.CH;
+    if (tid == 0) {
+        int seq = -1, start = 0, n = 0, seq_start = 0, bad = 0;
+        const bool ok = locate_chunk(p, C, gc, seq, start, n, seq_start, bad);
+        const int sl = ok ? __ldg(p.slot + seq) : -1;
+        if (ok && (sl < 0 || sl >= p.n_slots)) bad |= 2;
+        if (bad && h == 0) raise_error(p.err, (bad & 1 ? GDN_DERR_SEQLENS : 0) | (bad & 2 ? GDN_DERR_SLOT : 0));
+        info[0] = (ok && !bad) ? n : 0;
+        info[1] = start;
+        info[2] = seq_start;
+        info[3] = sl;
+    }
+    __syncthreads();
+    const int n = info[0], start = info[1], seq_start = info[2], sl = info[3];
+    if (n == 0) return;
+
+    // gates (rows >= n: beta = 0, log decay 0)
+    if (tid < C) {
+        float gg = 0.0f, bb = 0.0f;
+        if (tid < n) {
+            const size_t gi = (size_t)(start + tid) * p.Hv + h;
+            gg = -__fmul_rn(expf(p.A_log[h]), softplusf_rn(__fadd_rn(bf_bits(p.a[gi]), p.dt_bias[h])));
+            bb = sigmoidf_rn(bf_bits(p.b[gi]));
+        }
+        g[tid] = gg;
+        beta[tid] = bb;
+    }
+    // stage the conv inputs: rows start-3 .. start+n-1 (the slot's kept tail
+    // before the sequence), this head's q | k | v channels
+    constexpr int SEG = D * 2 / 16, CHUNKS = 3 * SEG;
+    for (int i = tid; i < (n + 3) * CHUNKS; i += kPrepTcThreads) {
+        const int row = i / CHUNKS, ch = i - row * CHUNKS;
+        const int part = ch / SEG, off = (ch - part * SEG) * 8;
+        const int c = pchannel<D>(part, off, p.Hk, kh, h);
+        const int tok = start - 3 + row;
+        const uint16_t *src = tok >= seq_start ? p.mixed + (size_t)tok * CH + c
+                                               : p.tail + ((size_t)sl * 3 + (3 - (seq_start - tok))) * CH + c;
+        cp_async16(xin + (size_t)row * 3 * D + part * D + off, src);
+    }
+    if (warp == 0) tc::tmem_alloc(&tmem_base, 256);
+    if (tid == 0) {
+        tc::mbar_init(&bar_mma, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    if (warp == 0) {   // inclusive prefix sum of the log decays, two rows per lane
+        const float a0 = g[2 * lane], a1 = g[2 * lane + 1];
+        float run = __fadd_rn(a0, a1);
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_up_sync(kFull, run, off);
+            if (lane >= off) run = __fadd_rn(run, o);
+        }
+        const float excl = __shfl_up_sync(kFull, run, 1);
+        Gc[2 * lane] = __fadd_rn(lane == 0 ? 0.0f : excl, a0);
+        Gc[2 * lane + 1] = run;
+    }
+
+    // conv + SiLU down the chunk, one channel per thread, sliding window of
+    // the four taps; q and k to fp32 rows, v straight into (diag(b) V)^T
+    for (int cc = tid; cc < 3 * D; cc += kPrepTcThreads) {
+        const int part = cc / D, e = cc - part * D;
+        const int c = pchannel<D>(part, e, p.Hk, kh, h);
+        const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + (size_t)c * 4));
+        const float w0 = bf_bits(wv.x & 0xffffu), w1 = bf_bits(wv.x >> 16);
+        const float w2 = bf_bits(wv.y & 0xffffu), w3 = bf_bits(wv.y >> 16);
+        const uint16_t *x = xin + cc;
+        float x0 = bf_bits(x[0]), x1 = bf_bits(x[3 * D]), x2 = bf_bits(x[6 * D]);
+        float *dst = part == 0 ? q + e : k + e;
+        for (int t0 = 0; t0 < C; t0 += 8) {
+            float vb[8];
+#pragma unroll
+            for (int e8 = 0; e8 < 8; ++e8) {
+                const int t = t0 + e8;
+                float act = 0.0f;
+                if (t < n) {
+                    const float x3 = bf_bits(x[(size_t)(t + 3) * 3 * D]);
+                    float acc = __fmul_rn(w0, x0);
+                    acc = __fmaf_rn(w1, x1, acc);
+                    acc = __fmaf_rn(w2, x2, acc);
+                    acc = __fmaf_rn(w3, x3, acc);
+                    act = __fdividef(acc, 1.0f + __expf(-acc));   // SiLU; prefill matches steps to tolerance
+                    x0 = x1;
+                    x1 = x2;
+                    x2 = x3;
+                }
+                if (part < 2) dst[t * LD] = act;
+                vb[e8] = __fmul_rn(beta[t], act);
+            }
+            if (part == 2) store_split8(v_hi, v_lo, e, t0, C, vb);
+        }
+    }
+    __syncthreads();
+    if (tid < C) {
+        eG[tid] = __expf(Gc[tid]);
+        eGC[tid] = __expf(__fsub_rn(Gc[n - 1], Gc[tid]));
+    }
+    // L2 norms of q and k rows (one warp per vector), q scaled
+    for (int j = warp; j < 2 * n; j += kPrepTcThreads / 32) {
+        float *x = (j & 1) ? k + (j >> 1) * LD : q + (j >> 1) * LD;
+        const float4 xv = *reinterpret_cast<const float4 *>(x + lane * 4);
+        float ss = __fmul_rn(xv.x, xv.x);
+        ss = __fmaf_rn(xv.y, xv.y, ss);
+        ss = __fmaf_rn(xv.z, xv.z, ss);
+        ss = __fmaf_rn(xv.w, xv.w, ss);
+        ss = warp_sum(ss);
+        const float s = __fmul_rn(rsqrtf(__fadd_rn(ss, p.eps_l2)), (j & 1) ? 1.0f : p.q_scale);
+        *reinterpret_cast<float4 *>(x + lane * 4) =
+            make_float4(__fmul_rn(xv.x, s), __fmul_rn(xv.y, s), __fmul_rn(xv.z, s), __fmul_rn(xv.w, s));
+    }
+    __syncthreads();
+
+    // operands of MMA 1 and 2, and the Q~ / K~^T outputs (rows fastest across
+    // threads: 8 threads fill one 128-byte core matrix)
+    unsigned char *blk = reinterpret_cast<unsigned char *>(p.ws_chunks) + ((size_t)gc * p.Hv + h) * TcBlock::kBytes;
+    for (int it = tid; it < 2 * C * (D / 8); it += kPrepTcThreads) {   // [K; Q], rows r, 8 columns j
+        const int r = it % (2 * C), j0 = (it / (2 * C)) * 8;
+        const float *src = r < C ? k + r * LD + j0 : q + (r - C) * LD + j0;
+        const float4 a4 = *reinterpret_cast<const float4 *>(src), b4 = *reinterpret_cast<const float4 *>(src + 4);
+        const float x[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
+        store_split8(kq_hi, kq_lo, r, j0, D, x);
+    }
+    for (int it = tid; it < D * (C / 8); it += kPrepTcThreads) {   // (b gamma K)^T and K~^T: rows j, 8 t
+        const int j = it % D, t0 = (it / D) * 8;
+        float y[8], kt[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float kv = k[(t0 + e) * LD + j];
+            y[e] = __fmul_rn(__fmul_rn(beta[t0 + e], eG[t0 + e]), kv);
+            kt[e] = (t0 + e) < n ? __fmul_rn(eGC[t0 + e], kv) : 0.0f;
+        }
+        store_split8(y_hi, y_lo, j, t0, C, y);
+        store_split8(blk + TcBlock::kK, blk + TcBlock::kK + 16384, j, t0, C, kt);
+    }
+    for (int it = tid; it < C * (D / 8); it += kPrepTcThreads) {   // Q~: rows t, 8 columns j
+        const int t = it % C, j0 = (it / C) * 8;
+        const float a = t < n ? eG[t] : 0.0f;
+        const float4 a4 = *reinterpret_cast<const float4 *>(q + t * LD + j0);
+        const float4 b4 = *reinterpret_cast<const float4 *>(q + t * LD + j0 + 4);
+        const float x[8] = {__fmul_rn(a, a4.x), __fmul_rn(a, a4.y), __fmul_rn(a, a4.z), __fmul_rn(a, a4.w),
+                            __fmul_rn(a, b4.x), __fmul_rn(a, b4.y), __fmul_rn(a, b4.z), __fmul_rn(a, b4.w)};
+        store_split8(blk + TcBlock::kQ, blk + TcBlock::kQ + 16384, t, j0, D, x);
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    // MMA 1: [A; QK] = [K; Q] K^T  (TMEM columns 0..63)
+    if (tid == 0) {
+        constexpr uint32_t idn = tc::idesc_bf16(128, C);
+        const uint32_t ah = tc::smem_u32(kq_hi), al = tc::smem_u32(kq_lo);
+        tc::mma_bf16(tmem_base, ah, ah, D, idn, false);
+        tc::mma_bf16(tmem_base, ah, al, D, idn, true);
+        tc::mma_bf16(tmem_base, al, ah, D, idn, true);
+        tc::mma_commit(&bar_mma);
+    }
+    bool ok = tc::mbar_wait(&bar_mma, 0, kPrepWaitLimit);
+    tc::fence_after_sync();
+    const int quarter = warp & 3, half = warp >> 2;
+    {   // lane r holds row r of [A; QK]; warps w and w + 4 split the 64 columns
+        const int r = quarter * 32 + lane;
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + half * (C / 2);
+        uint32_t v[C / 32][16];
+#pragma unroll
+        for (int q2 = 0; q2 < C / 32; ++q2) tc::tmem_ld16_nowait(taddr + q2 * 16, v[q2]);
+        tc::tmem_wait_ld();
+        __syncthreads();   // every MMA-1 read of the [K; Q] operand is long done; A / QK overwrite it
+        float *dst = r < C ? A + r * AS : QK + (r - C) * AS;
+#pragma unroll
+        for (int q2 = 0; q2 < C / 32; ++q2)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) dst[half * (C / 2) + q2 * 16 + e] = __uint_as_float(v[q2][e]);
+    }
+    __syncthreads();
+
+    // M = strict_lower(diag(b) Gamma o A) in place; P = lower(Gamma o QK) in place
+    for (int i = tid; i < C * C; i += kPrepTcThreads) {
+        const int t = i / C, s = i - t * C;
+        const bool live = t < n && s < n;
+        const float gam = live ? __expf(__fsub_rn(Gc[t], Gc[s])) : 0.0f;
+        A[t * AS + s] = (live && s < t) ? __fmul_rn(__fmul_rn(beta[t], gam), A[t * AS + s]) : 0.0f;
+        QK[t * AS + s] = (live && s <= t) ? __fmul_rn(gam, QK[t * AS + s]) : 0.0f;
+    }
+    __syncthreads();
+    for (int it = tid; it < C * (C / 8); it += kPrepTcThreads) {   // P output: rows t, 8 columns s
+        const int t = it % C, s0 = (it / C) * 8;
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = QK[t * AS + s0 + e];
+        store_split8(blk + TcBlock::kP, blk + TcBlock::kP + 8192, t, s0, C, x);
+    }
+    // T = (I + M)^-1: the four 16 x 16 diagonal blocks by forward
+    // substitution (one column per thread) ...
+    if (tid < C) {
+        const int b0 = (tid / 16) * 16, c = tid % 16;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = r == c ? 1.0f : 0.0f;
+#pragma unroll
+            for (int kk = 0; kk < r; ++kk) acc = __fmaf_rn(-A[(b0 + r) * AS + b0 + kk], x[kk], acc);
+            x[r] = r < c ? 0.0f : acc;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) T[(b0 + r) * AS + b0 + c] = x[r];
+    }
+    for (int i = tid; i < C * C; i += kPrepTcThreads) {   // zero the strictly upper blocks
+        const int t = i / C, s = i - t * C;
+        if (s / 16 > t / 16) T[t * AS + s] = 0.0f;
+    }
+    __syncthreads();
+    // ... then block row bi: T_bi,bj = -T_bi,bi * sum_{kb = bj}^{bi-1} M_bi,kb T_kb,bj
+    prep_inverse_block_row<1>(A, T, tid);
+    prep_inverse_block_row<2>(A, T, tid);
+    prep_inverse_block_row<3>(A, T, tid);
+    // T operand (rows t, K = s); A and QK are no longer read
+    for (int it = tid; it < C * (C / 8); it += kPrepTcThreads) {
+        const int t = it % C, s0 = (it / C) * 8;
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = T[t * AS + s0 + e];
+        store_split8(t_hi, t_lo, t, s0, C, x);
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    // MMA 2: W^T = (b gamma K)^T T^T (columns 64..127), U~^T = (b V)^T T^T (128..191)
+    if (tid == 0) {
+        constexpr uint32_t idn = tc::idesc_bf16(128, C);
+        const uint32_t th = tc::smem_u32(t_hi), tl = tc::smem_u32(t_lo);
+        const uint32_t yh = tc::smem_u32(y_hi), yl = tc::smem_u32(y_lo);
+        const uint32_t vh = tc::smem_u32(v_hi), vl = tc::smem_u32(v_lo);
+        tc::mma_bf16(tmem_base + 64, yh, th, C, idn, false);
+        tc::mma_bf16(tmem_base + 64, yh, tl, C, idn, true);
+        tc::mma_bf16(tmem_base + 64, yl, th, C, idn, true);
+        tc::mma_bf16(tmem_base + 128, vh, th, C, idn, false);
+        tc::mma_bf16(tmem_base + 128, vh, tl, C, idn, true);
+        tc::mma_bf16(tmem_base + 128, vl, th, C, idn, true);
+        tc::mma_commit(&bar_mma);
+    }
+    ok = tc::mbar_wait(&bar_mma, 1, kPrepWaitLimit) && ok;
+    tc::fence_after_sync();
+    {
+        // lane j of W^T: W[t][j] for every t (warps 0-3); lane i of U~^T: U~^T[i][t] (warps 4-7)
+        const int r = quarter * 32 + lane;
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (half ? 128 : 64);
+        uint32_t v[C / 16][16];
+#pragma unroll
+        for (int q2 = 0; q2 < C / 16; ++q2) tc::tmem_ld16_nowait(taddr + q2 * 16, v[q2]);
+        tc::tmem_wait_ld();
+        if (half == 0) {   // W (rows t, K = j) hi | lo into shared memory (the dead [K; Q] region)
+#pragma unroll
+            for (int q2 = 0; q2 < C / 16; ++q2)
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    store_split(w_stage, w_stage + 16384, q2 * 16 + e, r, D, __uint_as_float(v[q2][e]));
+        } else {
+            float4 *ut = reinterpret_cast<float4 *>(blk + TcBlock::kUt) + r * (C / 4);
+#pragma unroll
+            for (int q2 = 0; q2 < C / 16; ++q2)
+#pragma unroll
+                for (int e = 0; e < 16; e += 4)
+                    ut[q2 * 4 + e / 4] = make_float4(__uint_as_float(v[q2][e]), __uint_as_float(v[q2][e + 1]),
+                                                     __uint_as_float(v[q2][e + 2]), __uint_as_float(v[q2][e + 3]));
+        }
+    }
+    __syncthreads();
+    {   // the staged W, hi then lo, to the workspace as 16-byte stores
+        const uint4 *src = reinterpret_cast<const uint4 *>(w_stage);
+        uint4 *dst = reinterpret_cast<uint4 *>(blk + TcBlock::kW);
+        for (int it = tid; it < 32768 / 16; it += kPrepTcThreads) dst[it] = src[it];
+    }
+    if (tid == 0) {
+        *reinterpret_cast<float *>(blk + TcBlock::kMisc) = eG[n - 1];
+        if (!ok) raise_error(p.err, GDN_DERR_TIMEOUT);
+    }
+    if (tid == 0) {   // no MMA may still write TMEM when it is freed
+        tc::mma_commit(&bar_mma);
+        tc::mbar_wait(&bar_mma, 0, kPrepWaitLimit);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
+}
+
+// ---------------------------------------------------------------------------
+// scan on the tensor cores (d = 128): one CTA of 128 threads per (value
+// head, sequence).  Thread i owns TMEM lane i, i.e. state row i.  TMEM holds
+// three fp32 accumulators: U^T [128 x 64] (columns 0..63), O^T [128 x 64]
+// (64..127) and the state S [128 x 128] (128..255), which stays in TMEM from
+// chunk to chunk.  Every product is three bf16 MMAs (hi*hi + hi*lo + lo*hi)
+// accumulating in fp32.  Per chunk:
+//   S0 -> bf16 hi/lo A operand (shared memory); TMEM S <- gamma_C S0
+//   group 1: U^T = S0 W^T, O^T = S0 Q~^T                     (K = 128)
+//   U = U~ - U^T (fp32) -> bf16 hi/lo A operand
+//   group 2: O^T += U^T P^T, S += U^T K~                     (K = 64)
+//   O^T -> the workspace (fp32) for the norm pass
+// The chunk's operands arrive by 1-D bulk copies in two halves, each issued
+// as soon as the previous chunk's MMAs are done with that half.
+// ---------------------------------------------------------------------------
+constexpr int kScanTcThreads = 128;
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr size_t kScanTcSmem = TcBlock::kOpBytes + 65536 + 32768;
+
+__device__ __forceinline__ void issue_group1(unsigned char *ops, const unsigned char *blk, uint64_t *bar) {
+    tc::mbar_expect_tx(bar, TcBlock::kGroup1);
+    for (int off = 0; off < TcBlock::kGroup1; off += 16384) tc::bulk_g2s(ops + off, blk + off, 16384, bar);
+}
+
+__device__ __forceinline__ void issue_group2(unsigned char *ops, const unsigned char *blk, uint64_t *bar) {
+    tc::mbar_expect_tx(bar, TcBlock::kGroup2);
+    for (int off = 0; off < TcBlock::kGroup2; off += 16384)
+        tc::bulk_g2s(ops + TcBlock::kGroup1 + off, blk + TcBlock::kGroup1 + off, 16384, bar);
+}
+
+// S0 (TMEM, row i = this thread) -> bf16 hi/lo A operand in shared memory,
+// and TMEM S <- gamma_C * S0 for the coming U^T K~ accumulation.
+__device__ __forceinline__ void split_and_scale_state(uint32_t tS, unsigned char *S_hi, unsigned char *S_lo, int i,
+                                                      float gC) {
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+        uint32_t r[4][16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tc::tmem_ld16_nowait(tS + half * 64 + q * 16, r[q]);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float a[8], b[8], v[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[q][e]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                a[e] = v[e];
+                b[e] = v[8 + e];
+            }
+            const int col = half * 64 + q * 16;
+            store_split8(S_hi, S_lo, i, col, 128, a);
+            store_split8(S_hi, S_lo, i, col + 8, 128, b);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(gC, v[e]);
+            tc::tmem_st16_nowait(tS + col, v);
+        }
+    }
+    tc::tmem_wait_st();
+}
+
+template <int C>
+__global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(const PrefillParams p) {
+    constexpr int D = 128;
+    extern __shared__ __align__(1024) unsigned char tsm[];
+    unsigned char *ops = tsm;                            // W | Q~ | P | K~^T, hi and lo each
+    unsigned char *S_hi = tsm + TcBlock::kOpBytes;       // A operand S0 [128 x 128]
+    unsigned char *S_lo = S_hi + 32768;
+    unsigned char *U_hi = S_lo + 32768;                  // A operand U^T [128 x 64]
+    unsigned char *U_lo = U_hi + 16384;
+    __shared__ __align__(8) uint64_t bar_g1, bar_g2, bar_u, bar_s, bar_o, bar_end;
+    __shared__ uint32_t tmem_base;
+    __shared__ int fail;
+
+    const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    const int base = chunk_base(p, C, s);
+    if (base < 0) {
+        if (h == 0 && tid == 0) raise_error(p.err, GDN_DERR_SEQLENS);
+        return;
+    }
+    const int lo = __ldg(p.cu_seqlens + s), hi = __ldg(p.cu_seqlens + s + 1);
+    const int L_s = hi - lo;
+    if (L_s == 0) return;
+    const int sl = __ldg(p.slot + s);
+    if (sl < 0 || sl >= p.n_slots) {
+        if (h == 0 && tid == 0) raise_error(p.err, GDN_DERR_SLOT);
+        return;
+    }
+    const int n_chunks = (L_s + C - 1) / C;
+    const size_t blk_stride = (size_t)p.Hv * TcBlock::kBytes;
+    const unsigned char *blk0 =
+        reinterpret_cast<const unsigned char *>(p.ws_chunks) + ((size_t)base * p.Hv + h) * TcBlock::kBytes;
+
+    if (tid == 0) {
+        tc::mbar_init(&bar_g1, 1);
+        tc::mbar_init(&bar_g2, 1);
+        tc::mbar_init(&bar_u, 1);
+        tc::mbar_init(&bar_s, 1);
+        tc::mbar_init(&bar_o, 1);
+        tc::mbar_init(&bar_end, 1);
+        fail = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    tc::fence_async_smem();
+    if (warp == 0) tc::tmem_alloc(&tmem_base, 256);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t lane = (uint32_t)(warp * 32) << 16;
+    const uint32_t tU = tmem_base + lane, tO = tmem_base + 64 + lane, tS = tmem_base + 128 + lane;
+    const int i = tid;   // state row (value channel)
+    constexpr uint32_t idN64 = tc::idesc_bf16(128, 64), idN128 = tc::idesc_bf16(128, 128);
+
+    if (tid == 0) {
+        issue_group1(ops, blk0, &bar_g1);
+        issue_group2(ops, blk0, &bar_g2);
+    }
+    // the committed state row i into TMEM
+    float *srow = p.state + ((size_t)sl * p.Hv + h) * D * D + (size_t)i * D;
+#pragma unroll 1
+    for (int cb = 0; cb < D / 16; ++cb) {
+        float v[16];
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+            const float4 f = *reinterpret_cast<const float4 *>(srow + cb * 16 + e);
+            v[e] = f.x; v[e + 1] = f.y; v[e + 2] = f.z; v[e + 3] = f.w;
+        }
+        tc::tmem_st16_nowait(tS + cb * 16, v);
+    }
+    tc::tmem_wait_st();
+
+    // chunk 0's gamma_C; later chunks' are read one chunk ahead
+    float gC = *reinterpret_cast<const float *>(blk0 + TcBlock::kMisc);
+    split_and_scale_state(tS, S_hi, S_lo, i, gC);
+
+    bool ok = true;
+#pragma unroll 1
+    for (int c = 0; c < n_chunks && ok; ++c) {
+        const unsigned char *blk = blk0 + (size_t)c * blk_stride;
+        const bool more = c + 1 < n_chunks;
+        const int start = lo + c * C;
+        const int n = min(C, hi - start);
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();   // S operand written; the previous chunk's O readout is done
+        tc::fence_after_sync();
+        if (fail) {   // read after a barrier: the same value in every thread
+            ok = false;
+            break;
+        }
+
+        // group 1: U^T = S0 W^T (committed on its own), then O^T = S0 Q~^T
+        if (tid == 0) {
+            if (!tc::mbar_wait(&bar_g1, c & 1, kWaitLimit)) {
+                fail = 1;
+                tc::mma_commit(&bar_u);
+            } else {
+                const uint32_t a_hi = tc::smem_u32(S_hi), a_lo = tc::smem_u32(S_lo);
+                const uint32_t w_hi = tc::smem_u32(ops + TcBlock::kW), w_lo = w_hi + 16384;
+                const uint32_t q_hi = tc::smem_u32(ops + TcBlock::kQ), q_lo = q_hi + 16384;
+                tc::mma_bf16(tmem_base, a_hi, w_hi, D, idN64, false);
+                tc::mma_bf16(tmem_base, a_hi, w_lo, D, idN64, true);
+                tc::mma_bf16(tmem_base, a_lo, w_hi, D, idN64, true);
+                tc::mma_commit(&bar_u);
+                tc::mma_bf16(tmem_base + 64, a_hi, q_hi, D, idN64, false);
+                tc::mma_bf16(tmem_base + 64, a_hi, q_lo, D, idN64, true);
+                tc::mma_bf16(tmem_base + 64, a_lo, q_hi, D, idN64, true);
+            }
+        }
+        // while the MMAs run: this chunk's U~^T row (pulled toward L2 one
+        // chunk ahead), the next chunk's gamma_C, and an L2 prefetch of the
+        // next chunk's U~^T row
+        float4 ut[C / 4];
+        {
+            const float4 *src = reinterpret_cast<const float4 *>(blk + TcBlock::kUt) + i * (C / 4);
+#pragma unroll
+            for (int e = 0; e < C / 4; ++e) ut[e] = src[e];
+        }
+        float gC_nx = 0.0f;
+        if (more) {
+            const unsigned char *nb = blk + blk_stride;
+            gC_nx = *reinterpret_cast<const float *>(nb + TcBlock::kMisc);
+            const unsigned char *nu = nb + TcBlock::kUt + (size_t)i * C * 4;
+            prefetch_l2(nu);
+            prefetch_l2(nu + 128);
+        }
+        if (!tc::mbar_wait(&bar_u, c & 1, kWaitLimit)) fail = 1;
+        tc::fence_after_sync();
+
+        // U = U~ - S0 W^T (fp32), then its bf16 hi/lo operand (row i, K = t)
+        {
+            uint32_t r[C / 16][16];
+#pragma unroll
+            for (int q = 0; q < C / 16; ++q) tc::tmem_ld16_nowait(tU + q * 16, r[q]);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < C / 16; ++q) {
+                float a[8], b[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 u = ut[q * 4 + e];
+                    const float uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) {
+                        const float d = __fsub_rn(uu[f], __uint_as_float(r[q][4 * e + f]));
+                        if (4 * e + f < 8) a[4 * e + f] = d;
+                        else b[4 * e + f - 8] = d;
+                    }
+                }
+                store_split8(U_hi, U_lo, i, q * 16, C, a);
+                store_split8(U_hi, U_lo, i, q * 16 + 8, C, b);
+            }
+        }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (fail) {
+            ok = false;
+            break;
+        }
+
+        // group 2: S += U^T K~ (committed on its own), then O^T += U^T P^T
+        if (tid == 0) {
+            if (!tc::mbar_wait(&bar_g2, c & 1, kWaitLimit)) {
+                fail = 1;
+                tc::mma_commit(&bar_s);
+                tc::mma_commit(&bar_o);
+            } else {
+                const uint32_t a_hi = tc::smem_u32(U_hi), a_lo = tc::smem_u32(U_lo);
+                const uint32_t p_hi = tc::smem_u32(ops + TcBlock::kP), p_lo = p_hi + 8192;
+                const uint32_t k_hi = tc::smem_u32(ops + TcBlock::kK), k_lo = k_hi + 16384;
+                tc::mma_bf16(tmem_base + 128, a_hi, k_hi, C, idN128, true);
+                tc::mma_bf16(tmem_base + 128, a_hi, k_lo, C, idN128, true);
+                tc::mma_bf16(tmem_base + 128, a_lo, k_hi, C, idN128, true);
+                tc::mma_commit(&bar_s);
+                tc::mma_bf16(tmem_base + 64, a_hi, p_hi, C, idN64, true);
+                tc::mma_bf16(tmem_base + 64, a_hi, p_lo, C, idN64, true);
+                tc::mma_bf16(tmem_base + 64, a_lo, p_hi, C, idN64, true);
+                tc::mma_commit(&bar_o);
+            }
+        }
+        if (!tc::mbar_wait(&bar_s, c & 1, kWaitLimit)) fail = 1;
+        tc::fence_after_sync();
+        // every group-1 MMA is done too: W | Q~ may be refilled
+        if (tid == 0 && more && !fail) issue_group1(ops, blk + blk_stride, &bar_g1);
+        if (more && !fail) {
+            gC = gC_nx;
+            split_and_scale_state(tS, S_hi, S_lo, i, gC);   // the next chunk's S operand
+        }
+        if (!tc::mbar_wait(&bar_o, c & 1, kWaitLimit)) fail = 1;
+        tc::fence_after_sync();
+        if (tid == 0 && more && !fail) issue_group2(ops, blk + blk_stride, &bar_g2);
+
+        // O^T row i -> O[t][i] for the chunk's live rows
+        {
+            uint32_t r[C / 16][16];
+#pragma unroll
+            for (int q = 0; q < C / 16; ++q) tc::tmem_ld16_nowait(tO + q * 16, r[q]);
+            tc::tmem_wait_ld();
+            float *ocol = p.ws_out + ((size_t)start * p.Hv + h) * D + i;
+#pragma unroll
+            for (int q = 0; q < C / 16; ++q)
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (q * 16 + e < n) ocol[(size_t)(q * 16 + e) * p.Hv * D] = __uint_as_float(r[q][e]);
+        }
+    }
+    __syncthreads();
+    ok = fail == 0;
+
+    if (ok) {
+        // final state row i back to the slot
+#pragma unroll 1
+        for (int cb = 0; cb < D / 16; ++cb) {
+            float v[16];
+            tc::tmem_ld16(tS + cb * 16, v);
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+                *reinterpret_cast<float4 *>(srow + cb * 16 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        }
+        // the slot's new conv tail (as in the CUDA-core scan)
+        const int kh = h / p.G;
+        const bool lead = (h % p.G) == 0;
+        const size_t CH = (size_t)p.CH;
+        for (int cc = tid; cc < 3 * D; cc += kScanTcThreads) {
+            const int part = cc / D;
+            if (part < 2 && !lead) continue;
+            const int ch = pchannel<D>(part, cc - part * D, p.Hk, kh, h);
+            uint16_t *tl = p.tail + (size_t)sl * 3 * CH + ch;
+            const uint16_t old[3] = {tl[0], tl[CH], tl[2 * CH]};
+            uint16_t nw[3];
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+                const int pos = L_s - 3 + m;
+                nw[m] = pos >= 0 ? p.mixed[(size_t)(lo + pos) * CH + ch] : old[3 + pos];
+            }
+            tl[0] = nw[0];
+            tl[CH] = nw[1];
+            tl[2 * CH] = nw[2];
+        }
+    } else if (tid == 0) {
+        raise_error(p.err, GDN_DERR_TIMEOUT);
+    }
+    if (tid == 0) {   // no MMA may still write TMEM when it is freed
+        tc::mma_commit(&bar_end);
+        tc::mbar_wait(&bar_end, 0, kWaitLimit);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
 }
 
 // ---------------------------------------------------------------------------

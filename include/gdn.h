@@ -81,6 +81,7 @@ extern "C" {
 #define GDN_DERR_PARENT    4   /* parent[i] outside [-1, i) (window-local) */
 #define GDN_DERR_KEEP      8   /* keep_row[s] outside [-1, n_rows) */
 #define GDN_DERR_SEQLENS  16   /* cu_seqlens not monotone or > n_tokens */
+#define GDN_DERR_TIMEOUT  32   /* a bounded wait inside a kernel gave up */
 
 #define GDN_MAX_WINDOW 16      /* rows per stream in one window or tree */
 
