@@ -392,11 +392,63 @@ def run_extra(dev, stream, flush, reps=20, only=None):
 
     if only in (None, "tree"):
         out["tree_round_16x16"] = _extra_tree(dev, stream, flush, reps, hbm)
+    if only in (None, "replay"):
+        out["logged_round_replay_commit_16x16"] = _extra_logged_round(dev, stream, flush, reps, hbm)
     if only in (None, "decode"):
         out["decode_24_layers_2b_like"] = _extra_decode(dev, stream, flush, reps, hbm)
     if only in (None, "prefill"):
         out["prefill_27b_like"] = _extra_prefill(dev, stream, flush, reps, hbm, bf16, fp32_alu)
     return out
+
+
+def logged_round_bytes(g: synth.Geometry, n_streams: int, n_rows: int, n_committed: int) -> int:
+    """Window that logs instead of records, plus the replay commit."""
+    tile = g.d_v * g.d_k * 4
+    window = (n_streams * g.n_v_heads * tile + n_streams * 3 * g.channels * 2 + n_rows * 3 * g.channels * 2 +
+              n_rows * (g.channels + g.n_v_heads * g.d_v + 2 * g.n_v_heads) * 2 + n_rows * g.n_v_heads * g.d_v * 2 +
+              n_rows * (g.n_v_heads * (1 + g.d_v) + g.n_k_heads * g.d_k) * 4)
+    replay = n_committed * (2 * g.n_v_heads * tile + 2 * 3 * g.channels * 2)   # logs re-read from L2 not counted
+    return window + replay
+
+
+def _extra_logged_round(dev, stream, flush, reps, hbm):
+    """The verify round with logged rows (decay, write, key) and a replay
+    commit in place of recorded states and a copy commit."""
+    import torch
+    import gated_deltanet_speculative_gb300 as gdn
+    g = GEOM
+    R = N_STREAMS * WINDOW
+    w = synth.layer_weights(g, SEED)
+    cache = synth.slot_cache(g, N_STREAMS, SEED)
+    rows = synth.row_inputs(g, R, SEED)
+    rp = synth.row_ptr([WINDOW] * N_STREAMS)
+    rng = np.random.default_rng([SEED, 7])
+    acc = synth.accepted_lengths(N_STREAMS, WINDOW, rng)
+    keep = np.where(acc > 0, rp[:-1] + acc - 1, -1).astype(np.int32)
+    d = gdn.Dims(g.n_k_heads, g.n_v_heads, g.d_k, g.d_v)
+    dw = {"conv_w": _bf(w["conv_w"]).to(dev), "A_log": torch.from_numpy(w["A_log"]).to(dev),
+          "dt_bias": torch.from_numpy(w["dt_bias"]).to(dev), "norm_w": _bf(w["norm_w"]).to(dev)}
+    dc = {"state": torch.from_numpy(cache["state"]).to(dev), "tail": _bf(cache["tail"]).to(dev)}
+    dr = {k: _bf(rows[k]).to(dev) for k in ("mixed", "z", "a", "b")}
+    dr["y"] = torch.empty((R, g.n_v_heads, g.d_v), dtype=torch.bfloat16, device=dev)
+    la = torch.empty((R, g.n_v_heads), dtype=torch.float32, device=dev)
+    lu = torch.empty((R, g.n_v_heads, g.d_v), dtype=torch.float32, device=dev)
+    lk = torch.empty((R, g.n_k_heads, g.d_k), dtype=torch.float32, device=dev)
+    rt = torch.empty((R, 3, g.channels), dtype=torch.bfloat16, device=dev)
+    slot_t = torch.arange(N_STREAMS, dtype=torch.int32, device=dev)
+    rp_t = torch.from_numpy(rp).to(dev)
+    keep_t = torch.from_numpy(keep).to(dev)
+
+    def step():
+        gdn.window_log(d, dw, dc, slot_t, rp_t, dr, la, lu, lk, rt, stream)
+        gdn.commit_replay(d, dc, slot_t, rp_t, keep_t, la, lu, lk, rt, stream)
+
+    ms = _timed(step, reps, stream, flush)
+    ms_w = _timed(lambda: gdn.window_log(d, dw, dc, slot_t, rp_t, dr, la, lu, lk, rt, stream), reps, stream, flush)
+    b = logged_round_bytes(g, N_STREAMS, R, int((keep >= 0).sum()))
+    return {"ms_per_round": ms, "rows_per_s": R / (ms * 1e-3), "window_log_ms": ms_w,
+            "algorithmic_gbs": b / (ms * 1e-3) / 1e9, "frac_hbm": b / (ms * 1e-3) / 1e9 / hbm,
+            "algorithmic_bytes": b}
 
 
 def _extra_tree(dev, stream, flush, reps, hbm):
@@ -596,7 +648,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-extra", action="store_true", help="skip the tree / decode / prefill measurements")
-    ap.add_argument("--extra-only", choices=["tree", "decode", "prefill"],
+    ap.add_argument("--extra-only", choices=["tree", "decode", "prefill", "replay"],
                     help="run only this secondary measurement (3 repetitions) and print it; for profiling")
     args = ap.parse_args()
 

@@ -8,5 +8,6 @@ does not load the CUDA library; the first call does (and raises if it is
 missing).
 """
 from . import synth  # noqa: F401
-from ._binding import (Dims, GdnError, MAX_WINDOW, PREFILL_CHUNK, commit, get_device_error,  # noqa: F401
-                       library_path, load, prefill, prefill_workspace_size, step, tree, window)
+from ._binding import (Dims, GdnError, MAX_WINDOW, PREFILL_CHUNK, commit, commit_replay,  # noqa: F401
+                       get_device_error, library_path, load, prefill, prefill_workspace_size, step, tree,
+                       window, window_log)

@@ -63,6 +63,9 @@ _SIGS = {
     "gdn_prefill": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _I, _I,
                     ctypes.POINTER(c_rows), _I, _P, ctypes.c_size_t, _P],
     "gdn_prefill_workspace_size": [ctypes.POINTER(c_dims), _I, _I, _I],
+    "gdn_window_log": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _I, _I,
+                       ctypes.POINTER(c_rows), _P, _P, _P, _P, _P],
+    "gdn_commit_replay": [ctypes.POINTER(c_dims), ctypes.POINTER(c_cache), _P, _P, _P, _I, _I, _P, _P, _P, _P, _P],
     "gdn_status_string": [ctypes.c_int],
     "gdn_get_device_error": [_P, ctypes.POINTER(ctypes.c_int32)],
 }
@@ -215,6 +218,42 @@ def commit(dims: Dims, cache: dict, slot, keep_row, rec_state, rec_tail, stream=
     _need(rec_tail, "rec_tail", torch.bfloat16, (R, 3, dims.channels))
     _check("gdn_commit", lib.gdn_commit(ctypes.byref(dims.c()), ctypes.byref(cc), _ptr(slot), _ptr(keep_row), S, R,
                                         _ptr(rec_state), _ptr(rec_tail), _stream_ptr(stream)))
+
+
+def window_log(dims: Dims, weights: dict, cache: dict, slot, row_ptr, rows: dict, log_a, log_u, log_k, rec_tail,
+               stream=None):
+    """Chain verify windows logging each row's decay, write and key."""
+    lib = load()
+    _need(slot, "slot", torch.int32)
+    S = slot.numel()
+    _need(row_ptr, "row_ptr", torch.int32, (S + 1,))
+    R = rows["mixed"].shape[0]
+    cw, cc, cr = _weights(dims, weights), _cache(dims, cache), _rows(dims, rows, R)
+    _need(log_a, "log_a", torch.float32, (R, dims.n_v_heads))
+    _need(log_u, "log_u", torch.float32, (R, dims.n_v_heads, dims.d_v))
+    _need(log_k, "log_k", torch.float32, (R, dims.n_k_heads, dims.d_k))
+    _need(rec_tail, "rec_tail", torch.bfloat16, (R, 3, dims.channels))
+    _check("gdn_window_log", lib.gdn_window_log(ctypes.byref(dims.c()), ctypes.byref(cw), ctypes.byref(cc),
+                                                _ptr(slot), _ptr(row_ptr), S, R, ctypes.byref(cr), _ptr(log_a),
+                                                _ptr(log_u), _ptr(log_k), _ptr(rec_tail), _stream_ptr(stream)))
+
+
+def commit_replay(dims: Dims, cache: dict, slot, row_ptr, keep_row, log_a, log_u, log_k, rec_tail, stream=None):
+    """Commit by replaying the logged chain up to keep_row[s] (-1: untouched)."""
+    lib = load()
+    _need(slot, "slot", torch.int32)
+    S = slot.numel()
+    _need(row_ptr, "row_ptr", torch.int32, (S + 1,))
+    _need(keep_row, "keep_row", torch.int32, (S,))
+    cc = _cache(dims, cache)
+    R = log_a.shape[0]
+    _need(log_a, "log_a", torch.float32, (R, dims.n_v_heads))
+    _need(log_u, "log_u", torch.float32, (R, dims.n_v_heads, dims.d_v))
+    _need(log_k, "log_k", torch.float32, (R, dims.n_k_heads, dims.d_k))
+    _need(rec_tail, "rec_tail", torch.bfloat16, (R, 3, dims.channels))
+    _check("gdn_commit_replay", lib.gdn_commit_replay(ctypes.byref(dims.c()), ctypes.byref(cc), _ptr(slot),
+                                                      _ptr(row_ptr), _ptr(keep_row), S, R, _ptr(log_a), _ptr(log_u),
+                                                      _ptr(log_k), _ptr(rec_tail), _stream_ptr(stream)))
 
 
 PREFILL_CHUNK = 64

@@ -64,4 +64,81 @@ __global__ void __launch_bounds__(kCommitThreads) gdn_commit_kernel(const Commit
     for (size_t i = lo + threadIdx.x; i < hi; i += kCommitThreads) tdst[i] = __ldcs(tsrc + i);
 }
 
+// Replay commit: slot[s] <- the committed state advanced along rows
+// row_ptr[s] .. keep_row[s] of the stream's logged chain window, one rank-1
+// update per row,  S <- u k^T + a S  with the same rounding as the window
+// (fma(u_i, k_j, a * S_ij)), so the result equals the state the window would
+// have recorded for the kept row, bit for bit.  The conv tail is the kept
+// row's recorded tail.  (TensorFold #932, tree note: "keep replays the kept
+// path onto the recurrence in one pass".)
+struct ReplayParams {
+    int Hk, Hv, G, CH;
+    float *state;
+    uint16_t *tail;
+    int n_slots;
+    const int *slot;
+    const int *row_ptr;
+    const int *keep_row;
+    int n_rows;
+    const float *log_a;       // [R, Hv]
+    const float *log_u;       // [R, Hv, D]
+    const float *log_k;       // [R, Hk, D]
+    const uint16_t *rec_tail; // bf16 [R, 3, CH]
+    int *err;
+};
+
+constexpr int kReplayThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kReplayThreads) gdn_commit_replay_kernel(const ReplayParams p) {
+    constexpr int RPW = D / 8, CPL = D / 32;
+    __shared__ __align__(16) float us[GDN_MAX_WINDOW][D];
+    __shared__ __align__(16) float ks[GDN_MAX_WINDOW][D];
+    __shared__ float as[GDN_MAX_WINDOW];
+    const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int kr = __ldg(p.keep_row + s);
+    if (kr == -1) return;   // nothing accepted: the slot keeps its bits
+    const int sl = __ldg(p.slot + s), r0 = __ldg(p.row_ptr + s), r1 = __ldg(p.row_ptr + s + 1);
+    const bool bad_slot = sl < 0 || sl >= p.n_slots;
+    const bool bad_keep = r0 < 0 || r1 > p.n_rows || kr < r0 || kr >= r1 || kr - r0 >= GDN_MAX_WINDOW;
+    if (bad_slot || bad_keep) {
+        if (h == 0 && tid == 0) raise_error(p.err, bad_slot ? GDN_DERR_SLOT : GDN_DERR_KEEP);
+        return;
+    }
+    const int n = kr - r0 + 1, kh = h / p.G;
+    for (int i = tid; i < n * D / 4; i += kReplayThreads) {   // the path's logs into shared memory
+        const int t = i / (D / 4), c4 = (i - t * (D / 4)) * 4;
+        cp_async16(&us[t][c4], p.log_u + ((size_t)(r0 + t) * p.Hv + h) * D + c4);
+        cp_async16(&ks[t][c4], p.log_k + ((size_t)(r0 + t) * p.Hk + kh) * D + c4);
+    }
+    if (tid < n) as[tid] = __ldg(p.log_a + (size_t)(r0 + tid) * p.Hv + h);
+    float S[RPW][CPL];
+    float *tile = p.state + ((size_t)sl * p.Hv + h) * D * D;
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) S[r][c] = tile[(size_t)(warp * RPW + r) * D + lane * CPL + c];
+    cp_async_wait_all();
+    __syncthreads();
+    for (int t = 0; t < n; ++t) {
+        const float a = as[t];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const float ur = us[t][warp * RPW + r];
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) S[r][c] = __fmaf_rn(ur, ks[t][lane * CPL + c], __fmul_rn(a, S[r][c]));
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) tile[(size_t)(warp * RPW + r) * D + lane * CPL + c] = S[r][c];
+    // this CTA's share of the kept row's tail, in 16-byte units
+    const size_t units = (size_t)3 * p.CH / 8;
+    const size_t lo = units * h / p.Hv, hi = units * (h + 1) / p.Hv;
+    const uint4 *tsrc = reinterpret_cast<const uint4 *>(p.rec_tail + (size_t)kr * 3 * p.CH);
+    uint4 *tdst = reinterpret_cast<uint4 *>(p.tail + (size_t)sl * 3 * p.CH);
+    for (size_t i = lo + tid; i < hi; i += kReplayThreads) tdst[i] = __ldcs(tsrc + i);
+}
+
 }  // namespace gdn

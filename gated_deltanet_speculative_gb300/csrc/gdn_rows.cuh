@@ -25,7 +25,10 @@
 
 namespace gdn {
 
-enum RowMode : int { kStep = 0, kWindow = 1, kTree = 2 };
+// kWindowLog: a chain window that logs each row's decay, write u and key
+// instead of recording its state (TensorFold #932, tree note: each stream
+// logs its rows' decay, write and key, and keep replays the kept path).
+enum RowMode : int { kStep = 0, kWindow = 1, kTree = 2, kWindowLog = 3 };
 
 struct RowParams {
     int Hk, Hv, G, CH;
@@ -48,6 +51,9 @@ struct RowParams {
     int n_rows;
     float *rec_state;         // [R, Hv, D, D]
     uint16_t *rec_tail;       // bf16 [R, 3, CH]
+    float *log_a;             // [R, Hv] decay (kWindowLog)
+    float *log_u;             // [R, Hv, D] write u = b (v - a S k) (kWindowLog)
+    float *log_k;             // [R, Hk, D] normalised key (kWindowLog)
     int *err;                 // device error word
 };
 
@@ -308,6 +314,12 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         acc = warp_sum(acc);
         if (lane == 0) sm.kq[t] = acc;
     }
+    if (MODE == kWindowLog) {   // the rows' decay (every head) and normalised key (lead head of the group)
+        if (tid < n) p.log_a[(size_t)(r0 + tid) * p.Hv + h] = sm.decay[tid];
+        if (lead)
+            for (int i = tid; i < n * D; i += kRowThreads)
+                p.log_k[((size_t)(r0 + i / D) * p.Hk + kh) * D + i % D] = sm.k[i / D][i % D];
+    }
     __syncthreads();
 
     // ---- a5 + a6: the recurrence, row by row; no CTA barrier inside --------
@@ -351,10 +363,12 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
 #pragma unroll
             for (int c = 0; c < CPL; ++c) S[r][c] = __fmaf_rn(ur, kk[c], __fmul_rn(dec, S[r][c]));
         }
-        if (MODE != kStep) {
+        if (MODE == kWindow || MODE == kTree) {
             const bool streaming = !(MODE == kTree && sm.reused[t]);
             store_tile<D, RPW, CPL>(p.rec_state + ((size_t)(r0 + t) * p.Hv + h) * tile, S, warp, lane, streaming);
         }
+        if (MODE == kWindowLog && lane < 16 && (lane & ((1 << SHIFT) - 1)) == 0)
+            p.log_u[((size_t)(r0 + t) * p.Hv + h) * D + warp * RPW + vi] = u;
     }
     if (MODE == kStep) store_tile<D, RPW, CPL>(slot_tile, S, warp, lane, false);
     __syncthreads();

@@ -235,6 +235,37 @@ int gdn_prefill_noalloc(const gdn_dims *dims, const gdn_weights *w, const gdn_ca
                         const int32_t *slot, const int32_t *cu_seqlens, int32_t n_seqs,
                         int32_t n_tokens, const gdn_rows *rows, int32_t chunk, void *stream);
 
+/*
+ * gdn_window_log -- chain verify windows that log instead of record
+ * ([P932] tree note: "A verify no longer snapshots every row's state (1.3 GB
+ * shared, which capped the 27B at 8 rows): each stream logs its rows'
+ * decay, write and key, and keep replays the kept path onto the recurrence
+ * in one pass").  As gdn_window (same y and rec_tail, bit for bit), but in
+ * place of rec_state it writes, for every row r:
+ *   log_a  device fp32 [R, Hv]         the decay a_r
+ *   log_u  device fp32 [R, Hv, d_v]    the write u_r = b_r (v_r - a_r S_{r-1} k_r)
+ *   log_k  device fp32 [R, Hk, d_k]    the normalised key k_r (per key head)
+ * so that S_r = a_r S_{r-1} + u_r k_r^T.  About 1 KiB per row and head
+ * instead of 64 KiB.
+ */
+int gdn_window_log(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
+                   const int32_t *slot, const int32_t *row_ptr, int32_t n_streams,
+                   int32_t n_rows, const gdn_rows *rows, float *log_a, float *log_u,
+                   float *log_k, void *rec_tail, void *stream);
+
+/*
+ * gdn_commit_replay -- commit after gdn_window_log: for stream s with
+ * keep_row[s] = r in [row_ptr[s], row_ptr[s+1]), the slot's state is
+ * advanced along rows row_ptr[s] .. r with S <- a S + u k^T, in the window's
+ * own rounding, so it equals bit for bit what gdn_window would have recorded
+ * for row r; the tail becomes rec_tail[r].  keep_row[s] = -1 leaves the
+ * slot bit-unchanged.  Slots must be distinct.
+ */
+int gdn_commit_replay(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot,
+                      const int32_t *row_ptr, const int32_t *keep_row, int32_t n_streams,
+                      int32_t n_rows, const float *log_a, const float *log_u,
+                      const float *log_k, const void *rec_tail, void *stream);
+
 /* Text for a status code (static storage). */
 const char *gdn_status_string(int status);
 

@@ -1,0 +1,96 @@
+"""Logged windows and replay commit (TensorFold #932, tree note: each stream
+logs its rows' decay, write and key, and keep replays the kept path onto the
+recurrence in one pass).
+
+gdn_window_log must give gdn_window's y and tails bit for bit, its logs must
+be the oracle's per-row decay and key (to tolerance) and satisfy
+S_r = a_r S_{r-1} + u_r k_r^T against the recorded states, and
+gdn_commit_replay must leave every slot exactly as gdn_commit does."""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_speculative_gb300 as gdn
+import oracle
+from gated_deltanet_speculative_gb300 import synth
+
+from harness import Case, dev, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _logs(c: Case):
+    g = c.g
+    R = max(c.R, 1)
+    return (torch.full((R, g.n_v_heads), float("nan"), device="cuda"),
+            torch.full((R, g.n_v_heads, g.d_v), float("nan"), device="cuda"),
+            torch.full((R, g.n_k_heads, g.d_k), float("nan"), device="cuda"),
+            torch.full((R, 3, g.channels), float("nan"), dtype=torch.bfloat16, device="cuda"))
+
+
+@pytest.mark.parametrize("g", [synth.LIKE_27B, synth.Geometry(2, 4, 64, 64), synth.Geometry(2, 2, 32, 32)])
+def test_logged_window_and_replay_commit_equal_recorded_path(g):
+    lengths = [16, 5, 1, 16, 9, 0, 12]
+    c = Case(g, lengths, seed=91, n_slots=9)
+    d = c.dims_gpu()
+    w = c.dev_weights()
+    slot, rp = dev(c.slots), dev(c.row_ptr)
+    rng = np.random.default_rng(91)
+    acc = synth.accepted_lengths(c.S, 16, rng)
+    acc = np.minimum(acc, np.array(lengths))
+    acc[0], acc[3] = 0, 16
+    keep = np.where(acc > 0, c.row_ptr[:-1] + acc - 1, -1).astype(np.int32)
+
+    # recorded path
+    cache_r, rows_r = c.dev_cache(), c.dev_rows()
+    rs, rt = c.dev_records()
+    gdn.window(d, w, cache_r, slot, rp, rows_r, rs, rt)
+    gdn.commit(d, cache_r, slot, dev(keep), rs, rt)
+    # logged path
+    cache_l, rows_l = c.dev_cache(), c.dev_rows()
+    la, lu, lk, lt = _logs(c)
+    gdn.window_log(d, w, cache_l, slot, rp, rows_l, la, lu, lk, lt)
+    gdn.commit_replay(d, cache_l, slot, rp, dev(keep), la, lu, lk, lt)
+    assert gdn.get_device_error() == 0
+
+    assert np.array_equal(host_bits(rows_l["y"])[:c.R], host_bits(rows_r["y"])[:c.R])
+    assert np.array_equal(host_bits(lt)[:c.R], host_bits(rt)[:c.R])
+    assert np.array_equal(cache_l["state"].cpu().numpy().view(np.uint32), cache_r["state"].cpu().numpy().view(np.uint32))
+    assert np.array_equal(host_bits(cache_l["tail"]), host_bits(cache_r["tail"]))
+
+    # the logs themselves: decay and key against the oracle, and the rank-1
+    # step against the recorded states
+    la_n, lu_n, lk_n, rs_n = la.cpu().numpy(), lu.cpu().numpy(), lk.cpu().numpy(), rs.cpu().numpy()
+    for s in range(c.S):
+        lo, hi = c.stream_rows(s)
+        if hi == lo:
+            continue
+        r = c.rows
+        sl = int(c.slots[s])
+        ref = oracle.gdn_rows(c.dims_oracle(), c.w, c.cache["state"][sl], c.cache["tail"][sl], r["mixed"][lo:hi],
+                              r["z"][lo:hi], r["a"][lo:hi], r["b"][lo:hi], extras=True)
+        np.testing.assert_allclose(la_n[lo:hi], ref["decay"], rtol=1e-5, atol=1e-7)
+        for hh in range(g.n_v_heads):
+            kh = hh // g.group
+            np.testing.assert_allclose(lk_n[lo:hi, kh], ref["k"][:, hh], rtol=0, atol=2e-6)
+        prev = c.cache["state"][sl].astype(np.float64)
+        for t in range(lo, hi):
+            kk = lk_n[t][np.arange(g.n_v_heads) // g.group]            # [Hv, dk]
+            step = la_n[t][:, None, None] * prev + lu_n[t][:, :, None] * kk[:, None, :]
+            scale = np.abs(rs_n[t]).max()
+            assert np.abs(step - rs_n[t]).max() <= 1e-6 * scale
+            prev = rs_n[t].astype(np.float64)
+
+
+def test_replay_commit_rejects_keep_outside_the_stream_window():
+    g = synth.Geometry(2, 4, 32, 32)
+    c = Case(g, [4, 3], seed=93)
+    d = c.dims_gpu()
+    w, cache, rows = c.dev_weights(), c.dev_cache(), c.dev_rows()
+    la, lu, lk, lt = _logs(c)
+    gdn.window_log(d, w, cache, dev(c.slots), dev(c.row_ptr), rows, la, lu, lk, lt)
+    before = cache["state"].cpu().numpy().copy()
+    bad = np.array([5, -1], np.int32)   # row 5 belongs to stream 1, not stream 0
+    gdn.commit_replay(d, cache, dev(c.slots), dev(c.row_ptr), dev(bad), la, lu, lk, lt)
+    assert gdn.get_device_error() & 8
+    assert np.array_equal(cache["state"].cpu().numpy(), before)
