@@ -17,6 +17,7 @@ path only).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -50,29 +51,51 @@ class _Dims(ctypes.Structure):
                 ("eps_rms", ctypes.c_double)]
 
 
+def _configure(lib):
+    P = ctypes.c_void_p
+    lib.oracle_gdn_rows.restype = ctypes.c_int
+    lib.oracle_gdn_rows.argtypes = [ctypes.POINTER(_Dims), P, P, P, P, ctypes.c_int32, P, P, P,
+                                    P, P, P, P, ctypes.c_int32, ctypes.c_int32,
+                                    P, P, P, P, P, P, P, P, P, P]
+    lib.oracle_gates.restype = None
+    lib.oracle_gates.argtypes = [ctypes.c_double] * 4 + [P, P]
+    lib.oracle_delta_rule.restype = None
+    lib.oracle_delta_rule.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P,
+                                      ctypes.c_double, ctypes.c_double, P]
+    lib.oracle_gated_rmsnorm.restype = None
+    lib.oracle_gated_rmsnorm.argtypes = [ctypes.c_int, P, P, P, ctypes.c_double, P]
+    lib.oracle_l2norm.restype = None
+    lib.oracle_l2norm.argtypes = [ctypes.c_int, P, ctypes.c_double, ctypes.c_double]
+    lib.oracle_chunked_rule.restype = None
+    lib.oracle_chunked_rule.argtypes = [ctypes.c_int] * 4 + [P] * 7
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            P = ctypes.c_void_p
-            lib.oracle_gdn_rows.restype = ctypes.c_int
-            lib.oracle_gdn_rows.argtypes = [ctypes.POINTER(_Dims), P, P, P, P, ctypes.c_int32, P, P, P,
-                                            P, P, P, P, ctypes.c_int32, ctypes.c_int32,
-                                            P, P, P, P, P, P, P, P, P, P]
-            lib.oracle_gates.restype = None
-            lib.oracle_gates.argtypes = [ctypes.c_double] * 4 + [P, P]
-            lib.oracle_delta_rule.restype = None
-            lib.oracle_delta_rule.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P,
-                                              ctypes.c_double, ctypes.c_double, P]
-            lib.oracle_gated_rmsnorm.restype = None
-            lib.oracle_gated_rmsnorm.argtypes = [ctypes.c_int, P, P, P, ctypes.c_double, P]
-            lib.oracle_l2norm.restype = None
-            lib.oracle_l2norm.argtypes = [ctypes.c_int, P, ctypes.c_double, ctypes.c_double]
-            lib.oracle_chunked_rule.restype = None
-            lib.oracle_chunked_rule.argtypes = [ctypes.c_int] * 4 + [P] * 7
-            _lib = lib
+            _lib = _configure(ctypes.CDLL(build()))
     return _lib
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Route every oracle call through another build of gdn_oracle.c (the
+    mutation tests use it to check that the pins catch planted mistakes)."""
+    global _lib
+    _load()
+    with _lock:
+        old, _lib = _lib, _configure(ctypes.CDLL(path))
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = old
+
+
+def source_path() -> str:
+    return _SRC
 
 
 def _ptr(a):
