@@ -860,9 +860,9 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     if (tid == 0) {
         constexpr uint32_t idn = tc::idesc_bf16(128, C);
         const uint32_t ah = tc::smem_u32(kq_hi), al = tc::smem_u32(kq_lo);
-        tc::mma_bf16(tmem_base, ah, ah, D, idn, false);
-        tc::mma_bf16(tmem_base, ah, al, D, idn, true);
-        tc::mma_bf16(tmem_base, al, ah, D, idn, true);
+        tc::mma_bf16<D>(tmem_base, ah, ah, idn, false);
+        tc::mma_bf16<D>(tmem_base, ah, al, idn, true);
+        tc::mma_bf16<D>(tmem_base, al, ah, idn, true);
         tc::mma_commit(&bar_mma);
     }
     bool ok = tc::mbar_wait(&bar_mma, 0, kPrepWaitLimit);
@@ -943,12 +943,12 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         const uint32_t th = tc::smem_u32(t_hi), tl = tc::smem_u32(t_lo);
         const uint32_t yh = tc::smem_u32(y_hi), yl = tc::smem_u32(y_lo);
         const uint32_t vh = tc::smem_u32(v_hi), vl = tc::smem_u32(v_lo);
-        tc::mma_bf16(tmem_base + 64, yh, th, C, idn, false);
-        tc::mma_bf16(tmem_base + 64, yh, tl, C, idn, true);
-        tc::mma_bf16(tmem_base + 64, yl, th, C, idn, true);
-        tc::mma_bf16(tmem_base + 128, vh, th, C, idn, false);
-        tc::mma_bf16(tmem_base + 128, vh, tl, C, idn, true);
-        tc::mma_bf16(tmem_base + 128, vl, th, C, idn, true);
+        tc::mma_bf16<C>(tmem_base + 64, yh, th, idn, false);
+        tc::mma_bf16<C>(tmem_base + 64, yh, tl, idn, true);
+        tc::mma_bf16<C>(tmem_base + 64, yl, th, idn, true);
+        tc::mma_bf16<C>(tmem_base + 128, vh, th, idn, false);
+        tc::mma_bf16<C>(tmem_base + 128, vh, tl, idn, true);
+        tc::mma_bf16<C>(tmem_base + 128, vl, th, idn, true);
         tc::mma_commit(&bar_mma);
     }
     ok = tc::mbar_wait(&bar_mma, 1, kPrepWaitLimit) && ok;
@@ -1011,7 +1011,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
 // The chunk's operands arrive by 1-D bulk copies in two halves, each issued
 // as soon as the previous chunk's MMAs are done with that half.
 // ---------------------------------------------------------------------------
-constexpr int kScanTcThreads = 128;
+constexpr int kScanTcThreads = 256;   // two threads per TMEM lane, splitting the columns
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr size_t kScanTcSmem = TcBlock::kOpBytes + 65536 + 32768;
 
@@ -1026,33 +1026,31 @@ __device__ __forceinline__ void issue_group2(unsigned char *ops, const unsigned 
         tc::bulk_g2s(ops + TcBlock::kGroup1 + off, blk + TcBlock::kGroup1 + off, 16384, bar);
 }
 
-// S0 (TMEM, row i = this thread) -> bf16 hi/lo A operand in shared memory,
-// and TMEM S <- gamma_C * S0 for the coming U^T K~ accumulation.
+// S0 (TMEM) -> bf16 hi/lo A operand in shared memory, and TMEM S <- gamma_C
+// * S0 for the coming U^T K~ accumulation.  This thread handles row i,
+// columns [half * 64, half * 64 + 64).
 __device__ __forceinline__ void split_and_scale_state(uint32_t tS, unsigned char *S_hi, unsigned char *S_lo, int i,
-                                                      float gC) {
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-        uint32_t r[4][16];
+                                                      int half, float gC) {
+    uint32_t r[4][16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tc::tmem_ld16_nowait(tS + half * 64 + q * 16, r[q]);
-        tc::tmem_wait_ld();
+    for (int q = 0; q < 4; ++q) tc::tmem_ld16_nowait(tS + half * 64 + q * 16, r[q]);
+    tc::tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float a[8], b[8], v[16];
+    for (int q = 0; q < 4; ++q) {
+        float a[8], b[8], v[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[q][e]);
+        for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[q][e]);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                a[e] = v[e];
-                b[e] = v[8 + e];
-            }
-            const int col = half * 64 + q * 16;
-            store_split8(S_hi, S_lo, i, col, 128, a);
-            store_split8(S_hi, S_lo, i, col + 8, 128, b);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(gC, v[e]);
-            tc::tmem_st16_nowait(tS + col, v);
+        for (int e = 0; e < 8; ++e) {
+            a[e] = v[e];
+            b[e] = v[8 + e];
         }
+        const int col = half * 64 + q * 16;
+        store_split8(S_hi, S_lo, i, col, 128, a);
+        store_split8(S_hi, S_lo, i, col + 8, 128, b);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(gC, v[e]);
+        tc::tmem_st16_nowait(tS + col, v);
     }
     tc::tmem_wait_st();
 }
@@ -1104,9 +1102,10 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t lane = (uint32_t)(warp * 32) << 16;
+    const int quarter = warp & 3, half = warp >> 2;
+    const uint32_t lane = (uint32_t)(quarter * 32) << 16;
     const uint32_t tU = tmem_base + lane, tO = tmem_base + 64 + lane, tS = tmem_base + 128 + lane;
-    const int i = tid;   // state row (value channel)
+    const int i = quarter * 32 + (tid & 31);   // state row (value channel); columns split by `half`
     constexpr uint32_t idN64 = tc::idesc_bf16(128, 64), idN128 = tc::idesc_bf16(128, 128);
 
     if (tid == 0) {
@@ -1116,7 +1115,7 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
     // the committed state row i into TMEM
     float *srow = p.state + ((size_t)sl * p.Hv + h) * D * D + (size_t)i * D;
 #pragma unroll 1
-    for (int cb = 0; cb < D / 16; ++cb) {
+    for (int cb = half * 4; cb < half * 4 + 4; ++cb) {
         float v[16];
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
@@ -1129,7 +1128,7 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
 
     // chunk 0's gamma_C; later chunks' are read one chunk ahead
     float gC = *reinterpret_cast<const float *>(blk0 + TcBlock::kMisc);
-    split_and_scale_state(tS, S_hi, S_lo, i, gC);
+    split_and_scale_state(tS, S_hi, S_lo, i, half, gC);
 
     bool ok = true;
 #pragma unroll 1
@@ -1156,43 +1155,41 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
                 const uint32_t a_hi = tc::smem_u32(S_hi), a_lo = tc::smem_u32(S_lo);
                 const uint32_t w_hi = tc::smem_u32(ops + TcBlock::kW), w_lo = w_hi + 16384;
                 const uint32_t q_hi = tc::smem_u32(ops + TcBlock::kQ), q_lo = q_hi + 16384;
-                tc::mma_bf16(tmem_base, a_hi, w_hi, D, idN64, false);
-                tc::mma_bf16(tmem_base, a_hi, w_lo, D, idN64, true);
-                tc::mma_bf16(tmem_base, a_lo, w_hi, D, idN64, true);
+                tc::mma_bf16<D>(tmem_base, a_hi, w_hi, idN64, false);
+                tc::mma_bf16<D>(tmem_base, a_hi, w_lo, idN64, true);
+                tc::mma_bf16<D>(tmem_base, a_lo, w_hi, idN64, true);
                 tc::mma_commit(&bar_u);
-                tc::mma_bf16(tmem_base + 64, a_hi, q_hi, D, idN64, false);
-                tc::mma_bf16(tmem_base + 64, a_hi, q_lo, D, idN64, true);
-                tc::mma_bf16(tmem_base + 64, a_lo, q_hi, D, idN64, true);
+                tc::mma_bf16<D>(tmem_base + 64, a_hi, q_hi, idN64, false);
+                tc::mma_bf16<D>(tmem_base + 64, a_hi, q_lo, idN64, true);
+                tc::mma_bf16<D>(tmem_base + 64, a_lo, q_hi, idN64, true);
             }
         }
         // while the MMAs run: this chunk's U~^T row (pulled toward L2 one
         // chunk ahead), the next chunk's gamma_C, and an L2 prefetch of the
         // next chunk's U~^T row
-        float4 ut[C / 4];
+        float4 ut[C / 8];   // this thread's half of the row
         {
-            const float4 *src = reinterpret_cast<const float4 *>(blk + TcBlock::kUt) + i * (C / 4);
+            const float4 *src = reinterpret_cast<const float4 *>(blk + TcBlock::kUt) + i * (C / 4) + half * (C / 8);
 #pragma unroll
-            for (int e = 0; e < C / 4; ++e) ut[e] = src[e];
+            for (int e = 0; e < C / 8; ++e) ut[e] = src[e];
         }
         float gC_nx = 0.0f;
         if (more) {
             const unsigned char *nb = blk + blk_stride;
             gC_nx = *reinterpret_cast<const float *>(nb + TcBlock::kMisc);
-            const unsigned char *nu = nb + TcBlock::kUt + (size_t)i * C * 4;
-            prefetch_l2(nu);
-            prefetch_l2(nu + 128);
+            prefetch_l2(nb + TcBlock::kUt + (size_t)i * C * 4 + half * 128);
         }
         if (!tc::mbar_wait(&bar_u, c & 1, kWaitLimit)) fail = 1;
         tc::fence_after_sync();
 
         // U = U~ - S0 W^T (fp32), then its bf16 hi/lo operand (row i, K = t)
         {
-            uint32_t r[C / 16][16];
+            uint32_t r[C / 32][16];
 #pragma unroll
-            for (int q = 0; q < C / 16; ++q) tc::tmem_ld16_nowait(tU + q * 16, r[q]);
+            for (int q = 0; q < C / 32; ++q) tc::tmem_ld16_nowait(tU + half * (C / 2) + q * 16, r[q]);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < C / 16; ++q) {
+            for (int q = 0; q < C / 32; ++q) {
                 float a[8], b[8];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -1205,8 +1202,9 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
                         else b[4 * e + f - 8] = d;
                     }
                 }
-                store_split8(U_hi, U_lo, i, q * 16, C, a);
-                store_split8(U_hi, U_lo, i, q * 16 + 8, C, b);
+                const int col = half * (C / 2) + q * 16;
+                store_split8(U_hi, U_lo, i, col, C, a);
+                store_split8(U_hi, U_lo, i, col + 8, C, b);
             }
         }
         tc::fence_async_smem();
@@ -1228,13 +1226,13 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
                 const uint32_t a_hi = tc::smem_u32(U_hi), a_lo = tc::smem_u32(U_lo);
                 const uint32_t p_hi = tc::smem_u32(ops + TcBlock::kP), p_lo = p_hi + 8192;
                 const uint32_t k_hi = tc::smem_u32(ops + TcBlock::kK), k_lo = k_hi + 16384;
-                tc::mma_bf16(tmem_base + 128, a_hi, k_hi, C, idN128, true);
-                tc::mma_bf16(tmem_base + 128, a_hi, k_lo, C, idN128, true);
-                tc::mma_bf16(tmem_base + 128, a_lo, k_hi, C, idN128, true);
+                tc::mma_bf16<C>(tmem_base + 128, a_hi, k_hi, idN128, true);
+                tc::mma_bf16<C>(tmem_base + 128, a_hi, k_lo, idN128, true);
+                tc::mma_bf16<C>(tmem_base + 128, a_lo, k_hi, idN128, true);
                 tc::mma_commit(&bar_s);
-                tc::mma_bf16(tmem_base + 64, a_hi, p_hi, C, idN64, true);
-                tc::mma_bf16(tmem_base + 64, a_hi, p_lo, C, idN64, true);
-                tc::mma_bf16(tmem_base + 64, a_lo, p_hi, C, idN64, true);
+                tc::mma_bf16<C>(tmem_base + 64, a_hi, p_hi, idN64, true);
+                tc::mma_bf16<C>(tmem_base + 64, a_hi, p_lo, idN64, true);
+                tc::mma_bf16<C>(tmem_base + 64, a_lo, p_hi, idN64, true);
                 tc::mma_commit(&bar_o);
             }
         }
@@ -1244,7 +1242,7 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
         if (tid == 0 && more && !fail) issue_group1(ops, blk + blk_stride, &bar_g1);
         if (more && !fail) {
             gC = gC_nx;
-            split_and_scale_state(tS, S_hi, S_lo, i, gC);   // the next chunk's S operand
+            split_and_scale_state(tS, S_hi, S_lo, i, half, gC);   // the next chunk's S operand
         }
         if (!tc::mbar_wait(&bar_o, c & 1, kWaitLimit)) fail = 1;
         tc::fence_after_sync();
@@ -1252,16 +1250,18 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
 
         // O^T row i -> O[t][i] for the chunk's live rows
         {
-            uint32_t r[C / 16][16];
+            uint32_t r[C / 32][16];
 #pragma unroll
-            for (int q = 0; q < C / 16; ++q) tc::tmem_ld16_nowait(tO + q * 16, r[q]);
+            for (int q = 0; q < C / 32; ++q) tc::tmem_ld16_nowait(tO + half * (C / 2) + q * 16, r[q]);
             tc::tmem_wait_ld();
             float *ocol = p.ws_out + ((size_t)start * p.Hv + h) * D + i;
 #pragma unroll
-            for (int q = 0; q < C / 16; ++q)
+            for (int q = 0; q < C / 32; ++q)
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    if (q * 16 + e < n) ocol[(size_t)(q * 16 + e) * p.Hv * D] = __uint_as_float(r[q][e]);
+                for (int e = 0; e < 16; ++e) {
+                    const int t = half * (C / 2) + q * 16 + e;
+                    if (t < n) ocol[(size_t)t * p.Hv * D] = __uint_as_float(r[q][e]);
+                }
         }
     }
     __syncthreads();
@@ -1270,7 +1270,7 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
     if (ok) {
         // final state row i back to the slot
 #pragma unroll 1
-        for (int cb = 0; cb < D / 16; ++cb) {
+        for (int cb = half * 4; cb < half * 4 + 4; ++cb) {
             float v[16];
             tc::tmem_ld16(tS + cb * 16, v);
 #pragma unroll

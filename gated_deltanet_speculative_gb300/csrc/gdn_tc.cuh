@@ -44,17 +44,20 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D[M x N] (+)= A[M x K] * B[N x K]^T over K (a multiple of 16), issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint32_t a_saddr, uint32_t b_saddr, int K, uint32_t idesc,
+// D[M x N] (+)= A[M x K] * B[N x K]^T over K (a multiple of 16), issued by
+// one thread.  Step kb starts 256 bytes further into each operand, i.e. +16
+// in the descriptor's address field.
+template <int K>
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint32_t a_saddr, uint32_t b_saddr, uint32_t idesc,
                                          bool accumulate) {
+    const uint64_t a0 = smem_desc(a_saddr, K), b0 = smem_desc(b_saddr, K);
+#pragma unroll
     for (int kb = 0; kb < K / 16; ++kb) {
-        const uint64_t ad = smem_desc(a_saddr + kb * 256, K);
-        const uint64_t bd = smem_desc(b_saddr + kb * 256, K);
         const uint32_t acc = (accumulate || kb > 0) ? 1u : 0u;
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
-            "l"(ad), "l"(bd), "r"(idesc), "r"(acc));
+            "l"(a0 + (uint64_t)(kb * 16)), "l"(b0 + (uint64_t)(kb * 16)), "r"(idesc), "r"(acc));
     }
 }
 
