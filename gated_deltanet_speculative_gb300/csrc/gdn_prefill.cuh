@@ -616,13 +616,15 @@ __global__ void __launch_bounds__(NT, 1) gdn_prefill_scan_kernel(const PrefillPa
 }
 
 // ---------------------------------------------------------------------------
-// prep on the tensor cores (d = 128, C = 64): one CTA of 256 threads per
+// prep on the tensor cores (d = 128, C = 64): one CTA of 512 threads per
 // (value head, global chunk).  The chunk's WY/UT quantities in the form the
 // tensor-core scan consumes (TcBlock):
-//   gates first; conv + SiLU with v written straight into the (diag(b) V)^T
-//   operand; L2 norms of q and k;
+//   gates first; conv + SiLU (16-row pieces of one channel, no per-row
+//   branches) with v written straight into the (diag(b) V)^T operand; L2
+//   norms of q and k, eight rows per warp in one reduce-scatter;
 //   MMA 1:  [K; Q] (128 x 128) * K^T        -> A = K K^T and Q K^T
-//   M = strict_lower(diag(b) Gamma o A),  P = lower(Gamma o Q K^T)
+//   M = strict_lower(diag(b) Gamma o A),  P = lower(Gamma o Q K^T), both
+//   formed straight from the TMEM readout
 //   T = (I + M)^-1 in 16 x 16 blocks on the CUDA cores (fp32)
 //   MMA 2:  (diag(b gamma) K)^T * T^T -> W^T,   (diag(b) V)^T * T^T -> U~^T
 // Every MMA operand is split into bf16 hi + lo and multiplied three times
@@ -632,59 +634,70 @@ __global__ void __launch_bounds__(NT, 1) gdn_prefill_scan_kernel(const PrefillPa
 //   q, k fp32 [64][132]                         0 .. 67584    (q's part holds T fp32 later)
 //   region B                                    67584 .. +131072:
 //     B + 0      staged conv inputs (51456), then the [K; Q] operand hi | lo
-//                (65536), then A / QK fp32 [64][68] x 2 (34816) and the T
-//                operand hi | lo (16384, at B + 34816)
+//                (65536), then A / QK fp32 [64][65] x 2 (33280) and the T
+//                operand hi | lo (16384, at B + 34816); after MMA 2, W fp32
+//                [64][132] (33792) and U~^T fp32 [128][68] (34816, at B + 34816)
 //     B + 65536  (diag(b gamma) K)^T operand hi | lo (32768)
 //     B + 98304  (diag(b) V)^T operand hi | lo (32768)
 //   vectors g, beta, G, eG, eGC [64] each
 // ---------------------------------------------------------------------------
 // One block row of T = (I + M)^-1 (16 x 16 blocks, C = 64): for every
 // block column bj < BI,  T[BI][bj] = -T[BI][BI] * sum_{kb = bj}^{BI-1} M[BI][kb] T[kb][bj].
-// Thread (rr, cc) = (tid / 16, tid % 16) owns row rr, column cc of each block.
-template <int BI>
+// Thread (rr, cc) = (tid / 16, tid % 16) owns row rr, column cc of each
+// block; rows are AS floats apart.
+template <int BI, int AS>
 __device__ __forceinline__ void prep_inverse_block_row(const float *M, float *T, int tid) {
-    constexpr int AS = 68;
-    const int rr = tid / 16, cc = tid % 16;
+    const bool on = tid < 256;
+    const int rr = (tid / 16) & 15, cc = tid % 16;
     float z[BI];
 #pragma unroll
     for (int bj = 0; bj < BI; ++bj) z[bj] = 0.0f;
-    const float *mrow = M + (BI * 16 + rr) * AS;
+    if (on) {
+        const float *mrow = M + (BI * 16 + rr) * AS;
 #pragma unroll
-    for (int kk = 0; kk < BI * 16; ++kk) {
-        const float m = mrow[kk];
+        for (int kk = 0; kk < BI * 16; ++kk) {
+            const float m = mrow[kk];
 #pragma unroll
-        for (int bj = 0; bj < BI; ++bj)
-            if (kk >= bj * 16) z[bj] = __fmaf_rn(m, T[kk * AS + bj * 16 + cc], z[bj]);
+            for (int bj = 0; bj < BI; ++bj)
+                if (kk >= bj * 16) z[bj] = __fmaf_rn(m, T[kk * AS + bj * 16 + cc], z[bj]);
+        }
     }
     __syncthreads();
+    if (on) {
 #pragma unroll
-    for (int bj = 0; bj < BI; ++bj) T[(BI * 16 + rr) * AS + bj * 16 + cc] = z[bj];   // stash Z
+        for (int bj = 0; bj < BI; ++bj) T[(BI * 16 + rr) * AS + bj * 16 + cc] = z[bj];   // stash Z
+    }
     __syncthreads();
     float t[BI];
 #pragma unroll
     for (int bj = 0; bj < BI; ++bj) t[bj] = 0.0f;
-    const float *trow = T + (BI * 16 + rr) * AS + BI * 16;
+    if (on) {
+        const float *trow = T + (BI * 16 + rr) * AS + BI * 16;
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-        const float d = kk <= rr ? trow[kk] : 0.0f;
+        for (int kk = 0; kk < 16; ++kk) {
+            const float d = kk <= rr ? trow[kk] : 0.0f;
 #pragma unroll
-        for (int bj = 0; bj < BI; ++bj) t[bj] = __fmaf_rn(d, T[(BI * 16 + kk) * AS + bj * 16 + cc], t[bj]);
+            for (int bj = 0; bj < BI; ++bj) t[bj] = __fmaf_rn(d, T[(BI * 16 + kk) * AS + bj * 16 + cc], t[bj]);
+        }
     }
     __syncthreads();
+    if (on) {
 #pragma unroll
-    for (int bj = 0; bj < BI; ++bj) T[(BI * 16 + rr) * AS + bj * 16 + cc] = -t[bj];
+        for (int bj = 0; bj < BI; ++bj) T[(BI * 16 + rr) * AS + bj * 16 + cc] = -t[bj];
+    }
     __syncthreads();
 }
 
-constexpr int kPrepTcThreads = 256;
+constexpr int kPrepTcThreads = 512;
 constexpr int kPrepTcLD = 132;
 constexpr size_t kPrepTcQK = 2 * 64 * kPrepTcLD * 4;
 constexpr size_t kPrepTcSmem = kPrepTcQK + 131072 + 5 * 64 * 4;
 
 template <int C>
 __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(const PrefillParams p) {
-    constexpr int D = 128, LD = kPrepTcLD, AS = C + 4;
+    constexpr int D = 128, LD = kPrepTcLD, AS = C + 1;   // odd row stride: column walks across rows hit distinct banks
     static_assert(C == 64, "the tensor-core block layout is for C = 64");
+    static_assert(kPrepTcThreads / 32 * 8 == 2 * C, "the norm step gives each warp eight of the 2C rows");
     extern __shared__ __align__(1024) unsigned char psm[];
     float *q = reinterpret_cast<float *>(psm);
     float *k = q + C * LD;
@@ -697,7 +710,6 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     unsigned char *y_hi = B + 65536, *y_lo = y_hi + 16384;         // (b gamma K)^T [D][C]
     unsigned char *v_hi = B + 98304, *v_lo = v_hi + 16384;         // (b V)^T [D][C]
     float *T = q;                                                  // [C][AS] once q is consumed
-    unsigned char *w_stage = B + 0;                                // W hi | lo after MMA 2 (A / QK, T op dead)
     float *g = reinterpret_cast<float *>(B + 131072);
     float *beta = g + C, *Gc = beta + C, *eG = Gc + C, *eGC = eG + C;
     __shared__ int info[4];
@@ -766,38 +778,46 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         Gc[2 * lane + 1] = run;
     }
 
-    // conv + SiLU down the chunk, one channel per thread, sliding window of
-    // the four taps; q and k to fp32 rows, v straight into (diag(b) V)^T
-    for (int cc = tid; cc < 3 * D; cc += kPrepTcThreads) {
+    // conv + SiLU: work item (16-row piece, channel), a sliding window of the
+    // four taps down the piece; q and k to fp32 rows, v straight into
+    // (diag(b) V)^T.  Rows >= n read unstaged inputs and are replaced by 0
+    // with a select, so the 16 rows carry no branches.
+    constexpr int PR = 16;
+    for (int it = tid; it < (C / PR) * 3 * D; it += kPrepTcThreads) {
+        const int cc = it % (3 * D), t0 = (it / (3 * D)) * PR;   // warp-uniform part and t0
         const int part = cc / D, e = cc - part * D;
         const int c = pchannel<D>(part, e, p.Hk, kh, h);
         const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + (size_t)c * 4));
         const float w0 = bf_bits(wv.x & 0xffffu), w1 = bf_bits(wv.x >> 16);
         const float w2 = bf_bits(wv.y & 0xffffu), w3 = bf_bits(wv.y >> 16);
-        const uint16_t *x = xin + cc;
+        const uint16_t *x = xin + (size_t)t0 * 3 * D + cc;
         float x0 = bf_bits(x[0]), x1 = bf_bits(x[3 * D]), x2 = bf_bits(x[6 * D]);
-        float *dst = part == 0 ? q + e : k + e;
-        for (int t0 = 0; t0 < C; t0 += 8) {
-            float vb[8];
+        float act[PR];
 #pragma unroll
-            for (int e8 = 0; e8 < 8; ++e8) {
-                const int t = t0 + e8;
-                float act = 0.0f;
-                if (t < n) {
-                    const float x3 = bf_bits(x[(size_t)(t + 3) * 3 * D]);
-                    float acc = __fmul_rn(w0, x0);
-                    acc = __fmaf_rn(w1, x1, acc);
-                    acc = __fmaf_rn(w2, x2, acc);
-                    acc = __fmaf_rn(w3, x3, acc);
-                    act = __fdividef(acc, 1.0f + __expf(-acc));   // SiLU; prefill matches steps to tolerance
-                    x0 = x1;
-                    x1 = x2;
-                    x2 = x3;
-                }
-                if (part < 2) dst[t * LD] = act;
-                vb[e8] = __fmul_rn(beta[t], act);
+        for (int r = 0; r < PR; ++r) {
+            const float x3 = bf_bits(x[(size_t)(r + 3) * 3 * D]);
+            float acc = __fmul_rn(w0, x0);
+            acc = __fmaf_rn(w1, x1, acc);
+            acc = __fmaf_rn(w2, x2, acc);
+            acc = __fmaf_rn(w3, x3, acc);
+            const float sv = __fdividef(acc, 1.0f + __expf(-acc));   // SiLU; prefill matches steps to tolerance
+            act[r] = t0 + r < n ? sv : 0.0f;
+            x0 = x1;
+            x1 = x2;
+            x2 = x3;
+        }
+        if (part < 2) {
+            float *dst = (part == 0 ? q : k) + e;
+#pragma unroll
+            for (int r = 0; r < PR; ++r) dst[(t0 + r) * LD] = act[r];
+        } else {
+#pragma unroll
+            for (int h8 = 0; h8 < PR; h8 += 8) {
+                float vb[8];
+#pragma unroll
+                for (int e8 = 0; e8 < 8; ++e8) vb[e8] = __fmul_rn(beta[t0 + h8 + e8], act[h8 + e8]);
+                store_split8(v_hi, v_lo, e, t0 + h8, C, vb);
             }
-            if (part == 2) store_split8(v_hi, v_lo, e, t0, C, vb);
         }
     }
     __syncthreads();
@@ -805,30 +825,54 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         eG[tid] = __expf(Gc[tid]);
         eGC[tid] = __expf(__fsub_rn(Gc[n - 1], Gc[tid]));
     }
-    // L2 norms of q and k rows (one warp per vector), q scaled
-    for (int j = warp; j < 2 * n; j += kPrepTcThreads / 32) {
-        float *x = (j & 1) ? k + (j >> 1) * LD : q + (j >> 1) * LD;
-        const float4 xv = *reinterpret_cast<const float4 *>(x + lane * 4);
-        float ss = __fmul_rn(xv.x, xv.x);
-        ss = __fmaf_rn(xv.y, xv.y, ss);
-        ss = __fmaf_rn(xv.z, xv.z, ss);
-        ss = __fmaf_rn(xv.w, xv.w, ss);
-        ss = warp_sum(ss);
-        const float s = __fmul_rn(rsqrtf(__fadd_rn(ss, p.eps_l2)), (j & 1) ? 1.0f : p.q_scale);
-        *reinterpret_cast<float4 *>(x + lane * 4) =
-            make_float4(__fmul_rn(xv.x, s), __fmul_rn(xv.y, s), __fmul_rn(xv.z, s), __fmul_rn(xv.w, s));
+    // L2 norms of q and k rows, q scaled: warp w takes rows 8w .. 8w+7 of the
+    // interleaved list (q row j/2 for even j, k row j/2 for odd j); one
+    // reduce-scatter leaves row 8w + (lane >> 2)'s sum of squares in lane
+    // `lane`.  Rows >= n are zero and stay zero.
+    {
+        float4 xv[8];
+        float ss[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int j = warp * 8 + m;
+            const float *x = (j & 1) ? k + (j >> 1) * LD : q + (j >> 1) * LD;
+            xv[m] = *reinterpret_cast<const float4 *>(x + lane * 4);
+            float a2 = __fmul_rn(xv[m].x, xv[m].x);
+            a2 = __fmaf_rn(xv[m].y, xv[m].y, a2);
+            a2 = __fmaf_rn(xv[m].z, xv[m].z, a2);
+            ss[m] = __fmaf_rn(xv[m].w, xv[m].w, a2);
+        }
+        const float tot = reduce_scatter<8>(ss, lane);
+        const int jl = warp * 8 + (lane >> 2);
+        const float mine = __fmul_rn(rsqrtf(__fadd_rn(tot, p.eps_l2)), (jl & 1) ? 1.0f : p.q_scale);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int j = warp * 8 + m;
+            const float sc = __shfl_sync(kFull, mine, m * 4);
+            float *x = (j & 1) ? k + (j >> 1) * LD : q + (j >> 1) * LD;
+            *reinterpret_cast<float4 *>(x + lane * 4) =
+                make_float4(__fmul_rn(xv[m].x, sc), __fmul_rn(xv[m].y, sc), __fmul_rn(xv[m].z, sc), __fmul_rn(xv[m].w, sc));
+        }
     }
     __syncthreads();
 
     // operands of MMA 1 and 2, and the Q~ / K~^T outputs (rows fastest across
     // threads: 8 threads fill one 128-byte core matrix)
     unsigned char *blk = reinterpret_cast<unsigned char *>(p.ws_chunks) + ((size_t)gc * p.Hv + h) * TcBlock::kBytes;
-    for (int it = tid; it < 2 * C * (D / 8); it += kPrepTcThreads) {   // [K; Q], rows r, 8 columns j
-        const int r = it % (2 * C), j0 = (it / (2 * C)) * 8;
+    for (int it = tid; it < 2 * C * (D / 8); it += kPrepTcThreads) {   // [K; Q] rows r, 8 columns j; Q~ rows
+        const int r = it % (2 * C), j0 = (it / (2 * C)) * 8;   // r < C is warp-uniform
         const float *src = r < C ? k + r * LD + j0 : q + (r - C) * LD + j0;
         const float4 a4 = *reinterpret_cast<const float4 *>(src), b4 = *reinterpret_cast<const float4 *>(src + 4);
         const float x[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
         store_split8(kq_hi, kq_lo, r, j0, D, x);
+        if (r >= C) {   // Q~ = diag(gamma) Q, zero past the chunk's rows
+            const int t = r - C;
+            const float a = t < n ? eG[t] : 0.0f;
+            float xq[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xq[e] = __fmul_rn(a, x[e]);
+            store_split8(blk + TcBlock::kQ, blk + TcBlock::kQ + 16384, t, j0, D, xq);
+        }
     }
     for (int it = tid; it < D * (C / 8); it += kPrepTcThreads) {   // (b gamma K)^T and K~^T: rows j, 8 t
         const int j = it % D, t0 = (it / D) * 8;
@@ -841,15 +885,6 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         }
         store_split8(y_hi, y_lo, j, t0, C, y);
         store_split8(blk + TcBlock::kK, blk + TcBlock::kK + 16384, j, t0, C, kt);
-    }
-    for (int it = tid; it < C * (D / 8); it += kPrepTcThreads) {   // Q~: rows t, 8 columns j
-        const int t = it % C, j0 = (it / C) * 8;
-        const float a = t < n ? eG[t] : 0.0f;
-        const float4 a4 = *reinterpret_cast<const float4 *>(q + t * LD + j0);
-        const float4 b4 = *reinterpret_cast<const float4 *>(q + t * LD + j0 + 4);
-        const float x[8] = {__fmul_rn(a, a4.x), __fmul_rn(a, a4.y), __fmul_rn(a, a4.z), __fmul_rn(a, a4.w),
-                            __fmul_rn(a, b4.x), __fmul_rn(a, b4.y), __fmul_rn(a, b4.z), __fmul_rn(a, b4.w)};
-        store_split8(blk + TcBlock::kQ, blk + TcBlock::kQ + 16384, t, j0, D, x);
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
@@ -867,30 +902,26 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     }
     bool ok = tc::mbar_wait(&bar_mma, 0, kPrepWaitLimit);
     tc::fence_after_sync();
-    const int quarter = warp & 3, half = warp >> 2;
-    {   // lane r holds row r of [A; QK]; warps w and w + 4 split the 64 columns
+    const int quarter = warp & 3, part = warp >> 2;   // 16 warps: lane quarter x column part
+    {   // lane r holds row r of [A; QK]; the four warps on a lane quarter take
+        // 16 columns each and form M = strict_lower(diag(b) Gamma o A) and
+        // P = lower(Gamma o QK) in registers
         const int r = quarter * 32 + lane;
-        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + half * (C / 2);
-        uint32_t v[C / 32][16];
-#pragma unroll
-        for (int q2 = 0; q2 < C / 32; ++q2) tc::tmem_ld16_nowait(taddr + q2 * 16, v[q2]);
+        uint32_t v[16];
+        tc::tmem_ld16_nowait(tmem_base + ((uint32_t)(quarter * 32) << 16) + part * 16, v);
         tc::tmem_wait_ld();
         __syncthreads();   // every MMA-1 read of the [K; Q] operand is long done; A / QK overwrite it
-        float *dst = r < C ? A + r * AS : QK + (r - C) * AS;
+        const bool isA = r < C;   // warp-uniform
+        const int t = isA ? r : r - C;
+        const float Gt = Gc[t], bt = isA ? beta[t] : 1.0f;
+        float *dst = (isA ? A : QK) + t * AS + part * 16;
 #pragma unroll
-        for (int q2 = 0; q2 < C / 32; ++q2)
-#pragma unroll
-            for (int e = 0; e < 16; ++e) dst[half * (C / 2) + q2 * 16 + e] = __uint_as_float(v[q2][e]);
-    }
-    __syncthreads();
-
-    // M = strict_lower(diag(b) Gamma o A) in place; P = lower(Gamma o QK) in place
-    for (int i = tid; i < C * C; i += kPrepTcThreads) {
-        const int t = i / C, s = i - t * C;
-        const bool live = t < n && s < n;
-        const float gam = live ? __expf(__fsub_rn(Gc[t], Gc[s])) : 0.0f;
-        A[t * AS + s] = (live && s < t) ? __fmul_rn(__fmul_rn(beta[t], gam), A[t * AS + s]) : 0.0f;
-        QK[t * AS + s] = (live && s <= t) ? __fmul_rn(gam, QK[t * AS + s]) : 0.0f;
+        for (int e = 0; e < 16; ++e) {
+            const int sc = part * 16 + e;
+            const bool keep = t < n && sc < n && (isA ? sc < t : sc <= t);
+            const float gam = __expf(__fsub_rn(Gt, Gc[sc]));
+            dst[e] = keep ? __fmul_rn(__fmul_rn(bt, gam), __uint_as_float(v[e])) : 0.0f;
+        }
     }
     __syncthreads();
     for (int it = tid; it < C * (C / 8); it += kPrepTcThreads) {   // P output: rows t, 8 columns s
@@ -921,9 +952,9 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     }
     __syncthreads();
     // ... then block row bi: T_bi,bj = -T_bi,bi * sum_{kb = bj}^{bi-1} M_bi,kb T_kb,bj
-    prep_inverse_block_row<1>(A, T, tid);
-    prep_inverse_block_row<2>(A, T, tid);
-    prep_inverse_block_row<3>(A, T, tid);
+    prep_inverse_block_row<1, AS>(A, T, tid);
+    prep_inverse_block_row<2, AS>(A, T, tid);
+    prep_inverse_block_row<3, AS>(A, T, tid);
     // T operand (rows t, K = s); A and QK are no longer read
     for (int it = tid; it < C * (C / 8); it += kPrepTcThreads) {
         const int t = it % C, s0 = (it / C) * 8;
@@ -953,35 +984,49 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     }
     ok = tc::mbar_wait(&bar_mma, 1, kPrepWaitLimit) && ok;
     tc::fence_after_sync();
+    float *Wf = reinterpret_cast<float *>(B);             // W fp32 [64][LD]
+    float *Uf = reinterpret_cast<float *>(B + 34816);     // U~^T fp32 [128][AU]
+    constexpr int AU = C + 4;
     {
-        // lane j of W^T: W[t][j] for every t (warps 0-3); lane i of U~^T: U~^T[i][t] (warps 4-7)
+        // lane j of W^T: W[t][j] for every t (warps 0-7); lane i of U~^T: U~^T[i][t] (warps 8-15);
+        // two warps per lane quarter and matrix, 32 columns each, into fp32 stages
         const int r = quarter * 32 + lane;
-        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (half ? 128 : 64);
-        uint32_t v[C / 16][16];
+        const bool isU = part >= 2;
+        const int c0 = (part & 1) * (C / 2);
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (isU ? 128 : 64) + c0;
+        uint32_t v[C / 32][16];
 #pragma unroll
-        for (int q2 = 0; q2 < C / 16; ++q2) tc::tmem_ld16_nowait(taddr + q2 * 16, v[q2]);
+        for (int q2 = 0; q2 < C / 32; ++q2) tc::tmem_ld16_nowait(taddr + q2 * 16, v[q2]);
         tc::tmem_wait_ld();
-        if (half == 0) {   // W (rows t, K = j) hi | lo into shared memory (the dead [K; Q] region)
+        if (!isU) {   // column r of W: consecutive lanes, consecutive banks
 #pragma unroll
-            for (int q2 = 0; q2 < C / 16; ++q2)
+            for (int q2 = 0; q2 < C / 32; ++q2)
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    store_split(w_stage, w_stage + 16384, q2 * 16 + e, r, D, __uint_as_float(v[q2][e]));
-        } else {
-            float4 *ut = reinterpret_cast<float4 *>(blk + TcBlock::kUt) + r * (C / 4);
+                for (int e = 0; e < 16; ++e) Wf[(c0 + q2 * 16 + e) * LD + r] = __uint_as_float(v[q2][e]);
+        } else {      // row r of U~^T as float4s (eight lanes cover the 32 banks)
+            float4 *ur = reinterpret_cast<float4 *>(Uf + r * AU + c0);
 #pragma unroll
-            for (int q2 = 0; q2 < C / 16; ++q2)
+            for (int q2 = 0; q2 < C / 32; ++q2)
 #pragma unroll
                 for (int e = 0; e < 16; e += 4)
-                    ut[q2 * 4 + e / 4] = make_float4(__uint_as_float(v[q2][e]), __uint_as_float(v[q2][e + 1]),
+                    ur[q2 * 4 + e / 4] = make_float4(__uint_as_float(v[q2][e]), __uint_as_float(v[q2][e + 1]),
                                                      __uint_as_float(v[q2][e + 2]), __uint_as_float(v[q2][e + 3]));
         }
     }
     __syncthreads();
-    {   // the staged W, hi then lo, to the workspace as 16-byte stores
-        const uint4 *src = reinterpret_cast<const uint4 *>(w_stage);
-        uint4 *dst = reinterpret_cast<uint4 *>(blk + TcBlock::kW);
-        for (int it = tid; it < 32768 / 16; it += kPrepTcThreads) dst[it] = src[it];
+    for (int it = tid; it < C * (D / 8); it += kPrepTcThreads) {   // W hi | lo, rows t, 8 columns j
+        const int t = it % C, j0 = (it / C) * 8;
+        const float4 a4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0);
+        const float4 b4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0 + 4);
+        const float x[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
+        store_split8(blk + TcBlock::kW, blk + TcBlock::kW + 16384, t, j0, D, x);
+    }
+    {   // U~^T [128][64] fp32, row-major, coalesced 16-byte stores
+        float4 *dst = reinterpret_cast<float4 *>(blk + TcBlock::kUt);
+        for (int it = tid; it < D * C / 4; it += kPrepTcThreads) {
+            const int i = it / (C / 4), t4 = it % (C / 4);
+            dst[it] = *reinterpret_cast<const float4 *>(Uf + i * AU + t4 * 4);
+        }
     }
     if (tid == 0) {
         *reinterpret_cast<float *>(blk + TcBlock::kMisc) = eG[n - 1];
@@ -997,8 +1042,9 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// scan on the tensor cores (d = 128): one CTA of 128 threads per (value
-// head, sequence).  Thread i owns TMEM lane i, i.e. state row i.  TMEM holds
+// scan on the tensor cores (d = 128): one CTA of 256 threads per (value
+// head, sequence).  Threads i and i + 128 (warps w and w + 4) share TMEM lane
+// i, i.e. state row i, and split its columns.  TMEM holds
 // three fp32 accumulators: U^T [128 x 64] (columns 0..63), O^T [128 x 64]
 // (64..127) and the state S [128 x 128] (128..255), which stays in TMEM from
 // chunk to chunk.  Every product is three bf16 MMAs (hi*hi + hi*lo + lo*hi)
