@@ -91,29 +91,14 @@ struct TcBlock {
 };
 static_assert(TcBlock::kBytes == ChunkBlock<128, 64>::kFloats * 4, "tensor-core block must match the fp32 block size");
 
-// Store x at element (r, k) of a K-major bf16 operand (K columns) as hi in
-// `hi_base` and lo in `lo_base`.
-__device__ __forceinline__ void store_split(unsigned char *hi_base, unsigned char *lo_base, int r, int k, int K,
-                                            float x) {
-    uint16_t h, l;
-    tc::split_bf16(x, h, l);
-    const uint32_t off = tc::kmajor_offset(r, k, K);
-    *reinterpret_cast<uint16_t *>(hi_base + off) = h;
-    *reinterpret_cast<uint16_t *>(lo_base + off) = l;
-}
-
-// Store 8 consecutive k (k0 multiple of 8) of row r as two 16-byte writes.
+// Store 8 consecutive k (k0 multiple of 8) of row r of a K-major bf16
+// operand (K columns), split x = hi + lo: hi into `hi_base`, lo into
+// `lo_base`, one 16-byte write each.
 __device__ __forceinline__ void store_split8(unsigned char *hi_base, unsigned char *lo_base, int r, int k0, int K,
                                              const float (&x)[8]) {
     uint32_t hw[4], lw[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint16_t h0, l0, h1, l1;
-        tc::split_bf16(x[2 * j], h0, l0);
-        tc::split_bf16(x[2 * j + 1], h1, l1);
-        hw[j] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-        lw[j] = (uint32_t)l0 | ((uint32_t)l1 << 16);
-    }
+    for (int j = 0; j < 4; ++j) tc::split_bf16x2(x[2 * j], x[2 * j + 1], hw[j], lw[j]);
     const uint32_t off = tc::kmajor_offset(r, k0, K);
     *reinterpret_cast<uint4 *>(hi_base + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     *reinterpret_cast<uint4 *>(lo_base + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
@@ -625,7 +610,8 @@ __global__ void __launch_bounds__(NT, 1) gdn_prefill_scan_kernel(const PrefillPa
 //   MMA 1:  [K; Q] (128 x 128) * K^T        -> A = K K^T and Q K^T
 //   M = strict_lower(diag(b) Gamma o A),  P = lower(Gamma o Q K^T), both
 //   formed straight from the TMEM readout
-//   T = (I + M)^-1 in 16 x 16 blocks on the CUDA cores (fp32)
+//   T = (I + M)^-1 on the CUDA cores (fp32): 16 x 16 diagonal blocks by
+//   forward substitution, the rest by two levels of block doubling
 //   MMA 2:  (diag(b gamma) K)^T * T^T -> W^T,   (diag(b) V)^T * T^T -> U~^T
 // Every MMA operand is split into bf16 hi + lo and multiplied three times
 // (hi hi + hi lo + lo hi), accumulating in fp32.
@@ -641,53 +627,6 @@ __global__ void __launch_bounds__(NT, 1) gdn_prefill_scan_kernel(const PrefillPa
 //     B + 98304  (diag(b) V)^T operand hi | lo (32768)
 //   vectors g, beta, G, eG, eGC [64] each
 // ---------------------------------------------------------------------------
-// One block row of T = (I + M)^-1 (16 x 16 blocks, C = 64): for every
-// block column bj < BI,  T[BI][bj] = -T[BI][BI] * sum_{kb = bj}^{BI-1} M[BI][kb] T[kb][bj].
-// Thread (rr, cc) = (tid / 16, tid % 16) owns row rr, column cc of each
-// block; rows are AS floats apart.
-template <int BI, int AS>
-__device__ __forceinline__ void prep_inverse_block_row(const float *M, float *T, int tid) {
-    const bool on = tid < 256;
-    const int rr = (tid / 16) & 15, cc = tid % 16;
-    float z[BI];
-#pragma unroll
-    for (int bj = 0; bj < BI; ++bj) z[bj] = 0.0f;
-    if (on) {
-        const float *mrow = M + (BI * 16 + rr) * AS;
-#pragma unroll
-        for (int kk = 0; kk < BI * 16; ++kk) {
-            const float m = mrow[kk];
-#pragma unroll
-            for (int bj = 0; bj < BI; ++bj)
-                if (kk >= bj * 16) z[bj] = __fmaf_rn(m, T[kk * AS + bj * 16 + cc], z[bj]);
-        }
-    }
-    __syncthreads();
-    if (on) {
-#pragma unroll
-        for (int bj = 0; bj < BI; ++bj) T[(BI * 16 + rr) * AS + bj * 16 + cc] = z[bj];   // stash Z
-    }
-    __syncthreads();
-    float t[BI];
-#pragma unroll
-    for (int bj = 0; bj < BI; ++bj) t[bj] = 0.0f;
-    if (on) {
-        const float *trow = T + (BI * 16 + rr) * AS + BI * 16;
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-            const float d = kk <= rr ? trow[kk] : 0.0f;
-#pragma unroll
-            for (int bj = 0; bj < BI; ++bj) t[bj] = __fmaf_rn(d, T[(BI * 16 + kk) * AS + bj * 16 + cc], t[bj]);
-        }
-    }
-    __syncthreads();
-    if (on) {
-#pragma unroll
-        for (int bj = 0; bj < BI; ++bj) T[(BI * 16 + rr) * AS + bj * 16 + cc] = -t[bj];
-    }
-    __syncthreads();
-}
-
 constexpr int kPrepTcThreads = 512;
 constexpr int kPrepTcLD = 132;
 constexpr size_t kPrepTcQK = 2 * 64 * kPrepTcLD * 4;
@@ -874,18 +813,6 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
             store_split8(blk + TcBlock::kQ, blk + TcBlock::kQ + 16384, t, j0, D, xq);
         }
     }
-    for (int it = tid; it < D * (C / 8); it += kPrepTcThreads) {   // (b gamma K)^T and K~^T: rows j, 8 t
-        const int j = it % D, t0 = (it / D) * 8;
-        float y[8], kt[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float kv = k[(t0 + e) * LD + j];
-            y[e] = __fmul_rn(__fmul_rn(beta[t0 + e], eG[t0 + e]), kv);
-            kt[e] = (t0 + e) < n ? __fmul_rn(eGC[t0 + e], kv) : 0.0f;
-        }
-        store_split8(y_hi, y_lo, j, t0, C, y);
-        store_split8(blk + TcBlock::kK, blk + TcBlock::kK + 16384, j, t0, C, kt);
-    }
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
@@ -899,6 +826,19 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         tc::mma_bf16<D>(tmem_base, ah, al, idn, true);
         tc::mma_bf16<D>(tmem_base, al, ah, idn, true);
         tc::mma_commit(&bar_mma);
+    }
+    // while MMA 1 runs: the (b gamma K)^T operand of MMA 2 and K~^T for the scan
+    for (int it = tid; it < D * (C / 8); it += kPrepTcThreads) {   // (b gamma K)^T and K~^T: rows j, 8 t
+        const int j = it % D, t0 = (it / D) * 8;
+        float y[8], kt[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float kv = k[(t0 + e) * LD + j];
+            y[e] = __fmul_rn(__fmul_rn(beta[t0 + e], eG[t0 + e]), kv);
+            kt[e] = (t0 + e) < n ? __fmul_rn(eGC[t0 + e], kv) : 0.0f;
+        }
+        store_split8(y_hi, y_lo, j, t0, C, y);
+        store_split8(blk + TcBlock::kK, blk + TcBlock::kK + 16384, j, t0, C, kt);
     }
     bool ok = tc::mbar_wait(&bar_mma, 0, kPrepWaitLimit);
     tc::fence_after_sync();
@@ -924,15 +864,9 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         }
     }
     __syncthreads();
-    for (int it = tid; it < C * (C / 8); it += kPrepTcThreads) {   // P output: rows t, 8 columns s
-        const int t = it % C, s0 = (it / C) * 8;
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = QK[t * AS + s0 + e];
-        store_split8(blk + TcBlock::kP, blk + TcBlock::kP + 8192, t, s0, C, x);
-    }
-    // T = (I + M)^-1: the four 16 x 16 diagonal blocks by forward
-    // substitution (one column per thread) ...
+    // T = (I + M)^-1 by 16 x 16 blocks.  Threads < C invert the four diagonal
+    // blocks by forward substitution (one column each) while the others
+    // write P to the workspace.
     if (tid < C) {
         const int b0 = (tid / 16) * 16, c = tid % 16;
         float x[16];
@@ -945,16 +879,73 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) T[(b0 + r) * AS + b0 + c] = x[r];
+    } else {
+        for (int it = tid - C; it < C * (C / 8); it += kPrepTcThreads - C) {   // P: rows t, 8 columns s
+            const int t = it % C, s0 = (it / C) * 8;
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = QK[t * AS + s0 + e];
+            store_split8(blk + TcBlock::kP, blk + TcBlock::kP + 8192, t, s0, C, x);
+        }
     }
     for (int i = tid; i < C * C; i += kPrepTcThreads) {   // zero the strictly upper blocks
         const int t = i / C, s = i - t * C;
         if (s / 16 > t / 16) T[t * AS + s] = 0.0f;
     }
     __syncthreads();
-    // ... then block row bi: T_bi,bj = -T_bi,bi * sum_{kb = bj}^{bi-1} M_bi,kb T_kb,bj
-    prep_inverse_block_row<1, AS>(A, T, tid);
-    prep_inverse_block_row<2, AS>(A, T, tid);
-    prep_inverse_block_row<3, AS>(A, T, tid);
+    // Off-diagonal blocks by doubling: for a block lower-triangular
+    // L = [L11 0; L21 L22], L^-1 has lower-left block -L22^-1 L21 L11^-1.
+    // Level 1 (16-blocks): T10 = -T11 (M10 T00), T32 = -T33 (M32 T22);
+    // level 2 (32-blocks): T[32:, :32] = -T[32:, 32:] (M[32:, :32] T[:32, :32]).
+    // The zero upper halves of the diagonal blocks let every sum run full length.
+    float *X = QK;   // scratch once P is out
+    {
+        const int pr = tid >> 8, rr = (tid >> 4) & 15, cc = tid & 15;
+        const int bi = 2 * pr + 1, bj = 2 * pr;
+        const float *m = A + (bi * 16 + rr) * AS + bj * 16;
+        const float *tb = T + (bj * 16) * AS + bj * 16 + cc;
+        float acc = 0.0f;
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) acc = __fmaf_rn(m[kk], tb[kk * AS], acc);
+        X[(pr * 16 + rr) * AS + cc] = acc;
+        __syncthreads();
+        const float *td = T + (bi * 16 + rr) * AS + bi * 16;
+        const float *xc = X + (pr * 16) * AS + cc;
+        acc = 0.0f;
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) acc = __fmaf_rn(td[kk], xc[kk * AS], acc);
+        T[(bi * 16 + rr) * AS + bj * 16 + cc] = -acc;
+    }
+    __syncthreads();
+    constexpr int H = C / 2;
+#pragma unroll
+    for (int it = tid; it < H * H; it += kPrepTcThreads) {
+        const int r = it / H, c = it % H;
+        const float *m = A + (H + r) * AS;
+        float acc = 0.0f;
+#pragma unroll
+        for (int kk = 0; kk < H; ++kk) acc = __fmaf_rn(m[kk], T[kk * AS + c], acc);
+        X[r * AS + c] = acc;
+    }
+    __syncthreads();
+    {
+        float res[H * H / kPrepTcThreads];
+#pragma unroll
+        for (int u = 0; u < H * H / kPrepTcThreads; ++u) {
+            const int it = tid + u * kPrepTcThreads, r = it / H, c = it % H;
+            const float *td = T + (H + r) * AS + H;
+            float acc = 0.0f;
+#pragma unroll
+            for (int kk = 0; kk < H; ++kk) acc = __fmaf_rn(td[kk], X[kk * AS + c], acc);
+            res[u] = -acc;
+        }
+#pragma unroll
+        for (int u = 0; u < H * H / kPrepTcThreads; ++u) {
+            const int it = tid + u * kPrepTcThreads, r = it / H, c = it % H;
+            T[(H + r) * AS + c] = res[u];
+        }
+    }
+    __syncthreads();
     // T operand (rows t, K = s); A and QK are no longer read
     for (int it = tid; it < C * (C / 8); it += kPrepTcThreads) {
         const int t = it % C, s0 = (it / C) * 8;

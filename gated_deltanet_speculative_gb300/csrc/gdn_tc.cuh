@@ -169,13 +169,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Split fp32 x into bf16 hi + lo (hi = rn(x), lo = rn(x - hi)); returns the
-// two 16-bit patterns packed hi | lo << 16.
-__device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    const __nv_bfloat16 l = __float2bfloat16_rn(__fsub_rn(x, __bfloat162float(h)));
-    hi = __bfloat16_as_ushort(h);
-    lo = __bfloat16_as_ushort(l);
+// Split the fp32 pair (x0, x1) into bf16 hi + lo (hi = rn(x), lo = rn(x -
+// hi)), each pair packed in one word with x0 in the low 16 bits.
+// cvt.rn.bf16x2.f32 d, a, b puts rn(a) in the upper half and rn(b) in the lower.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(x1), "f"(x0));
+    const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(__fsub_rn(x1, h1)), "f"(__fsub_rn(x0, h0)));
 }
 
 }  // namespace tc
