@@ -1049,8 +1049,15 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
 // as soon as the previous chunk's MMAs are done with that half.
 // ---------------------------------------------------------------------------
 constexpr int kScanTcThreads = 256;   // two threads per TMEM lane, splitting the columns
+constexpr int kScanPrefetchAhead = 2;   // chunk blocks pulled into L2 this many chunks early
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr size_t kScanTcSmem = TcBlock::kOpBytes + 65536 + 32768;
+
+// One chunk block (TcBlock::kBytes) toward L2, in 16 KB pieces.
+__device__ __forceinline__ void prefetch_block_l2(const unsigned char *blk) {
+    for (int off = 0; off < TcBlock::kBytes; off += 16384)
+        tc::bulk_prefetch_l2(blk + off, (uint32_t)min(16384, TcBlock::kBytes - off));
+}
 
 __device__ __forceinline__ void issue_group1(unsigned char *ops, const unsigned char *blk, uint64_t *bar) {
     tc::mbar_expect_tx(bar, TcBlock::kGroup1);
@@ -1148,6 +1155,7 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
     if (tid == 0) {
         issue_group1(ops, blk0, &bar_g1);
         issue_group2(ops, blk0, &bar_g2);
+        for (int c = 1; c < kScanPrefetchAhead && c < n_chunks; ++c) prefetch_block_l2(blk0 + (size_t)c * blk_stride);
     }
     // the committed state row i into TMEM
     float *srow = p.state + ((size_t)sl * p.Hv + h) * D * D + (size_t)i * D;
@@ -1182,6 +1190,7 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
             ok = false;
             break;
         }
+        if (tid == 0 && c + kScanPrefetchAhead < n_chunks) prefetch_block_l2(blk + kScanPrefetchAhead * blk_stride);
 
         // group 1: U^T = S0 W^T (committed on its own), then O^T = S0 Q~^T
         if (tid == 0) {
@@ -1201,9 +1210,8 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
                 tc::mma_bf16<D>(tmem_base + 64, a_lo, q_hi, idN64, true);
             }
         }
-        // while the MMAs run: this chunk's U~^T row (pulled toward L2 one
-        // chunk ahead), the next chunk's gamma_C, and an L2 prefetch of the
-        // next chunk's U~^T row
+        // while the MMAs run: this chunk's U~^T row and the next chunk's
+        // gamma_C (both in blocks already pulled toward L2)
         float4 ut[C / 8];   // this thread's half of the row
         {
             const float4 *src = reinterpret_cast<const float4 *>(blk + TcBlock::kUt) + i * (C / 4) + half * (C / 8);
@@ -1214,7 +1222,6 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
         if (more) {
             const unsigned char *nb = blk + blk_stride;
             gC_nx = *reinterpret_cast<const float *>(nb + TcBlock::kMisc);
-            prefetch_l2(nb + TcBlock::kUt + (size_t)i * C * 4 + half * 128);
         }
         if (!tc::mbar_wait(&bar_u, c & 1, kWaitLimit)) fail = 1;
         tc::fence_after_sync();
