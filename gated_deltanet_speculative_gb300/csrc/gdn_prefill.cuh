@@ -70,20 +70,21 @@ struct ChunkBlock {
 
 // The same block as laid out for the tensor-core scan (d = 128, C = 64), in
 // bytes.  bf16 operands are pre-split (x = hi + lo, both bf16) and stored in
-// the K-major no-swizzle layout of gdn_tc.cuh, hi block then lo block:
-//   W    rows t (64), K = j (128)     B operand of U^T = S0 W^T
-//   Q~   rows t (64), K = j (128)     B operand of O^T = S0 Q~^T
-//   P    rows t (64), K = s (64)      B operand of O^T += U^T P^T
-//   K~^T rows j (128), K = t (64)     B operand of S = gamma_C S0 + U^T K~
+// the K-major no-swizzle layout of gdn_tc.cuh, hi block then lo block.  Two
+// stacked operands, so that each group of the scan is one wide product:
+//   [W; Q~]     rows 0..63 W (rows t), 64..127 Q~ (rows t), K = j (128):
+//               B operand of [U^T | O^T] = S0 [W; Q~]^T         (N = 128)
+//   [P; K~^T]   rows 0..63 P (rows t, K = s), 64..191 K~^T (rows j, K = t),
+//               K = 64:  B operand of [O^T | S] += U^T [P; K~^T]^T  (N = 192)
 //   U~^T fp32 [128 i][64 t]           added to -S0 W^T in fp32
 //   gamma_C
 struct TcBlock {
-    static constexpr int kW = 0;
-    static constexpr int kQ = 32768;
-    static constexpr int kP = 65536;
-    static constexpr int kK = 81920;
-    static constexpr int kGroup1 = 65536;      // bytes of W | Q~
-    static constexpr int kGroup2 = 49152;      // bytes of P | K~^T
+    static constexpr int kWQ = 0;           // [W; Q~] hi; lo at + kWQLo
+    static constexpr int kWQLo = 32768;
+    static constexpr int kPK = 65536;       // [P; K~^T] hi; lo at + kPKLo
+    static constexpr int kPKLo = 24576;
+    static constexpr int kGroup1 = 65536;   // bytes of [W; Q~]
+    static constexpr int kGroup2 = 49152;   // bytes of [P; K~^T]
     static constexpr int kOpBytes = 114688;
     static constexpr int kUt = 114688;
     static constexpr int kMisc = 147456;
@@ -810,7 +811,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
             float xq[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) xq[e] = __fmul_rn(a, x[e]);
-            store_split8(blk + TcBlock::kQ, blk + TcBlock::kQ + 16384, t, j0, D, xq);
+            store_split8(blk + TcBlock::kWQ, blk + TcBlock::kWQ + TcBlock::kWQLo, C + t, j0, D, xq);
         }
     }
     tc::fence_async_smem();
@@ -838,7 +839,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
             kt[e] = (t0 + e) < n ? __fmul_rn(eGC[t0 + e], kv) : 0.0f;
         }
         store_split8(y_hi, y_lo, j, t0, C, y);
-        store_split8(blk + TcBlock::kK, blk + TcBlock::kK + 16384, j, t0, C, kt);
+        store_split8(blk + TcBlock::kPK, blk + TcBlock::kPK + TcBlock::kPKLo, C + j, t0, C, kt);
     }
     bool ok = tc::mbar_wait(&bar_mma, 0, kPrepWaitLimit);
     tc::fence_after_sync();
@@ -885,7 +886,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = QK[t * AS + s0 + e];
-            store_split8(blk + TcBlock::kP, blk + TcBlock::kP + 8192, t, s0, C, x);
+            store_split8(blk + TcBlock::kPK, blk + TcBlock::kPK + TcBlock::kPKLo, t, s0, C, x);
         }
     }
     for (int i = tid; i < C * C; i += kPrepTcThreads) {   // zero the strictly upper blocks
@@ -1010,7 +1011,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         const float4 a4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0);
         const float4 b4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0 + 4);
         const float x[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
-        store_split8(blk + TcBlock::kW, blk + TcBlock::kW + 16384, t, j0, D, x);
+        store_split8(blk + TcBlock::kWQ, blk + TcBlock::kWQ + TcBlock::kWQLo, t, j0, D, x);
     }
     {   // U~^T [128][64] fp32, row-major, coalesced 16-byte stores
         float4 *dst = reinterpret_cast<float4 *>(blk + TcBlock::kUt);
@@ -1041,12 +1042,15 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
 // chunk to chunk.  Every product is three bf16 MMAs (hi*hi + hi*lo + lo*hi)
 // accumulating in fp32.  Per chunk:
 //   S0 -> bf16 hi/lo A operand (shared memory); TMEM S <- gamma_C S0
-//   group 1: U^T = S0 W^T, O^T = S0 Q~^T                     (K = 128)
+//   group 1: [U^T | O^T] = S0 [W; Q~]^T          (N = 128, K = 128)
 //   U = U~ - U^T (fp32) -> bf16 hi/lo A operand
-//   group 2: O^T += U^T P^T, S += U^T K~                     (K = 64)
+//   group 2: [O^T | S] += U^T [P; K~^T]^T         (N = 192, K = 64)
 //   O^T -> the workspace (fp32) for the norm pass
-// The chunk's operands arrive by 1-D bulk copies in two halves, each issued
-// as soon as the previous chunk's MMAs are done with that half.
+// One wide product per group reads its A operand once per K step; a
+// 128 x 64 x 16 step is bound by shared-memory operand reads, a 128 x 128
+// one runs at the tensor rate.  The chunk's operands arrive by 1-D bulk
+// copies in two halves, each issued as soon as the group that reads it is
+// done, with the whole block pulled into L2 two chunks ahead.
 // ---------------------------------------------------------------------------
 constexpr int kScanTcThreads = 256;   // two threads per TMEM lane, splitting the columns
 constexpr int kScanPrefetchAhead = 2;   // chunk blocks pulled into L2 this many chunks early
@@ -1108,7 +1112,7 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
     unsigned char *S_lo = S_hi + 32768;
     unsigned char *U_hi = S_lo + 32768;                  // A operand U^T [128 x 64]
     unsigned char *U_lo = U_hi + 16384;
-    __shared__ __align__(8) uint64_t bar_g1, bar_g2, bar_u, bar_s, bar_o, bar_end;
+    __shared__ __align__(8) uint64_t bar_g1, bar_g2, bar_u, bar_s, bar_end;
     __shared__ uint32_t tmem_base;
     __shared__ int fail;
 
@@ -1136,7 +1140,6 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
         tc::mbar_init(&bar_g2, 1);
         tc::mbar_init(&bar_u, 1);
         tc::mbar_init(&bar_s, 1);
-        tc::mbar_init(&bar_o, 1);
         tc::mbar_init(&bar_end, 1);
         fail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1150,7 +1153,7 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
     const uint32_t lane = (uint32_t)(quarter * 32) << 16;
     const uint32_t tU = tmem_base + lane, tO = tmem_base + 64 + lane, tS = tmem_base + 128 + lane;
     const int i = quarter * 32 + (tid & 31);   // state row (value channel); columns split by `half`
-    constexpr uint32_t idN64 = tc::idesc_bf16(128, 64), idN128 = tc::idesc_bf16(128, 128);
+    constexpr uint32_t idN128 = tc::idesc_bf16(128, 128), idN192 = tc::idesc_bf16(128, 192);
 
     if (tid == 0) {
         issue_group1(ops, blk0, &bar_g1);
@@ -1192,22 +1195,18 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
         }
         if (tid == 0 && c + kScanPrefetchAhead < n_chunks) prefetch_block_l2(blk + kScanPrefetchAhead * blk_stride);
 
-        // group 1: U^T = S0 W^T (committed on its own), then O^T = S0 Q~^T
+        // group 1: [U^T | O^T] = S0 [W; Q~]^T, one N = 128 product into TMEM columns 0..127
         if (tid == 0) {
             if (!tc::mbar_wait(&bar_g1, c & 1, kWaitLimit)) {
                 fail = 1;
                 tc::mma_commit(&bar_u);
             } else {
                 const uint32_t a_hi = tc::smem_u32(S_hi), a_lo = tc::smem_u32(S_lo);
-                const uint32_t w_hi = tc::smem_u32(ops + TcBlock::kW), w_lo = w_hi + 16384;
-                const uint32_t q_hi = tc::smem_u32(ops + TcBlock::kQ), q_lo = q_hi + 16384;
-                tc::mma_bf16<D>(tmem_base, a_hi, w_hi, idN64, false);
-                tc::mma_bf16<D>(tmem_base, a_hi, w_lo, idN64, true);
-                tc::mma_bf16<D>(tmem_base, a_lo, w_hi, idN64, true);
+                const uint32_t b_hi = tc::smem_u32(ops + TcBlock::kWQ), b_lo = b_hi + TcBlock::kWQLo;
+                tc::mma_bf16<D>(tmem_base, a_hi, b_hi, idN128, false);
+                tc::mma_bf16<D>(tmem_base, a_hi, b_lo, idN128, true);
+                tc::mma_bf16<D>(tmem_base, a_lo, b_hi, idN128, true);
                 tc::mma_commit(&bar_u);
-                tc::mma_bf16<D>(tmem_base + 64, a_hi, q_hi, idN64, false);
-                tc::mma_bf16<D>(tmem_base + 64, a_hi, q_lo, idN64, true);
-                tc::mma_bf16<D>(tmem_base + 64, a_lo, q_hi, idN64, true);
             }
         }
         // while the MMAs run: this chunk's U~^T row and the next chunk's
@@ -1225,6 +1224,8 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
         }
         if (!tc::mbar_wait(&bar_u, c & 1, kWaitLimit)) fail = 1;
         tc::fence_after_sync();
+        // [W; Q~] is read by no MMA any more: the next chunk's copy starts now
+        if (tid == 0 && more && !fail) issue_group1(ops, blk + blk_stride, &bar_g1);
 
         // U = U~ - S0 W^T (fp32), then its bf16 hi/lo operand (row i, K = t)
         {
@@ -1260,37 +1261,28 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
             break;
         }
 
-        // group 2: S += U^T K~ (committed on its own), then O^T += U^T P^T
+        // group 2: [O^T | S] += U^T [P; K~^T]^T, one N = 192 product into TMEM columns 64..255
         if (tid == 0) {
             if (!tc::mbar_wait(&bar_g2, c & 1, kWaitLimit)) {
                 fail = 1;
                 tc::mma_commit(&bar_s);
-                tc::mma_commit(&bar_o);
             } else {
                 const uint32_t a_hi = tc::smem_u32(U_hi), a_lo = tc::smem_u32(U_lo);
-                const uint32_t p_hi = tc::smem_u32(ops + TcBlock::kP), p_lo = p_hi + 8192;
-                const uint32_t k_hi = tc::smem_u32(ops + TcBlock::kK), k_lo = k_hi + 16384;
-                tc::mma_bf16<C>(tmem_base + 128, a_hi, k_hi, idN128, true);
-                tc::mma_bf16<C>(tmem_base + 128, a_hi, k_lo, idN128, true);
-                tc::mma_bf16<C>(tmem_base + 128, a_lo, k_hi, idN128, true);
+                const uint32_t b_hi = tc::smem_u32(ops + TcBlock::kPK), b_lo = b_hi + TcBlock::kPKLo;
+                tc::mma_bf16<C>(tmem_base + 64, a_hi, b_hi, idN192, true);
+                tc::mma_bf16<C>(tmem_base + 64, a_hi, b_lo, idN192, true);
+                tc::mma_bf16<C>(tmem_base + 64, a_lo, b_hi, idN192, true);
                 tc::mma_commit(&bar_s);
-                tc::mma_bf16<C>(tmem_base + 64, a_hi, p_hi, idN64, true);
-                tc::mma_bf16<C>(tmem_base + 64, a_hi, p_lo, idN64, true);
-                tc::mma_bf16<C>(tmem_base + 64, a_lo, p_hi, idN64, true);
-                tc::mma_commit(&bar_o);
             }
         }
         if (!tc::mbar_wait(&bar_s, c & 1, kWaitLimit)) fail = 1;
         tc::fence_after_sync();
-        // every group-1 MMA is done too: W | Q~ may be refilled
-        if (tid == 0 && more && !fail) issue_group1(ops, blk + blk_stride, &bar_g1);
+        // every MMA of the chunk is done: [P; K~^T] may be refilled
+        if (tid == 0 && more && !fail) issue_group2(ops, blk + blk_stride, &bar_g2);
         if (more && !fail) {
             gC = gC_nx;
             split_and_scale_state(tS, S_hi, S_lo, i, half, gC);   // the next chunk's S operand
         }
-        if (!tc::mbar_wait(&bar_o, c & 1, kWaitLimit)) fail = 1;
-        tc::fence_after_sync();
-        if (tid == 0 && more && !fail) issue_group2(ops, blk + blk_stride, &bar_g2);
 
         // O^T row i -> O[t][i] for the chunk's live rows
         {
