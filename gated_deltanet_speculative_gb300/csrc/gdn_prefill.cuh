@@ -1036,69 +1036,60 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
 // ---------------------------------------------------------------------------
 // scan on the tensor cores (d = 128): one CTA of 256 threads per (value
 // head, sequence).  Threads i and i + 128 (warps w and w + 4) share TMEM lane
-// i, i.e. state row i, and split its columns.  TMEM holds
-// three fp32 accumulators: U^T [128 x 64] (columns 0..63), O^T [128 x 64]
-// (64..127) and the state S [128 x 128] (128..255), which stays in TMEM from
-// chunk to chunk.  Every product is three bf16 MMAs (hi*hi + hi*lo + lo*hi)
-// accumulating in fp32.  Per chunk:
-//   S0 -> bf16 hi/lo A operand (shared memory); TMEM S <- gamma_C S0
+// i, i.e. state row i, and split its columns.  TMEM (512 columns) holds
+//   0..127    [U^T | O^T] fp32 [128 x 64] each
+//   128..255  the state S fp32 [128 x 128], kept from chunk to chunk
+//   256..319  S0 hi, 320..383 S0 lo   (bf16 pairs: A operand of group 1)
+//   384..415  U^T hi, 416..447 U^T lo (bf16 pairs: A operand of group 2)
+// A operands in TMEM put row m in lane m and elements (m, 2c), (m, 2c + 1)
+// in the low and high half of column c.  Every product is three bf16 MMAs
+// (hi*hi + hi*lo + lo*hi) accumulating in fp32.  Per chunk:
 //   group 1: [U^T | O^T] = S0 [W; Q~]^T          (N = 128, K = 128)
 //   U = U~ - U^T (fp32) -> bf16 hi/lo A operand
 //   group 2: [O^T | S] += U^T [P; K~^T]^T         (N = 192, K = 64)
+//   S -> bf16 hi/lo A operand of the next chunk; S <- gamma_C' S
 //   O^T -> the workspace (fp32) for the norm pass
-// One wide product per group reads its A operand once per K step; a
-// 128 x 64 x 16 step is bound by shared-memory operand reads, a 128 x 128
-// one runs at the tensor rate.  The chunk's operands arrive by 1-D bulk
-// copies in two halves, each issued as soon as the group that reads it is
-// done, with the whole block pulled into L2 two chunks ahead.
+// With both A operands in TMEM a 128 x 128 x 16 step reads only its B tile
+// from shared memory.  The chunk operands are double-buffered in shared
+// memory: chunk c+1's two bulk copies (one per group; a bulk-copy issue costs
+// tens of cycles whatever its size) are issued by a thread of warp 1 when
+// chunk c starts, so the MMA-issuing thread never waits on them.
 // ---------------------------------------------------------------------------
 constexpr int kScanTcThreads = 256;   // two threads per TMEM lane, splitting the columns
-constexpr int kScanPrefetchAhead = 2;   // chunk blocks pulled into L2 this many chunks early
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr size_t kScanTcSmem = TcBlock::kOpBytes + 65536 + 32768;
+constexpr size_t kScanTcSmem = 2 * (size_t)TcBlock::kOpBytes;
+constexpr uint32_t kTmemS = 128, kTmemShi = 256, kTmemSlo = 320, kTmemUhi = 384, kTmemUlo = 416;
 
-// One chunk block (TcBlock::kBytes) toward L2, in 16 KB pieces.
-__device__ __forceinline__ void prefetch_block_l2(const unsigned char *blk) {
-    for (int off = 0; off < TcBlock::kBytes; off += 16384)
-        tc::bulk_prefetch_l2(blk + off, (uint32_t)min(16384, TcBlock::kBytes - off));
+// The chunk's [W; Q~] and [P; K~^T] operands into one buffer, each group
+// completing on its own barrier.
+__device__ __forceinline__ void issue_chunk_copies(unsigned char *ops, const unsigned char *blk, uint64_t *bar1,
+                                                   uint64_t *bar2) {
+    tc::mbar_expect_tx(bar1, TcBlock::kGroup1);
+    tc::bulk_g2s(ops, blk, TcBlock::kGroup1, bar1);
+    tc::mbar_expect_tx(bar2, TcBlock::kGroup2);
+    tc::bulk_g2s(ops + TcBlock::kGroup1, blk + TcBlock::kGroup1, TcBlock::kGroup2, bar2);
 }
 
-__device__ __forceinline__ void issue_group1(unsigned char *ops, const unsigned char *blk, uint64_t *bar) {
-    tc::mbar_expect_tx(bar, TcBlock::kGroup1);
-    for (int off = 0; off < TcBlock::kGroup1; off += 16384) tc::bulk_g2s(ops + off, blk + off, 16384, bar);
-}
-
-__device__ __forceinline__ void issue_group2(unsigned char *ops, const unsigned char *blk, uint64_t *bar) {
-    tc::mbar_expect_tx(bar, TcBlock::kGroup2);
-    for (int off = 0; off < TcBlock::kGroup2; off += 16384)
-        tc::bulk_g2s(ops + TcBlock::kGroup1 + off, blk + TcBlock::kGroup1 + off, 16384, bar);
-}
-
-// S0 (TMEM) -> bf16 hi/lo A operand in shared memory, and TMEM S <- gamma_C
-// * S0 for the coming U^T K~ accumulation.  This thread handles row i,
-// columns [half * 64, half * 64 + 64).
-__device__ __forceinline__ void split_and_scale_state(uint32_t tS, unsigned char *S_hi, unsigned char *S_lo, int i,
-                                                      int half, float gC) {
+// S (TMEM fp32) -> its bf16 hi/lo pair columns (the next group-1 A operand),
+// and S <- gamma_C * S for the coming U^T K~ accumulation.  This thread
+// handles its lane's columns [half * 64, half * 64 + 64).
+__device__ __forceinline__ void split_and_scale_state(uint32_t tmem_lane, int half, float gC) {
     uint32_t r[4][16];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) tc::tmem_ld16_nowait(tS + half * 64 + q * 16, r[q]);
+    for (int q = 0; q < 4; ++q) tc::tmem_ld16_nowait(tmem_lane + kTmemS + half * 64 + q * 16, r[q]);
     tc::tmem_wait_ld();
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        float a[8], b[8], v[16];
+        uint32_t hw[8], lw[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[q][e]);
+        for (int e = 0; e < 8; ++e)
+            tc::split_bf16x2(__uint_as_float(r[q][2 * e]), __uint_as_float(r[q][2 * e + 1]), hw[e], lw[e]);
+        tc::tmem_st8_nowait(tmem_lane + kTmemShi + half * 32 + q * 8, hw);
+        tc::tmem_st8_nowait(tmem_lane + kTmemSlo + half * 32 + q * 8, lw);
+        float v[16];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            a[e] = v[e];
-            b[e] = v[8 + e];
-        }
-        const int col = half * 64 + q * 16;
-        store_split8(S_hi, S_lo, i, col, 128, a);
-        store_split8(S_hi, S_lo, i, col + 8, 128, b);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(gC, v[e]);
-        tc::tmem_st16_nowait(tS + col, v);
+        for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(gC, __uint_as_float(r[q][e]));
+        tc::tmem_st16_nowait(tmem_lane + kTmemS + half * 64 + q * 16, v);
     }
     tc::tmem_wait_st();
 }
@@ -1106,13 +1097,9 @@ __device__ __forceinline__ void split_and_scale_state(uint32_t tS, unsigned char
 template <int C>
 __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(const PrefillParams p) {
     constexpr int D = 128;
-    extern __shared__ __align__(1024) unsigned char tsm[];
-    unsigned char *ops = tsm;                            // W | Q~ | P | K~^T, hi and lo each
-    unsigned char *S_hi = tsm + TcBlock::kOpBytes;       // A operand S0 [128 x 128]
-    unsigned char *S_lo = S_hi + 32768;
-    unsigned char *U_hi = S_lo + 32768;                  // A operand U^T [128 x 64]
-    unsigned char *U_lo = U_hi + 16384;
-    __shared__ __align__(8) uint64_t bar_g1, bar_g2, bar_u, bar_s, bar_end;
+    static_assert(C == 64, "the TMEM column map is for C = 64");
+    extern __shared__ __align__(1024) unsigned char tsm[];   // two operand buffers
+    __shared__ __align__(8) uint64_t bar_g1[2], bar_g2[2], bar_u, bar_s, bar_end;
     __shared__ uint32_t tmem_base;
     __shared__ int fail;
 
@@ -1136,8 +1123,10 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
         reinterpret_cast<const unsigned char *>(p.ws_chunks) + ((size_t)base * p.Hv + h) * TcBlock::kBytes;
 
     if (tid == 0) {
-        tc::mbar_init(&bar_g1, 1);
-        tc::mbar_init(&bar_g2, 1);
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&bar_g1[b], 1);
+            tc::mbar_init(&bar_g2[b], 1);
+        }
         tc::mbar_init(&bar_u, 1);
         tc::mbar_init(&bar_s, 1);
         tc::mbar_init(&bar_end, 1);
@@ -1145,21 +1134,17 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     tc::fence_async_smem();
-    if (warp == 0) tc::tmem_alloc(&tmem_base, 256);
+    if (warp == 0) tc::tmem_alloc(&tmem_base, 512);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const int quarter = warp & 3, half = warp >> 2;
-    const uint32_t lane = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tU = tmem_base + lane, tO = tmem_base + 64 + lane, tS = tmem_base + 128 + lane;
+    const uint32_t tl = tmem_base + ((uint32_t)(quarter * 32) << 16);   // this warp's lane quarter
     const int i = quarter * 32 + (tid & 31);   // state row (value channel); columns split by `half`
     constexpr uint32_t idN128 = tc::idesc_bf16(128, 128), idN192 = tc::idesc_bf16(128, 192);
 
-    if (tid == 0) {
-        issue_group1(ops, blk0, &bar_g1);
-        issue_group2(ops, blk0, &bar_g2);
-        for (int c = 1; c < kScanPrefetchAhead && c < n_chunks; ++c) prefetch_block_l2(blk0 + (size_t)c * blk_stride);
-    }
+    constexpr int kCopier = 32;   // lane 0 of warp 1 issues the bulk copies
+    if (tid == kCopier) issue_chunk_copies(tsm, blk0, &bar_g1[0], &bar_g2[0]);
     // the committed state row i into TMEM
     float *srow = p.state + ((size_t)sl * p.Hv + h) * D * D + (size_t)i * D;
 #pragma unroll 1
@@ -1170,22 +1155,24 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
             const float4 f = *reinterpret_cast<const float4 *>(srow + cb * 16 + e);
             v[e] = f.x; v[e + 1] = f.y; v[e + 2] = f.z; v[e + 3] = f.w;
         }
-        tc::tmem_st16_nowait(tS + cb * 16, v);
+        tc::tmem_st16_nowait(tl + kTmemS + cb * 16, v);
     }
     tc::tmem_wait_st();
 
     // chunk 0's gamma_C; later chunks' are read one chunk ahead
     float gC = *reinterpret_cast<const float *>(blk0 + TcBlock::kMisc);
-    split_and_scale_state(tS, S_hi, S_lo, i, half, gC);
+    split_and_scale_state(tl, half, gC);
 
     bool ok = true;
+    int issued = 1;   // chunks whose copies have been issued
 #pragma unroll 1
     for (int c = 0; c < n_chunks && ok; ++c) {
         const unsigned char *blk = blk0 + (size_t)c * blk_stride;
+        unsigned char *ops = tsm + (c & 1) * TcBlock::kOpBytes;
+        const uint32_t par = (c >> 1) & 1;   // fill count of this buffer, mod 2
         const bool more = c + 1 < n_chunks;
         const int start = lo + c * C;
         const int n = min(C, hi - start);
-        tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();   // S operand written; the previous chunk's O readout is done
         tc::fence_after_sync();
@@ -1193,24 +1180,28 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
             ok = false;
             break;
         }
-        if (tid == 0 && c + kScanPrefetchAhead < n_chunks) prefetch_block_l2(blk + kScanPrefetchAhead * blk_stride);
+        // the other buffer was last read by chunk c-1's MMAs, all complete
+        if (tid == kCopier && more)
+            issue_chunk_copies(tsm + ((c + 1) & 1) * TcBlock::kOpBytes, blk + blk_stride, &bar_g1[(c + 1) & 1],
+                               &bar_g2[(c + 1) & 1]);
+        if (more) issued = c + 2;
 
         // group 1: [U^T | O^T] = S0 [W; Q~]^T, one N = 128 product into TMEM columns 0..127
         if (tid == 0) {
-            if (!tc::mbar_wait(&bar_g1, c & 1, kWaitLimit)) {
+            if (!tc::mbar_wait(&bar_g1[c & 1], par, kWaitLimit)) {
                 fail = 1;
                 tc::mma_commit(&bar_u);
             } else {
-                const uint32_t a_hi = tc::smem_u32(S_hi), a_lo = tc::smem_u32(S_lo);
                 const uint32_t b_hi = tc::smem_u32(ops + TcBlock::kWQ), b_lo = b_hi + TcBlock::kWQLo;
-                tc::mma_bf16<D>(tmem_base, a_hi, b_hi, idN128, false);
-                tc::mma_bf16<D>(tmem_base, a_hi, b_lo, idN128, true);
-                tc::mma_bf16<D>(tmem_base, a_lo, b_hi, idN128, true);
+                tc::mma_bf16_ta<D>(tmem_base, tmem_base + kTmemShi, b_hi, idN128, false);
+                tc::mma_bf16_ta<D>(tmem_base, tmem_base + kTmemShi, b_lo, idN128, true);
+                tc::mma_bf16_ta<D>(tmem_base, tmem_base + kTmemSlo, b_hi, idN128, true);
                 tc::mma_commit(&bar_u);
             }
         }
-        // while the MMAs run: this chunk's U~^T row and the next chunk's
-        // gamma_C (both in blocks already pulled toward L2)
+        // while the MMAs run: this chunk's U~^T row (pulled toward L2 one
+        // chunk ahead), the next chunk's gamma_C and an L2 prefetch of the
+        // next chunk's U~^T row
         float4 ut[C / 8];   // this thread's half of the row
         {
             const float4 *src = reinterpret_cast<const float4 *>(blk + TcBlock::kUt) + i * (C / 4) + half * (C / 8);
@@ -1219,40 +1210,32 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
         }
         float gC_nx = 0.0f;
         if (more) {
-            const unsigned char *nb = blk + blk_stride;
-            gC_nx = *reinterpret_cast<const float *>(nb + TcBlock::kMisc);
+            gC_nx = *reinterpret_cast<const float *>(blk + blk_stride + TcBlock::kMisc);
+            prefetch_l2(blk + blk_stride + TcBlock::kUt + (size_t)i * C * 4 + half * (C * 2));
         }
         if (!tc::mbar_wait(&bar_u, c & 1, kWaitLimit)) fail = 1;
         tc::fence_after_sync();
-        // [W; Q~] is read by no MMA any more: the next chunk's copy starts now
-        if (tid == 0 && more && !fail) issue_group1(ops, blk + blk_stride, &bar_g1);
 
-        // U = U~ - S0 W^T (fp32), then its bf16 hi/lo operand (row i, K = t)
+        // U = U~ - S0 W^T (fp32), then its bf16 hi/lo pairs (row i, K = t) into TMEM
         {
             uint32_t r[C / 32][16];
 #pragma unroll
-            for (int q = 0; q < C / 32; ++q) tc::tmem_ld16_nowait(tU + half * (C / 2) + q * 16, r[q]);
+            for (int q = 0; q < C / 32; ++q) tc::tmem_ld16_nowait(tl + half * (C / 2) + q * 16, r[q]);
             tc::tmem_wait_ld();
+            uint32_t hw[C / 4], lw[C / 4];
 #pragma unroll
-            for (int q = 0; q < C / 32; ++q) {
-                float a[8], b[8];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4 u = ut[q * 4 + e];
-                    const float uu[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int f = 0; f < 4; ++f) {
-                        const float d = __fsub_rn(uu[f], __uint_as_float(r[q][4 * e + f]));
-                        if (4 * e + f < 8) a[4 * e + f] = d;
-                        else b[4 * e + f - 8] = d;
-                    }
-                }
-                const int col = half * (C / 2) + q * 16;
-                store_split8(U_hi, U_lo, i, col, C, a);
-                store_split8(U_hi, U_lo, i, col + 8, C, b);
+            for (int e = 0; e < C / 8; ++e) {   // float4 e holds t = half * C/2 + 4e .. 4e + 3
+                const float4 u = ut[e];
+                const int q = e / 4, f = (e % 4) * 4;
+                tc::split_bf16x2(__fsub_rn(u.x, __uint_as_float(r[q][f])), __fsub_rn(u.y, __uint_as_float(r[q][f + 1])),
+                                 hw[2 * e], lw[2 * e]);
+                tc::split_bf16x2(__fsub_rn(u.z, __uint_as_float(r[q][f + 2])), __fsub_rn(u.w, __uint_as_float(r[q][f + 3])),
+                                 hw[2 * e + 1], lw[2 * e + 1]);
             }
+            tc::tmem_st16_nowait(tl + kTmemUhi + half * (C / 4), hw);
+            tc::tmem_st16_nowait(tl + kTmemUlo + half * (C / 4), lw);
+            tc::tmem_wait_st();
         }
-        tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
@@ -1263,32 +1246,29 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
 
         // group 2: [O^T | S] += U^T [P; K~^T]^T, one N = 192 product into TMEM columns 64..255
         if (tid == 0) {
-            if (!tc::mbar_wait(&bar_g2, c & 1, kWaitLimit)) {
+            if (!tc::mbar_wait(&bar_g2[c & 1], par, kWaitLimit)) {
                 fail = 1;
                 tc::mma_commit(&bar_s);
             } else {
-                const uint32_t a_hi = tc::smem_u32(U_hi), a_lo = tc::smem_u32(U_lo);
                 const uint32_t b_hi = tc::smem_u32(ops + TcBlock::kPK), b_lo = b_hi + TcBlock::kPKLo;
-                tc::mma_bf16<C>(tmem_base + 64, a_hi, b_hi, idN192, true);
-                tc::mma_bf16<C>(tmem_base + 64, a_hi, b_lo, idN192, true);
-                tc::mma_bf16<C>(tmem_base + 64, a_lo, b_hi, idN192, true);
+                tc::mma_bf16_ta<C>(tmem_base + 64, tmem_base + kTmemUhi, b_hi, idN192, true);
+                tc::mma_bf16_ta<C>(tmem_base + 64, tmem_base + kTmemUhi, b_lo, idN192, true);
+                tc::mma_bf16_ta<C>(tmem_base + 64, tmem_base + kTmemUlo, b_hi, idN192, true);
                 tc::mma_commit(&bar_s);
             }
         }
         if (!tc::mbar_wait(&bar_s, c & 1, kWaitLimit)) fail = 1;
         tc::fence_after_sync();
-        // every MMA of the chunk is done: [P; K~^T] may be refilled
-        if (tid == 0 && more && !fail) issue_group2(ops, blk + blk_stride, &bar_g2);
         if (more && !fail) {
             gC = gC_nx;
-            split_and_scale_state(tS, S_hi, S_lo, i, half, gC);   // the next chunk's S operand
+            split_and_scale_state(tl, half, gC);   // the next chunk's S operand
         }
 
         // O^T row i -> O[t][i] for the chunk's live rows
         {
             uint32_t r[C / 32][16];
 #pragma unroll
-            for (int q = 0; q < C / 32; ++q) tc::tmem_ld16_nowait(tO + half * (C / 2) + q * 16, r[q]);
+            for (int q = 0; q < C / 32; ++q) tc::tmem_ld16_nowait(tl + 64 + half * (C / 2) + q * 16, r[q]);
             tc::tmem_wait_ld();
             float *ocol = p.ws_out + ((size_t)start * p.Hv + h) * D + i;
 #pragma unroll
@@ -1308,7 +1288,7 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
 #pragma unroll 1
         for (int cb = half * 4; cb < half * 4 + 4; ++cb) {
             float v[16];
-            tc::tmem_ld16(tS + cb * 16, v);
+            tc::tmem_ld16(tl + kTmemS + cb * 16, v);
 #pragma unroll
             for (int e = 0; e < 16; e += 4)
                 *reinterpret_cast<float4 *>(srow + cb * 16 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
@@ -1321,28 +1301,35 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
             const int part = cc / D;
             if (part < 2 && !lead) continue;
             const int ch = pchannel<D>(part, cc - part * D, p.Hk, kh, h);
-            uint16_t *tl = p.tail + (size_t)sl * 3 * CH + ch;
-            const uint16_t old[3] = {tl[0], tl[CH], tl[2 * CH]};
+            uint16_t *tl16 = p.tail + (size_t)sl * 3 * CH + ch;
+            const uint16_t old[3] = {tl16[0], tl16[CH], tl16[2 * CH]};
             uint16_t nw[3];
 #pragma unroll
             for (int m = 0; m < 3; ++m) {
                 const int pos = L_s - 3 + m;
                 nw[m] = pos >= 0 ? p.mixed[(size_t)(lo + pos) * CH + ch] : old[3 + pos];
             }
-            tl[0] = nw[0];
-            tl[CH] = nw[1];
-            tl[2 * CH] = nw[2];
+            tl16[0] = nw[0];
+            tl16[CH] = nw[1];
+            tl16[2 * CH] = nw[2];
         }
     } else if (tid == 0) {
         raise_error(p.err, GDN_DERR_TIMEOUT);
     }
-    if (tid == 0) {   // no MMA may still write TMEM when it is freed
+    if (tid == 0) {
+        // no bulk copy may still land in this CTA's shared memory, and no MMA
+        // may still write TMEM, when the CTA leaves (bounded waits)
+        // the last fill of each buffer (an already completed phase returns at once)
+        for (int c2 = max(0, issued - 2); c2 < issued; ++c2) {
+            tc::mbar_wait(&bar_g1[c2 & 1], (c2 >> 1) & 1, kWaitLimit);
+            tc::mbar_wait(&bar_g2[c2 & 1], (c2 >> 1) & 1, kWaitLimit);
+        }
         tc::mma_commit(&bar_end);
         tc::mbar_wait(&bar_end, 0, kWaitLimit);
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
+    if (warp == 0) tc::tmem_dealloc(tmem_base, 512);
 }
 
 // ---------------------------------------------------------------------------

@@ -61,6 +61,23 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint32_t a_saddr, uint
     }
 }
 
+// The same product with A in TMEM: row m of A in lane m, elements (m, 2c)
+// and (m, 2c + 1) in the low and high half of column c, so step kb starts 8
+// columns further in.
+template <int K>
+__device__ __forceinline__ void mma_bf16_ta(uint32_t tmem_d, uint32_t tmem_a, uint32_t b_saddr, uint32_t idesc,
+                                            bool accumulate) {
+    const uint64_t b0 = smem_desc(b_saddr, K);
+#pragma unroll
+    for (int kb = 0; kb < K / 16; ++kb) {
+        const uint32_t acc = (accumulate || kb > 0) ? 1u : 0u;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+            "r"(tmem_a + (uint32_t)(kb * 8)), "l"(b0 + (uint64_t)(kb * 16)), "r"(idesc), "r"(acc));
+    }
+}
+
 // Arrive on `mbar` once every MMA this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *mbar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(mbar))
@@ -98,12 +115,6 @@ __device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gmem_src, u
             smem_u32(smem_dst)),
         "l"(gmem_src), "r"(bytes), "r"(smem_u32(mbar))
         : "memory");
-}
-
-// Pull `bytes` (a multiple of 16) at a 16-byte aligned global address into L2;
-// nothing waits for it.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *gmem, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -156,6 +167,23 @@ __device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const float (&v
         "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
         "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
         "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
+// 8 consecutive 32-bit columns of this thread's lane, without waiting.
+__device__ __forceinline__ void tmem_st8_nowait(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+// 16 raw 32-bit columns, without waiting.
+__device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
 
