@@ -13,25 +13,53 @@ cudaError_t launch_rows_d32(int mode, const RowParams &p, int n_streams, cudaStr
 cudaError_t launch_rows_d64(int mode, const RowParams &p, int n_streams, cudaStream_t st);
 cudaError_t launch_rows_d128(int mode, const RowParams &p, int n_streams, cudaStream_t st);
 
+// Steps in clusters of the G value heads that share a key head (the in-place
+// tail shift of the shared q/k channels waits for all of them), each head's
+// state rows split over P CTAs of the cluster.
+template <int D, int P>
+cudaError_t launch_step(const RowParams &p, int n_streams, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.Hv * P, n_streams);
+    cfg.blockDim = dim3(kRowThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.G * P;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gdn_rows_kernel<D, kStep, P>, p);
+}
+
+// Row slices per step CTA: double P while the cluster stays within 8 CTAs,
+// every warp keeps at least one state row, and the grid stays within two
+// CTAs per SM.
+inline int step_slices(int D, int G, int Hv, int n_streams) {
+    static int n_sm[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (n_sm[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 1;
+        n_sm[dev] = v;
+    }
+    int P = 1;
+    while (P * 2 * G <= 8 && P * 2 <= D / 8 && (long long)Hv * n_streams * P * 2 <= 2LL * n_sm[dev]) P *= 2;
+    return P;
+}
+
 template <int D>
 cudaError_t launch_rows(int mode, const RowParams &p, int n_streams, cudaStream_t st) {
     const dim3 grid(p.Hv, n_streams), block(kRowThreads);
     if (mode == kStep) {
-        // clusters of the G value heads that share a key head: the in-place
-        // tail shift of the shared q/k channels waits for all of them
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = grid;
-        cfg.blockDim = block;
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = p.G;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, gdn_rows_kernel<D, kStep>, p);
+        const int P = step_slices(D, p.G, p.Hv, n_streams);
+        if constexpr (D >= 64)
+            if (P == 8) return launch_step<D, 8>(p, n_streams, st);
+        if (P == 4) return launch_step<D, 4>(p, n_streams, st);
+        if (P == 2) return launch_step<D, 2>(p, n_streams, st);
+        return launch_step<D, 1>(p, n_streams, st);
     }
     if (mode == kWindow) gdn_rows_kernel<D, kWindow><<<grid, block, 0, st>>>(p);
     else if (mode == kWindowLog) gdn_rows_kernel<D, kWindowLog><<<grid, block, 0, st>>>(p);

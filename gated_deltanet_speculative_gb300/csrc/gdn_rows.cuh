@@ -7,6 +7,13 @@
 //   registers for the whole window, so it crosses HBM once on the way in and
 //   once per recorded row on the way out.
 //
+// Steps may also split the tile's rows over P CTAs of a cluster (P slices of
+// D/P rows; every state row evolves from its own row, k, q and the gates
+// alone).  Each row's sums stay inside one warp with the same lane layout,
+// so a sliced step equals an unsliced one bit for bit; the RMSNorm, the only
+// step that mixes rows, gathers the whole o vector into every slice through
+// distributed shared memory and reduces it in the unsliced order.
+//
 // Per row (TensorFold #932, Qwen3.5 CUDA engine note: gated delta rule and
 // causal convolution; tree note: taps and recurrence follow each row's
 // branch):
@@ -73,6 +80,8 @@ struct __align__(16) RowSmem {
         float o[kMaxRows][D];   // written by the recurrence, after the conv
     } u;
     uint16_t z[kMaxRows][D];
+    uint16_t cw[3 * D][4];   // conv weights of this head's q | k | v channels
+    uint16_t nw[D];          // RMSNorm weight
     float decay[kMaxRows];
     float beta[kMaxRows];
     float kq[kMaxRows];
@@ -137,9 +146,18 @@ __device__ __forceinline__ int channel_of(int part, int e, int Hk, int kh, int h
     return part == 0 ? kh * D + e : (part == 1 ? (Hk + kh) * D + e : 2 * Hk * D + h * D + e);
 }
 
-template <int D, int MODE>
+// Store v at the same shared-memory variable of CTA `rank` of this cluster.
+__device__ __forceinline__ void st_cluster_f32(const float *local, uint32_t rank, float v) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
+}
+
+template <int D, int MODE, int P = 1>
 __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParams p) {
-    constexpr int RPW = D / kRowWarps;            // state rows per warp
+    static_assert(P == 1 || MODE == kStep, "only steps split the state rows");
+    constexpr int RPW = D / (kRowWarps * P);      // state rows per warp
     constexpr int CPL = D / 32;                   // state columns per lane
     constexpr int NV = 2 * RPW;                   // partial sums per lane: S k and S q
     constexpr int SHIFT = 5 - Log2<NV>::value;    // lane l holds total (l >> SHIFT)
@@ -148,7 +166,10 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
     static_assert(NV >= 2 && NV <= 32, "unsupported head width");
 
     __shared__ RowSmem<D> sm;
-    const int h = blockIdx.x, s = blockIdx.y;
+    __shared__ float o_all[P > 1 ? D : 1];        // the whole o vector, gathered from the slices
+    const int h = blockIdx.x / P, s = blockIdx.y;
+    const int sli = blockIdx.x % P;               // row slice: state rows [row0, row0 + D/P)
+    const int row0 = sli * (D / P);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kh = h / p.G;
     const size_t CH = (size_t)p.CH;
@@ -161,11 +182,20 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         r0 = __ldg(p.row_ptr + s);
         n = __ldg(p.row_ptr + s + 1) - r0;
     }
+    // While those words are in flight: the conv and norm weights (independent
+    // of every index), so that no later phase waits on a load of its own.
+    for (int i = tid; i < 3 * D / 2; i += kRowThreads) {   // two channels (16 bytes) per copy
+        const int part = i / (D / 2), e0 = (i - part * (D / 2)) * 2;
+        cp_async16(&sm.cw[part * D + e0][0], p.conv_w + (size_t)channel_of<D>(part, e0, p.Hk, kh, h) * 4);
+    }
+    if (tid < D / 8) cp_async16(&sm.nw[tid * 8], p.norm_w + tid * 8);
+    const float A_log = __ldg(p.A_log + h), dt_bias = __ldg(p.dt_bias + h);
     {
         int bad = (sl < 0 || sl >= p.n_slots) ? GDN_DERR_SLOT : 0;
         if (MODE != kStep && (r0 < 0 || n < 0 || n > kMaxRows || r0 > p.n_rows - n)) bad |= GDN_DERR_ROWS;
         if (bad || n == 0) {   // uniform over the CTA and over its cluster (same stream)
             if (bad && h == 0 && tid == 0) raise_error(p.err, bad);
+            cp_async_wait_all();   // no copy may land after the CTA has left
             return;
         }
     }
@@ -175,7 +205,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
     const size_t tile = (size_t)D * D;
     float *slot_tile = p.state + ((size_t)sl * p.Hv + h) * tile;
     float S[RPW][CPL];
-    load_tile<D, RPW, CPL>(S, slot_tile, warp, lane);
+    load_tile<D, RPW, CPL>(S, slot_tile + (size_t)row0 * D, warp, lane);
 
     // Stage the committed tail and the window's rows (this head's q | k | v
     // channels) and the z rows into shared memory, 16 bytes per copy.
@@ -192,6 +222,15 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         cp_async16(&sm.z[t][ch * 8], p.z + ((size_t)(r0 + t) * p.Hv + h) * D + ch * 8);
     }
     if (MODE == kTree && tid < n) sm.parent[tid] = __ldg(p.parent + r0 + tid);
+    // ---- a4: gates
+    if (tid < n) {
+        const size_t gi = (size_t)(r0 + tid) * p.Hv + h;
+        const float ain = bf_bits(p.a[gi]);
+        const float bin = bf_bits(p.b[gi]);
+        const float g = -__fmul_rn(expf(A_log), softplusf_rn(__fadd_rn(ain, dt_bias)));
+        sm.decay[tid] = expf(g);
+        sm.beta[tid] = sigmoidf_rn(bin);
+    }
     cp_async_wait_all();
     __syncthreads();
 
@@ -228,9 +267,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         const int t = i / (3 * D / 4);
         const int cc = (i - t * (3 * D / 4)) * 4;
         const int part = cc / D, e = cc - part * D;
-        const int c = channel_of<D>(part, e, p.Hk, kh, h);
-        const uint4 *wp = reinterpret_cast<const uint4 *>(p.conv_w + (size_t)c * 4);
-        const uint4 wa = __ldg(wp), wb = __ldg(wp + 1);
+        const uint4 *wp = reinterpret_cast<const uint4 *>(&sm.cw[cc][0]);
+        const uint4 wa = wp[0], wb = wp[1];
         const uint32_t wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
         // taps, oldest first: 3, 2 and 1 steps back along the branch, then the row
         const uint2 x0 = *reinterpret_cast<const uint2 *>(&sm.u.xin[3 + sm.anc[t][2]][cc]);
@@ -272,7 +310,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         // Every CTA of this key-head group has staged the old tail; now shift
         // it in place: the lead CTA moves the shared q/k channels, each CTA its v.
         cluster_sync_all();
-        for (int i = tid; i < 3 * per_row; i += kRowThreads) {
+        for (int i = tid; i < (sli == 0 ? 3 * per_row : 0); i += kRowThreads) {   // slice 0 of each head
             const int m = i / per_row;
             const int ch = own_lo + i - m * per_row;
             const int part = ch / SEG, off = (ch - part * SEG) * 8;
@@ -282,7 +320,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         }
     }
 
-    // ---- a3: L2 norm of q and k; a4: gates ----------------------------------
+    // ---- a3: L2 norm of q and k ------------------------------------------------
     for (int j = warp; j < 2 * n; j += kRowWarps) {
         float *x = (j & 1) ? sm.k[j >> 1] : sm.q[j >> 1];
         float xv[CPL];
@@ -296,14 +334,6 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         const float scale = (j & 1) ? 1.0f : p.q_scale;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) x[lane * CPL + c] = __fmul_rn(__fmul_rn(xv[c], inv), scale);
-    }
-    if (tid < n) {
-        const size_t gi = (size_t)(r0 + tid) * p.Hv + h;
-        const float ain = bf_bits(p.a[gi]);
-        const float bin = bf_bits(p.b[gi]);
-        const float g = -__fmul_rn(expf(p.A_log[h]), softplusf_rn(__fadd_rn(ain, p.dt_bias[h])));
-        sm.decay[tid] = expf(g);
-        sm.beta[tid] = sigmoidf_rn(bin);
     }
     __syncthreads();
 
@@ -353,10 +383,18 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         const float tot = reduce_scatter<NV>(part, lane);   // lanes < 16: S k; lanes >= 16: S q
         const float dec = sm.decay[t], bet = sm.beta[t];
         float u = 0.0f;
-        if (lane < 16) u = __fmul_rn(bet, __fsub_rn(sm.v[t][warp * RPW + vi], __fmul_rn(dec, tot)));
+        if (lane < 16) u = __fmul_rn(bet, __fsub_rn(sm.v[t][row0 + warp * RPW + vi], __fmul_rn(dec, tot)));
         const float u_pair = __shfl_xor_sync(kFull, u, 16);
-        if (lane >= 16 && (lane & ((1 << SHIFT) - 1)) == 0)
-            sm.u.o[t][warp * RPW + vi - RPW] = __fmaf_rn(u_pair, sm.kq[t], __fmul_rn(dec, tot));
+        if (lane >= 16 && (lane & ((1 << SHIFT) - 1)) == 0) {
+            const int row = row0 + warp * RPW + vi - RPW;
+            const float ov = __fmaf_rn(u_pair, sm.kq[t], __fmul_rn(dec, tot));
+            if constexpr (P > 1) {   // into every slice of this head (cluster ranks (h % G) * P + j)
+#pragma unroll
+                for (int j = 0; j < P; ++j) st_cluster_f32(&o_all[row], (uint32_t)((h % p.G) * P + j), ov);
+            } else {
+                sm.u.o[t][row] = ov;
+            }
+        }
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
             const float ur = __shfl_sync(kFull, u, r << SHIFT);
@@ -370,14 +408,15 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         if (MODE == kWindowLog && lane < 16 && (lane & ((1 << SHIFT) - 1)) == 0)
             p.log_u[((size_t)(r0 + t) * p.Hv + h) * D + warp * RPW + vi] = u;
     }
-    if (MODE == kStep) store_tile<D, RPW, CPL>(slot_tile, S, warp, lane, false);
-    __syncthreads();
+    if (MODE == kStep) store_tile<D, RPW, CPL>(slot_tile + (size_t)row0 * D, S, warp, lane, false);
+    if constexpr (P > 1) cluster_sync_all();   // every slice's o rows have landed in every slice
+    else __syncthreads();
 
     // ---- a7: gated RMSNorm, y in bf16 ----------------------------------------
     for (int t = warp; t < n; t += kRowWarps) {
         float ov[CPL];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) ov[c] = sm.u.o[t][lane * CPL + c];
+        for (int c = 0; c < CPL; ++c) ov[c] = P > 1 ? o_all[lane * CPL + c] : sm.u.o[t][lane * CPL + c];
         float ss = __fmul_rn(ov[0], ov[0]);
 #pragma unroll
         for (int c = 1; c < CPL; ++c) ss = __fmaf_rn(ov[c], ov[c], ss);
@@ -386,8 +425,9 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         const size_t base = ((size_t)(r0 + t) * p.Hv + h) * D + lane * CPL;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
+            if (P > 1 && (lane * CPL + c < row0 || lane * CPL + c >= row0 + D / P)) continue;   // another slice's
             const float zz = bf_bits(sm.z[t][lane * CPL + c]);
-            const float wn = bf_bits(p.norm_w[lane * CPL + c]);
+            const float wn = bf_bits(sm.nw[lane * CPL + c]);
             const float yv = __fmul_rn(__fmul_rn(__fmul_rn(ov[c], inv), wn), silu(zz));
             p.y[base + c] = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
         }

@@ -135,6 +135,26 @@ def test_window_rows_equal_one_row_steps_bitwise():
         assert np.array_equal(tl, out["rec_tail"][lo:hi])
 
 
+@pytest.mark.parametrize("g,n_streams", [(synth.LIKE_2B, 1), (synth.LIKE_2B, 4), (synth.LIKE_2B, 8),
+                                          (synth.LIKE_2B, 16), (synth.TINY, 1), (synth.TINY, 2)])
+def test_sliced_steps_equal_window_rows_bitwise(g, n_streams):
+    """Steps of few streams split each head's state rows over up to 8 CTAs of
+    a cluster (2B-like: 8, 4, 2, 1 slices at 1, 4, 8, 16 streams); a step must
+    still equal the one-row window of the same inputs bit for bit."""
+    c = Case(g, [1] * n_streams, seed=29 + n_streams, n_slots=n_streams + 2)
+    out = run_window(c)
+    d = c.dims_gpu()
+    w, cache, rows = c.dev_weights(), c.dev_cache(), c.dev_rows()
+    gdn.step(d, w, cache, dev(c.slots), rows)
+    assert gdn.get_device_error() == 0
+    y, st, tl = host_bits(rows["y"]), cache["state"].cpu().numpy(), host_bits(cache["tail"])
+    for s in range(c.S):
+        sl = int(c.slots[s])
+        assert np.array_equal(y[s], out["y"][s]), f"y stream {s}"
+        assert np.array_equal(st[sl].view(np.uint32), out["rec_state"][s].view(np.uint32)), f"state stream {s}"
+        assert np.array_equal(tl[sl], out["rec_tail"][s]), f"tail stream {s}"
+
+
 def test_step_against_oracle_many_streams():
     c = Case(synth.LIKE_2B, [1] * 8, seed=23, n_slots=11)
     d = c.dims_gpu()
