@@ -72,18 +72,18 @@ struct ChunkBlock {
 // bytes.  bf16 operands are pre-split (x = hi + lo, both bf16) and stored in
 // the K-major no-swizzle layout of gdn_tc.cuh, hi block then lo block.  Two
 // stacked operands, so that each group of the scan is one wide product:
-//   [W; Q~]     rows 0..63 W (rows t), 64..127 Q~ (rows t), K = j (128):
-//               B operand of [U^T | O^T] = S0 [W; Q~]^T         (N = 128)
+//   [-W; Q~]    rows 0..63 -W (rows t), 64..127 Q~ (rows t), K = j (128):
+//               B operand of [U^T | O^T] = [U~^T | 0] + S0 [-W; Q~]^T  (N = 128)
 //   [P; K~^T]   rows 0..63 P (rows t, K = s), 64..191 K~^T (rows j, K = t),
 //               K = 64:  B operand of [O^T | S] += U^T [P; K~^T]^T  (N = 192)
-//   U~^T fp32 [128 i][64 t]           added to -S0 W^T in fp32
+//   U~^T fp32 [128 i][64 t]           the group-1 accumulator's start
 //   gamma_C
 struct TcBlock {
-    static constexpr int kWQ = 0;           // [W; Q~] hi; lo at + kWQLo
+    static constexpr int kWQ = 0;           // [-W; Q~] hi; lo at + kWQLo
     static constexpr int kWQLo = 32768;
     static constexpr int kPK = 65536;       // [P; K~^T] hi; lo at + kPKLo
     static constexpr int kPKLo = 24576;
-    static constexpr int kGroup1 = 65536;   // bytes of [W; Q~]
+    static constexpr int kGroup1 = 65536;   // bytes of [-W; Q~]
     static constexpr int kGroup2 = 49152;   // bytes of [P; K~^T]
     static constexpr int kOpBytes = 114688;
     static constexpr int kUt = 114688;
@@ -1006,11 +1006,11 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         }
     }
     __syncthreads();
-    for (int it = tid; it < C * (D / 8); it += kPrepTcThreads) {   // W hi | lo, rows t, 8 columns j
+    for (int it = tid; it < C * (D / 8); it += kPrepTcThreads) {   // -W hi | lo, rows t, 8 columns j
         const int t = it % C, j0 = (it / C) * 8;
         const float4 a4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0);
         const float4 b4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0 + 4);
-        const float x[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
+        const float x[8] = {-a4.x, -a4.y, -a4.z, -a4.w, -b4.x, -b4.y, -b4.z, -b4.w};
         store_split8(blk + TcBlock::kWQ, blk + TcBlock::kWQ + TcBlock::kWQLo, t, j0, D, x);
     }
     {   // U~^T [128][64] fp32, row-major, coalesced 16-byte stores
@@ -1044,8 +1044,10 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
 // A operands in TMEM put row m in lane m and elements (m, 2c), (m, 2c + 1)
 // in the low and high half of column c.  Every product is three bf16 MMAs
 // (hi*hi + hi*lo + lo*hi) accumulating in fp32.  Per chunk:
-//   group 1: [U^T | O^T] = S0 [W; Q~]^T          (N = 128, K = 128)
-//   U = U~ - U^T (fp32) -> bf16 hi/lo A operand
+//   group 1: [U^T | O^T] = [U~^T | 0] + S0 [-W; Q~]^T   (N = 128, K = 128;
+//            U~^T is stored into TMEM a chunk ahead, so U = U~ - S0 W^T
+//            leaves the tensor core finished)
+//   U -> bf16 hi/lo A operand
 //   group 2: [O^T | S] += U^T [P; K~^T]^T         (N = 192, K = 64)
 //   S -> bf16 hi/lo A operand of the next chunk; S <- gamma_C' S
 //   O^T -> the workspace (fp32) for the norm pass
@@ -1092,6 +1094,34 @@ __device__ __forceinline__ void split_and_scale_state(uint32_t tmem_lane, int ha
         tc::tmem_st16_nowait(tmem_lane + kTmemS + half * 64 + q * 16, v);
     }
     tc::tmem_wait_st();
+}
+
+// Seed the group-1 accumulator of this thread's lane: its half of the chunk's
+// U~^T row into the U columns, zeros into the O columns.
+template <int C>
+__device__ __forceinline__ void seed_group1(uint32_t tmem_lane, int half, const float4 (&ut)[C / 8]) {
+#pragma unroll
+    for (int q = 0; q < C / 32; ++q) {
+        float v[16], z[16];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 u = ut[q * 4 + e];
+            v[4 * e] = u.x; v[4 * e + 1] = u.y; v[4 * e + 2] = u.z; v[4 * e + 3] = u.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) z[e] = 0.0f;
+        tc::tmem_st16_nowait(tmem_lane + half * (C / 2) + q * 16, v);
+        tc::tmem_st16_nowait(tmem_lane + 64 + half * (C / 2) + q * 16, z);
+    }
+    tc::tmem_wait_st();
+}
+
+// This thread's half of row i of a chunk's U~^T (fp32 [128][C]).
+template <int C>
+__device__ __forceinline__ void load_ut(float4 (&ut)[C / 8], const unsigned char *blk, int i, int half) {
+    const float4 *src = reinterpret_cast<const float4 *>(blk + TcBlock::kUt) + i * (C / 4) + half * (C / 8);
+#pragma unroll
+    for (int e = 0; e < C / 8; ++e) ut[e] = src[e];
 }
 
 template <int C>
@@ -1159,9 +1189,12 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
     }
     tc::tmem_wait_st();
 
-    // chunk 0's gamma_C; later chunks' are read one chunk ahead
+    // chunk 0's gamma_C and U~^T row; later chunks' are read one chunk ahead
     float gC = *reinterpret_cast<const float *>(blk0 + TcBlock::kMisc);
+    float4 ut[C / 8];
+    load_ut<C>(ut, blk0, i, half);
     split_and_scale_state(tl, half, gC);
+    seed_group1<C>(tl, half, ut);
 
     bool ok = true;
     int issued = 1;   // chunks whose copies have been issued
@@ -1193,30 +1226,22 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
                 tc::mma_commit(&bar_u);
             } else {
                 const uint32_t b_hi = tc::smem_u32(ops + TcBlock::kWQ), b_lo = b_hi + TcBlock::kWQLo;
-                tc::mma_bf16_ta<D>(tmem_base, tmem_base + kTmemShi, b_hi, idN128, false);
+                tc::mma_bf16_ta<D>(tmem_base, tmem_base + kTmemShi, b_hi, idN128, true);
                 tc::mma_bf16_ta<D>(tmem_base, tmem_base + kTmemShi, b_lo, idN128, true);
                 tc::mma_bf16_ta<D>(tmem_base, tmem_base + kTmemSlo, b_hi, idN128, true);
                 tc::mma_commit(&bar_u);
             }
         }
-        // while the MMAs run: this chunk's U~^T row (pulled toward L2 one
-        // chunk ahead), the next chunk's gamma_C and an L2 prefetch of the
-        // next chunk's U~^T row
-        float4 ut[C / 8];   // this thread's half of the row
-        {
-            const float4 *src = reinterpret_cast<const float4 *>(blk + TcBlock::kUt) + i * (C / 4) + half * (C / 8);
-#pragma unroll
-            for (int e = 0; e < C / 8; ++e) ut[e] = src[e];
-        }
+        // while the MMAs run: the next chunk's gamma_C and U~^T row
         float gC_nx = 0.0f;
         if (more) {
             gC_nx = *reinterpret_cast<const float *>(blk + blk_stride + TcBlock::kMisc);
-            prefetch_l2(blk + blk_stride + TcBlock::kUt + (size_t)i * C * 4 + half * (C * 2));
+            load_ut<C>(ut, blk + blk_stride, i, half);
         }
         if (!tc::mbar_wait(&bar_u, c & 1, kWaitLimit)) fail = 1;
         tc::fence_after_sync();
 
-        // U = U~ - S0 W^T (fp32), then its bf16 hi/lo pairs (row i, K = t) into TMEM
+        // U (finished by the tensor core) -> its bf16 hi/lo pairs (row i, K = t) in TMEM
         {
             uint32_t r[C / 32][16];
 #pragma unroll
@@ -1224,14 +1249,9 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
             tc::tmem_wait_ld();
             uint32_t hw[C / 4], lw[C / 4];
 #pragma unroll
-            for (int e = 0; e < C / 8; ++e) {   // float4 e holds t = half * C/2 + 4e .. 4e + 3
-                const float4 u = ut[e];
-                const int q = e / 4, f = (e % 4) * 4;
-                tc::split_bf16x2(__fsub_rn(u.x, __uint_as_float(r[q][f])), __fsub_rn(u.y, __uint_as_float(r[q][f + 1])),
-                                 hw[2 * e], lw[2 * e]);
-                tc::split_bf16x2(__fsub_rn(u.z, __uint_as_float(r[q][f + 2])), __fsub_rn(u.w, __uint_as_float(r[q][f + 3])),
-                                 hw[2 * e + 1], lw[2 * e + 1]);
-            }
+            for (int e = 0; e < C / 4; ++e)
+                tc::split_bf16x2(__uint_as_float(r[e / 8][(e % 8) * 2]), __uint_as_float(r[e / 8][(e % 8) * 2 + 1]),
+                                 hw[e], lw[e]);
             tc::tmem_st16_nowait(tl + kTmemUhi + half * (C / 4), hw);
             tc::tmem_st16_nowait(tl + kTmemUlo + half * (C / 4), lw);
             tc::tmem_wait_st();
@@ -1279,6 +1299,7 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
                     if (t < n) ocol[(size_t)t * p.Hv * D] = __uint_as_float(r[q][e]);
                 }
         }
+        if (more && !fail) seed_group1<C>(tl, half, ut);   // after this lane's U and O columns are read
     }
     __syncthreads();
     ok = fail == 0;
