@@ -1,6 +1,7 @@
 // gdn_api.cu -- the C ABI (include/gdn.h): host-side validation, launch
 // configuration and status codes.  Nothing here allocates device memory;
-// every buffer and stream belongs to the caller.
+// every buffer belongs to the caller (the d = 128 prefill also uses one side
+// stream and three events of its own per device, made on first use).
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -153,6 +154,60 @@ int rows_entry(int mode, const gdn_dims *dims, const gdn_weights *w, const gdn_c
 
 }  // namespace
 
+namespace gdn {
+// gdn_prefill with a choice of launch plan (see launch_prefill).
+int prefill_entry(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
+                  const int32_t *cu_seqlens, int32_t n_seqs, int32_t n_tokens, const gdn_rows *rows, int32_t chunk,
+                  void *workspace, size_t workspace_bytes, void *stream, bool pipelined) {
+    GDN_TRY(check_dims(dims));
+    GDN_TRY(check_weights(w));
+    GDN_TRY(check_cache(cache));
+    GDN_TRY(check_rows(rows));
+    if (!slot || !cu_seqlens) return GDN_ENULL;
+    if (n_seqs <= 0 || n_seqs > 65535 || n_tokens <= 0 || n_tokens > (1 << 22) || chunk != gdn::kPrefillChunk)
+        return GDN_EINVAL;
+    if (!aligned(slot, 4) || !aligned(cu_seqlens, 4)) return GDN_EALIGN;
+    const size_t need = gdn_prefill_workspace_size(dims, n_seqs, n_tokens, chunk);
+    if (!workspace || workspace_bytes < need) return GDN_EWORKSPACE;
+    if (!aligned(workspace, 16)) return GDN_EALIGN;
+    const size_t max_chunks = (size_t)n_tokens / chunk + (size_t)n_seqs;
+    if (max_chunks > 65535) return GDN_EINVAL;
+    int *err = error_word();
+    if (!err) return GDN_ECUDA;
+    gdn::PrefillParams p = {};
+    p.Hk = dims->n_k_heads;
+    p.Hv = dims->n_v_heads;
+    p.G = dims->n_v_heads / dims->n_k_heads;
+    p.CH = 2 * dims->n_k_heads * dims->d_k + dims->n_v_heads * dims->d_v;
+    p.q_scale = dims->q_scale;
+    p.eps_l2 = dims->eps_l2;
+    p.eps_rms = dims->eps_rms;
+    p.conv_w = static_cast<const uint16_t *>(w->conv_w);
+    p.A_log = w->A_log;
+    p.dt_bias = w->dt_bias;
+    p.norm_w = static_cast<const uint16_t *>(w->norm_w);
+    p.state = cache->state;
+    p.tail = static_cast<uint16_t *>(cache->tail);
+    p.n_slots = cache->n_slots;
+    p.mixed = static_cast<const uint16_t *>(rows->mixed);
+    p.z = static_cast<const uint16_t *>(rows->z);
+    p.a = static_cast<const uint16_t *>(rows->a);
+    p.b = static_cast<const uint16_t *>(rows->b);
+    p.y = static_cast<uint16_t *>(rows->y);
+    p.slot = slot;
+    p.cu_seqlens = cu_seqlens;
+    p.n_seqs = n_seqs;
+    p.n_tokens = n_tokens;
+    p.max_chunks = (int)max_chunks;
+    p.ws_chunks = static_cast<float *>(workspace);
+    p.ws_out = p.ws_chunks + max_chunks * dims->n_v_heads * gdn::prefill_chunk_floats(dims->d_k);
+    p.err = err;
+    return gdn::launch_prefill(dims->d_k, p, static_cast<cudaStream_t>(stream), pipelined) == cudaSuccess
+               ? GDN_OK
+               : GDN_ECUDA;
+}
+}  // namespace gdn
+
 extern "C" {
 
 int gdn_step(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
@@ -216,52 +271,10 @@ size_t gdn_prefill_workspace_size(const gdn_dims *dims, int32_t n_seqs, int32_t 
 int gdn_prefill(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
                 const int32_t *cu_seqlens, int32_t n_seqs, int32_t n_tokens, const gdn_rows *rows, int32_t chunk,
                 void *workspace, size_t workspace_bytes, void *stream) {
-    GDN_TRY(check_dims(dims));
-    GDN_TRY(check_weights(w));
-    GDN_TRY(check_cache(cache));
-    GDN_TRY(check_rows(rows));
-    if (!slot || !cu_seqlens) return GDN_ENULL;
-    if (n_seqs <= 0 || n_seqs > 65535 || n_tokens <= 0 || n_tokens > (1 << 22) || chunk != gdn::kPrefillChunk)
-        return GDN_EINVAL;
-    if (!aligned(slot, 4) || !aligned(cu_seqlens, 4)) return GDN_EALIGN;
-    const size_t need = gdn_prefill_workspace_size(dims, n_seqs, n_tokens, chunk);
-    if (!workspace || workspace_bytes < need) return GDN_EWORKSPACE;
-    if (!aligned(workspace, 16)) return GDN_EALIGN;
-    const size_t max_chunks = (size_t)n_tokens / chunk + (size_t)n_seqs;
-    if (max_chunks > 65535) return GDN_EINVAL;
-    int *err = error_word();
-    if (!err) return GDN_ECUDA;
-    gdn::PrefillParams p = {};
-    p.Hk = dims->n_k_heads;
-    p.Hv = dims->n_v_heads;
-    p.G = dims->n_v_heads / dims->n_k_heads;
-    p.CH = 2 * dims->n_k_heads * dims->d_k + dims->n_v_heads * dims->d_v;
-    p.q_scale = dims->q_scale;
-    p.eps_l2 = dims->eps_l2;
-    p.eps_rms = dims->eps_rms;
-    p.conv_w = static_cast<const uint16_t *>(w->conv_w);
-    p.A_log = w->A_log;
-    p.dt_bias = w->dt_bias;
-    p.norm_w = static_cast<const uint16_t *>(w->norm_w);
-    p.state = cache->state;
-    p.tail = static_cast<uint16_t *>(cache->tail);
-    p.n_slots = cache->n_slots;
-    p.mixed = static_cast<const uint16_t *>(rows->mixed);
-    p.z = static_cast<const uint16_t *>(rows->z);
-    p.a = static_cast<const uint16_t *>(rows->a);
-    p.b = static_cast<const uint16_t *>(rows->b);
-    p.y = static_cast<uint16_t *>(rows->y);
-    p.slot = slot;
-    p.cu_seqlens = cu_seqlens;
-    p.n_seqs = n_seqs;
-    p.n_tokens = n_tokens;
-    p.max_chunks = (int)max_chunks;
-    p.ws_chunks = static_cast<float *>(workspace);
-    p.ws_out = p.ws_chunks + max_chunks * dims->n_v_heads * gdn::prefill_chunk_floats(dims->d_k);
-    p.err = err;
-    return gdn::launch_prefill(dims->d_k, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK
-                                                                                               : GDN_ECUDA;
+    return gdn::prefill_entry(dims, w, cache, slot, cu_seqlens, n_seqs, n_tokens, rows, chunk, workspace,
+                              workspace_bytes, stream, true);
 }
+
 
 int gdn_window_log(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
                    const int32_t *row_ptr, int32_t n_streams, int32_t n_rows, const gdn_rows *rows, float *log_a,

@@ -46,6 +46,7 @@ struct PrefillParams {
     const int *slot;         // [S]
     const int *cu_seqlens;   // [S + 1]
     int n_seqs, n_tokens, max_chunks;
+    int c_lo, c_hi;          // global chunks [c_lo, c_hi) of this launch (tensor-core prep and scan)
     float *ws_chunks;        // [max_chunks, Hv, chunk block]
     float *ws_out;           // [T, Hv, D] fp32 O
     int *err;
@@ -656,7 +657,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     __shared__ __align__(8) uint64_t bar_mma;
     __shared__ uint32_t tmem_base;
 
-    const int h = blockIdx.x, gc = blockIdx.y, tid = threadIdx.x;
+    const int h = blockIdx.x, gc = p.c_lo + blockIdx.y, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int kh = h / p.G;
     const size_t CH = (size_t)p.CH;
@@ -1148,9 +1149,14 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
         return;
     }
     const int n_chunks = (L_s + C - 1) / C;
+    // this launch's chunks of the sequence: [c_first, c_end); the state comes
+    // from the slot and goes back to it, so launches over consecutive ranges
+    // continue one another
+    const int c_first = max(0, p.c_lo - base), c_end = min(n_chunks, p.c_hi - base);
+    if (c_first >= c_end) return;
     const size_t blk_stride = (size_t)p.Hv * TcBlock::kBytes;
-    const unsigned char *blk0 =
-        reinterpret_cast<const unsigned char *>(p.ws_chunks) + ((size_t)base * p.Hv + h) * TcBlock::kBytes;
+    const unsigned char *blk0 = reinterpret_cast<const unsigned char *>(p.ws_chunks) +
+                                ((size_t)(base + c_first) * p.Hv + h) * TcBlock::kBytes;
 
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
@@ -1197,14 +1203,15 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
     seed_group1<C>(tl, half, ut);
 
     bool ok = true;
-    int issued = 1;   // chunks whose copies have been issued
+    int issued = 1;   // chunks (counted from c_first) whose copies have been issued
+    const int n_run = c_end - c_first;
 #pragma unroll 1
-    for (int c = 0; c < n_chunks && ok; ++c) {
+    for (int c = 0; c < n_run && ok; ++c) {   // c counts from c_first
         const unsigned char *blk = blk0 + (size_t)c * blk_stride;
         unsigned char *ops = tsm + (c & 1) * TcBlock::kOpBytes;
         const uint32_t par = (c >> 1) & 1;   // fill count of this buffer, mod 2
-        const bool more = c + 1 < n_chunks;
-        const int start = lo + c * C;
+        const bool more = c + 1 < n_run;
+        const int start = lo + (c_first + c) * C;
         const int n = min(C, hi - start);
         tc::fence_before_sync();
         __syncthreads();   // S operand written; the previous chunk's O readout is done
@@ -1314,11 +1321,12 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
             for (int e = 0; e < 16; e += 4)
                 *reinterpret_cast<float4 *>(srow + cb * 16 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
         }
-        // the slot's new conv tail (as in the CUDA-core scan)
+        // the slot's new conv tail (as in the CUDA-core scan), by the launch
+        // that ends the sequence
         const int kh = h / p.G;
         const bool lead = (h % p.G) == 0;
         const size_t CH = (size_t)p.CH;
-        for (int cc = tid; cc < 3 * D; cc += kScanTcThreads) {
+        for (int cc = tid; cc < (c_end == n_chunks ? 3 * D : 0); cc += kScanTcThreads) {
             const int part = cc / D;
             if (part < 2 && !lead) continue;
             const int ch = pchannel<D>(part, cc - part * D, p.Hk, kh, h);

@@ -28,6 +28,7 @@
 #include <mutex>
 
 #include "../../include/gdn.h"
+#include "gdn_prefill_launch.h"
 
 namespace {
 
@@ -63,6 +64,7 @@ extern "C" int gdn_prefill_noalloc(const gdn_dims *dims, const gdn_weights *w, c
     void *scratch = nullptr;
     const int rc = scratch_address(&scratch);
     if (rc != GDN_OK) return rc;
-    return gdn_prefill(dims, w, cache, slot, cu_seqlens, n_seqs, n_tokens, rows, chunk, scratch,
-                       (size_t)GDN_PREFILL_NOALLOC_SCRATCH_BYTES, stream);
+    // everything on the caller's stream: no side stream or event is made here
+    return gdn::prefill_entry(dims, w, cache, slot, cu_seqlens, n_seqs, n_tokens, rows, chunk, scratch,
+                              (size_t)GDN_PREFILL_NOALLOC_SCRATCH_BYTES, stream, false);
 }

@@ -202,8 +202,18 @@ int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot
  *               bytes, 16-byte aligned; its contents on entry do not
  *               matter and are garbage on return; GDN_EWORKSPACE if absent
  *               or too small
- * Three launches on `stream`: prep (chunk x head), scan (sequence x head x
- * d_v slice) and norm (token x head).
+ * Launches: prep (chunk x head), scan (sequence x head; for d < 128 also
+ * x d_v slice) and norm (token x head).  They run after the work enqueued
+ * on `stream` before the call, and work enqueued on `stream` after the call
+ * runs after them, so the call behaves as if all of it were on `stream`.
+ * For d = 128 the chunks are taken in four groups: prep of a group
+ * runs on `stream` and its scan on a highest-priority side stream of the
+ * library (one per device, with three events, made by the first such call
+ * on that device), joined back to `stream` by events, so the scan overlaps
+ * the prep of later groups.  The side stream is shared: calls made from
+ * several host threads at once are serialised on it.  The fork and join
+ * are ordinary event record / wait calls, so the call can be captured in
+ * a CUDA graph.
  */
 int gdn_prefill(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
                 const int32_t *slot, const int32_t *cu_seqlens, int32_t n_seqs,
@@ -228,7 +238,8 @@ size_t gdn_prefill_workspace_size(const gdn_dims *dims, int32_t n_seqs, int32_t 
  *   The first call on a device looks up the array's device address (make it
  *   before any stream capture).  All calls share the array: calls whose work
  *   overlaps on the GPU race and must be serialised by the caller.  Nothing
- *   in the array needs to start at zero.  No cudaMalloc or cudaFree is made.
+ *   in the array needs to start at zero.  No cudaMalloc or cudaFree is made,
+ *   and no stream or event is created: every launch goes on `stream`.
  */
 #define GDN_PREFILL_NOALLOC_SCRATCH_BYTES (64u << 20)
 int gdn_prefill_noalloc(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,

@@ -126,3 +126,50 @@ def test_prefill_bad_seqlens_sets_error_and_skips():
     assert gdn.get_device_error() & 16
     with pytest.raises(gdn.GdnError):
         gdn.prefill(d, w, cache, dev(c.slots), dev(c.row_ptr), rows, ws[:100])
+
+
+def test_pipelined_prefill_equals_single_stream_bitwise():
+    """For d = 128 gdn_prefill takes the chunks in groups: the scan of a
+    group runs on a side stream while later groups' prep runs, and the state
+    passes from one scan launch to the next through the slot (fp32, exact).
+    gdn_prefill_noalloc runs the same kernels as one prep, one scan and one
+    norm on the caller's stream; the two must agree bit for bit, with
+    sequences that straddle group boundaries and a one-token sequence, and
+    the caller's stream must see the finished result."""
+    import ctypes
+    from gated_deltanet_speculative_gb300 import _binding as B
+    g = synth.Geometry(4, 12, 128, 128)
+    c = Case(g, [700, 130, 64, 1], seed=67, n_slots=6)
+    d = c.dims_gpu()
+    T = c.R
+    assert gdn.prefill_workspace_size(d, c.S, T) <= 64 << 20
+
+    side = torch.cuda.Stream()   # a caller stream other than the default one
+    w, cache, rows = c.dev_weights(), c.dev_cache(), c.dev_rows()
+    ws = torch.empty(gdn.prefill_workspace_size(d, c.S, T), dtype=torch.uint8, device="cuda")
+    slot, cu = dev(c.slots), dev(c.row_ptr)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        gdn.prefill(d, w, cache, slot, cu, rows, ws, stream=side)
+        out = {"y": rows["y"].clone(), "state": cache["state"].clone(), "tail": cache["tail"].clone()}
+    side.synchronize()
+    assert gdn.get_device_error() == 0
+
+    fn = gdn.load().gdn_prefill_noalloc
+    fn.argtypes = [ctypes.POINTER(B.c_dims), ctypes.POINTER(B.c_weights), ctypes.POINTER(B.c_cache),
+                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(B.c_rows),
+                   ctypes.c_int32, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    w2, cache2, rows2 = c.dev_weights(), c.dev_cache(), c.dev_rows()
+    cw, cc, cr = B._weights(d, w2), B._cache(d, cache2), B._rows(d, rows2, T)
+    rc = fn(ctypes.byref(d.c()), ctypes.byref(cw), ctypes.byref(cc), ctypes.c_void_p(slot.data_ptr()),
+            ctypes.c_void_p(cu.data_ptr()), c.S, T, ctypes.byref(cr), 64,
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert gdn.get_device_error() == 0
+    assert np.array_equal(host_bits(out["y"]), host_bits(rows2["y"]))
+    assert np.array_equal(out["state"].cpu().numpy().view(np.uint32), cache2["state"].cpu().numpy().view(np.uint32))
+    assert np.array_equal(host_bits(out["tail"]), host_bits(cache2["tail"]))
+    # and against the oracle
+    compare(c, {"y": host_bits(out["y"]), "state": out["state"].cpu().numpy(), "tail": host_bits(out["tail"])})
