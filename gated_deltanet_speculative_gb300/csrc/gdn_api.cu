@@ -1,7 +1,7 @@
 // gdn_api.cu -- the C ABI (include/gdn.h): host-side validation, launch
 // configuration and status codes.  Nothing here allocates device memory;
-// every buffer belongs to the caller (the d = 128 prefill also uses one side
-// stream and three events of its own per device, made on first use).
+// every buffer belongs to the caller (the d = 128 prefill also uses two side
+// streams and four events of its own per device, made on first use).
 #include <cmath>
 #include <cstdint>
 #include <mutex>

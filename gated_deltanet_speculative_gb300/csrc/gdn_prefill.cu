@@ -13,24 +13,43 @@ namespace {
 // Chunk groups of a pipelined tensor-core prefill: prep of group g runs on
 // the caller's stream, the scan of group g on a high-priority side stream as
 // soon as that prep is done, so the scan (one CTA per head and sequence, far
-// fewer than the SMs) overlaps the prep of the groups after it.  Both kernels
-// hold one CTA per SM, so a scan CTA waits for a prep CTA to retire; more
-// groups pipeline more finely but pay that wait (and a state round trip
-// through the slot) more often.  On GB300, 27B-like heads: 1 / 2 / 4 / 6 /
-// 10 / 16 groups took 0.81 / 0.72 / 0.68 / 0.72 / 0.77 / 0.72 ms for one
-// 4722-token prompt and 1.10 / 1.13 / 1.07 / 1.08 / 1.16 / 1.24 ms for
-// 512 + 1024 + 2048 + 4096 tokens.
-constexpr int kPrefillGroups = 4;
+// fewer than the SMs) overlaps the prep of the groups after it; the norm of
+// group g runs on a third stream after that scan, so it never holds up the
+// next scan.
+// Only the last group's scan and norm cannot overlap any prep, so the groups
+// shrink: each takes kGroupShare of the chunks left (at least kGroupMin).
+// The scan keeps up as long as a group's scan is no longer than the next
+// group's prep: on GB300, 27B-like heads, a chunk costs ~4.8 us of scan and
+// ~7.5 us of (shared-SM) prep, which a share of 0.35 leaves room for.
+constexpr double kGroupShare = 0.35;
+constexpr int kGroupMin = 4;
+constexpr int kMaxGroups = 32;
+
+// Group boundaries of `chunks` chunks into b[0..n]; returns n.
+int chunk_groups(int chunks, int (&b)[kMaxGroups + 1]) {
+    int n = 0, at = 0;
+    b[0] = 0;
+    while (at < chunks && n < kMaxGroups) {
+        const int left = chunks - at;
+        int take = (int)(left * kGroupShare + 0.999);
+        take = take < kGroupMin ? kGroupMin : take;
+        if (left - take < kGroupMin || n == kMaxGroups - 1) take = left;
+        at += take;
+        b[++n] = at;
+    }
+    return n;
+}
 
 struct SideStream {
-    cudaStream_t stream = nullptr;
-    cudaEvent_t start = nullptr, ready = nullptr, done = nullptr;
+    cudaStream_t stream = nullptr;   // scans, highest priority
+    cudaStream_t norm = nullptr;     // norms
+    cudaEvent_t start = nullptr, ready = nullptr, scanned = nullptr, done = nullptr;
 };
 constexpr int kMaxDevices = 64;
 SideStream g_side[kMaxDevices];
 std::mutex g_side_mu;   // one pipelined enqueue at a time (they share the side stream's events)
 
-// The side stream and events of the current device, made on first use
+// The side streams and events of the current device, made on first use
 // (call with g_side_mu held).
 cudaError_t side_stream(SideStream **out) {
     int dev = -1;
@@ -41,14 +60,17 @@ cudaError_t side_stream(SideStream **out) {
     if (!ss.stream) {
         int lo = 0, hi = 0;
         if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess) return e;
-        cudaStream_t s = nullptr;
+        cudaStream_t s = nullptr, sn = nullptr;
         if ((e = cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, hi)) != cudaSuccess) return e;
-        cudaEvent_t ev[3] = {};
+        if ((e = cudaStreamCreateWithPriority(&sn, cudaStreamNonBlocking, lo)) != cudaSuccess) return e;
+        cudaEvent_t ev[4] = {};
         for (auto &x : ev)
             if ((e = cudaEventCreateWithFlags(&x, cudaEventDisableTiming)) != cudaSuccess) return e;
         ss.start = ev[0];
         ss.ready = ev[1];
-        ss.done = ev[2];
+        ss.scanned = ev[2];
+        ss.done = ev[3];
+        ss.norm = sn;
         ss.stream = s;
     }
     *out = &ss;
@@ -73,7 +95,8 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
         e = cudaFuncSetAttribute(gdn_prefill_scan_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kScanTcSmem);
         if (e != cudaSuccess) return e;
-        const int groups = pipelined ? min(p.max_chunks, kPrefillGroups) : 1;
+        int bounds[kMaxGroups + 1];
+        const int groups = pipelined ? chunk_groups(p.max_chunks, bounds) : 1;
         if (groups <= 1) {
             gdn_prefill_prep_tc_kernel<C><<<dim3(p.Hv, p.max_chunks), kPrepTcThreads, kPrepTcSmem, st>>>(p);
             gdn_prefill_scan_tc_kernel<C><<<dim3(p.Hv, p.n_seqs), kScanTcThreads, kScanTcSmem, st>>>(p);
@@ -83,23 +106,26 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
         std::lock_guard<std::mutex> lock(g_side_mu);
         SideStream *ss = nullptr;
         if ((e = side_stream(&ss)) != cudaSuccess) return e;
-        // the side stream starts after the caller's earlier work ...
+        // the side streams start after the caller's earlier work ...
         if ((e = cudaEventRecord(ss->start, st)) != cudaSuccess) return e;
         if ((e = cudaStreamWaitEvent(ss->stream, ss->start, 0)) != cudaSuccess) return e;
-        const int per = (p.max_chunks + groups - 1) / groups;
-        for (int lo = 0; lo < p.max_chunks; lo += per) {
-            p.c_lo = lo;
-            p.c_hi = min(p.max_chunks, lo + per);
+        if ((e = cudaStreamWaitEvent(ss->norm, ss->start, 0)) != cudaSuccess) return e;
+        for (int g = 0; g < groups; ++g) {
+            p.c_lo = bounds[g];
+            p.c_hi = bounds[g + 1];
             gdn_prefill_prep_tc_kernel<C><<<dim3(p.Hv, p.c_hi - p.c_lo), kPrepTcThreads, kPrepTcSmem, st>>>(p);
             // (a recorded event may be recorded again once a wait on it is enqueued)
             if ((e = cudaEventRecord(ss->ready, st)) != cudaSuccess) return e;
             if ((e = cudaStreamWaitEvent(ss->stream, ss->ready, 0)) != cudaSuccess) return e;
             gdn_prefill_scan_tc_kernel<C><<<dim3(p.Hv, p.n_seqs), kScanTcThreads, kScanTcSmem, ss->stream>>>(p);
+            if ((e = cudaEventRecord(ss->scanned, ss->stream)) != cudaSuccess) return e;
+            if ((e = cudaStreamWaitEvent(ss->norm, ss->scanned, 0)) != cudaSuccess) return e;
+            gdn_prefill_norm_chunks_kernel<D, C><<<dim3(p.Hv, p.c_hi - p.c_lo), kNormThreads, 0, ss->norm>>>(p);
         }
-        gdn_prefill_norm_kernel<D><<<norm_blocks, kNormThreads, 0, ss->stream>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        // ... and the caller's stream continues after all of it
-        if ((e = cudaEventRecord(ss->done, ss->stream)) != cudaSuccess) return e;
+        // ... and the caller's stream continues after all of it (the last
+        // norm follows the last scan)
+        if ((e = cudaEventRecord(ss->done, ss->norm)) != cudaSuccess) return e;
         return cudaStreamWaitEvent(st, ss->done, 0);
     } else {
         e = cudaFuncSetAttribute(gdn_prefill_prep_kernel<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,

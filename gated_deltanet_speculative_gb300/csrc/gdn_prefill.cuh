@@ -1365,11 +1365,8 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
 // norm: one warp per (token, value head): y = O / sqrt(mean O^2 + eps) * w * SiLU(z)
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kNormThreads) gdn_prefill_norm_kernel(const PrefillParams p) {
+__device__ __forceinline__ void norm_item(const PrefillParams &p, size_t item, int lane) {
     constexpr int CPL = D / 32;
-    const int lane = threadIdx.x & 31;
-    const size_t item = (size_t)blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5);
-    if (item >= (size_t)p.n_tokens * p.Hv) return;
     const float *o = p.ws_out + item * D + lane * CPL;
     float ov[CPL];
 #pragma unroll
@@ -1386,6 +1383,32 @@ __global__ void __launch_bounds__(kNormThreads) gdn_prefill_norm_kernel(const Pr
         const float yv = __fmul_rn(__fmul_rn(__fmul_rn(ov[c], inv), wn), silu(zz));
         p.y[item * D + lane * CPL + c] = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
     }
+}
+
+// Every (token, head) of the pass.
+template <int D>
+__global__ void __launch_bounds__(kNormThreads) gdn_prefill_norm_kernel(const PrefillParams p) {
+    const size_t item = (size_t)blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5);
+    if (item >= (size_t)p.n_tokens * p.Hv) return;
+    norm_item<D>(p, item, threadIdx.x & 31);
+}
+
+// The tokens of global chunks [c_lo, c_hi): one CTA per (value head, chunk),
+// so a pipelined pass normalises each chunk group right after its scan.
+template <int D, int C>
+__global__ void __launch_bounds__(kNormThreads) gdn_prefill_norm_chunks_kernel(const PrefillParams p) {
+    __shared__ int info[2];
+    const int h = blockIdx.x, gc = p.c_lo + blockIdx.y;
+    if (threadIdx.x == 0) {
+        int seq = -1, start = 0, n = 0, seq_start = 0, bad = 0;
+        const bool ok = locate_chunk(p, C, gc, seq, start, n, seq_start, bad);
+        info[0] = (ok && !bad) ? n : 0;
+        info[1] = start;
+    }
+    __syncthreads();
+    const int n = info[0], start = info[1];
+    for (int t = threadIdx.x >> 5; t < n; t += kNormThreads / 32)
+        norm_item<D>(p, (size_t)(start + t) * p.Hv + h, threadIdx.x & 31);
 }
 
 }  // namespace gdn
