@@ -98,7 +98,7 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
         int bounds[kMaxGroups + 1];
         const int groups = pipelined ? chunk_groups(p.max_chunks, bounds) : 1;
         if (groups <= 1) {
-            gdn_prefill_prep_tc_kernel<C><<<dim3(p.Hv, p.max_chunks), kPrepTcThreads, kPrepTcSmem, st>>>(p);
+            gdn_prefill_prep_tc_kernel<C><<<dim3(p.Hk, p.max_chunks), kPrepTcThreads, kPrepTcSmem, st>>>(p);
             gdn_prefill_scan_tc_kernel<C><<<dim3(p.Hv, p.n_seqs), kScanTcThreads, kScanTcSmem, st>>>(p);
             gdn_prefill_norm_kernel<D><<<norm_blocks, kNormThreads, 0, st>>>(p);
             return cudaGetLastError();
@@ -113,7 +113,7 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
         for (int g = 0; g < groups; ++g) {
             p.c_lo = bounds[g];
             p.c_hi = bounds[g + 1];
-            gdn_prefill_prep_tc_kernel<C><<<dim3(p.Hv, p.c_hi - p.c_lo), kPrepTcThreads, kPrepTcSmem, st>>>(p);
+            gdn_prefill_prep_tc_kernel<C><<<dim3(p.Hk, p.c_hi - p.c_lo), kPrepTcThreads, kPrepTcSmem, st>>>(p);
             // (a recorded event may be recorded again once a wait on it is enqueued)
             if ((e = cudaEventRecord(ss->ready, st)) != cudaSuccess) return e;
             if ((e = cudaStreamWaitEvent(ss->stream, ss->ready, 0)) != cudaSuccess) return e;

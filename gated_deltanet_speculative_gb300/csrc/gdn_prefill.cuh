@@ -604,69 +604,76 @@ __global__ void __launch_bounds__(NT, 1) gdn_prefill_scan_kernel(const PrefillPa
 
 // ---------------------------------------------------------------------------
 // prep on the tensor cores (d = 128, C = 64): one CTA of 512 threads per
-// (value head, global chunk).  The chunk's WY/UT quantities in the form the
-// tensor-core scan consumes (TcBlock):
-//   gates first; conv + SiLU (16-row pieces of one channel, no per-row
-//   branches) with v written straight into the (diag(b) V)^T operand; L2
-//   norms of q and k, eight rows per warp in one reduce-scatter;
-//   MMA 1:  [K; Q] (128 x 128) * K^T        -> A = K K^T and Q K^T
-//   M = strict_lower(diag(b) Gamma o A),  P = lower(Gamma o Q K^T), both
-//   formed straight from the TMEM readout
+// (key head, global chunk), all chunks in parallel.  It writes the chunk
+// block (TcBlock) of each of the G value heads that share the key head.
+// Once per key head:
+//   conv + SiLU of the q and k channels (16-row pieces of one channel, no
+//   per-row branches); L2 norms, eight rows per warp in one reduce-scatter;
+//   MMA 1:  [K; Q] (128 x 128) * K^T -> K K^T and Q K^T, left in TMEM
+// Then for each value head h of the group (its v inputs staged while the
+// previous head is worked on):
+//   gates of h; conv + SiLU of h's v channels straight into (diag(b) V)^T;
+//   (diag(b gamma) K)^T, K~^T and Q~ = diag(gamma) Q;
+//   M = strict_lower(diag(b) Gamma o A), P = lower(Gamma o Q K^T), formed
+//   from the TMEM readout of MMA 1 with h's gates;
 //   T = (I + M)^-1 on the CUDA cores (fp32): 16 x 16 diagonal blocks by
-//   forward substitution, the rest by two levels of block doubling
+//   forward substitution, the rest by two levels of block doubling;
 //   MMA 2:  (diag(b gamma) K)^T * T^T -> W^T,   (diag(b) V)^T * T^T -> U~^T
 // Every MMA operand is split into bf16 hi + lo and multiplied three times
 // (hi hi + hi lo + lo hi), accumulating in fp32.
-//
-// Shared memory (bytes):
-//   q, k fp32 [64][132]                         0 .. 67584    (q's part holds T fp32 later)
-//   region B                                    67584 .. +131072:
-//     B + 0      staged conv inputs (51456), then the [K; Q] operand hi | lo
-//                (65536), then A / QK fp32 [64][65] x 2 (33280) and the T
-//                operand hi | lo (16384, at B + 34816); after MMA 2, W fp32
-//                [64][132] (33792) and U~^T fp32 [128][68] (34816, at B + 34816)
-//     B + 65536  (diag(b gamma) K)^T operand hi | lo (32768)
-//     B + 98304  (diag(b) V)^T operand hi | lo (32768)
-//   vectors g, beta, G, eG, eGC [64] each
 // ---------------------------------------------------------------------------
 constexpr int kPrepTcThreads = 512;
-constexpr int kPrepTcLD = 132;
-constexpr size_t kPrepTcQK = 2 * 64 * kPrepTcLD * 4;
-constexpr size_t kPrepTcSmem = kPrepTcQK + 131072 + 5 * 64 * 4;
+constexpr int kPrepTcLD = 132;                 // fp32 row of q, k and the W stage
+// Shared memory (bytes):
+constexpr int kPtQ = 0;                        // q fp32 [64][132], kept for every head
+constexpr int kPtK = 33792;                    // k fp32 [64][132], kept for every head
+constexpr int kPtR1 = 67584;                   // 65536: [K; Q] operand hi | lo; then per head
+                                               //   (diag(b) V)^T | (diag(b gamma) K)^T operands,
+                                               //   then the W fp32 stage [64][132]
+constexpr int kPtR2 = kPtR1 + 65536;           // 66304: q | k conv inputs [67][256] bf16; then per
+                                               //   head M, P, T fp32 [64][65] and the T operand
+                                               //   (at + 49920), then the U~^T fp32 stage [128][68]
+constexpr int kPtR3 = kPtR2 + 66304;           // 17152: v conv inputs [67][128] bf16 of one head
+constexpr int kPtVec = kPtR3 + 17152;          // g, beta, G, eG, eGC [64] each
+constexpr size_t kPrepTcSmem = kPtVec + 5 * 64 * 4;
 
 template <int C>
 __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(const PrefillParams p) {
     constexpr int D = 128, LD = kPrepTcLD, AS = C + 1;   // odd row stride: column walks across rows hit distinct banks
+    constexpr int AU = C + 4;                            // U~^T stage row (16-byte aligned)
     static_assert(C == 64, "the tensor-core block layout is for C = 64");
     static_assert(kPrepTcThreads / 32 * 8 == 2 * C, "the norm step gives each warp eight of the 2C rows");
+    static_assert(3 * C * AS * 4 + 16384 <= 66304 && 128 * AU * 4 <= 66304, "region 2 holds M, P, T, T op / U~^T");
     extern __shared__ __align__(1024) unsigned char psm[];
-    float *q = reinterpret_cast<float *>(psm);
-    float *k = q + C * LD;
-    unsigned char *B = psm + kPrepTcQK;
-    uint16_t *xin = reinterpret_cast<uint16_t *>(B);               // [C+3][3D]
-    unsigned char *kq_hi = B, *kq_lo = B + 32768;                 // [K; Q] operand
-    float *A = reinterpret_cast<float *>(B);                       // [C][AS] after MMA 1
-    float *QK = A + C * AS;
-    unsigned char *t_hi = B + 34816, *t_lo = t_hi + 8192;          // T operand [C][C]
-    unsigned char *y_hi = B + 65536, *y_lo = y_hi + 16384;         // (b gamma K)^T [D][C]
-    unsigned char *v_hi = B + 98304, *v_lo = v_hi + 16384;         // (b V)^T [D][C]
-    float *T = q;                                                  // [C][AS] once q is consumed
-    float *g = reinterpret_cast<float *>(B + 131072);
+    float *q = reinterpret_cast<float *>(psm + kPtQ);
+    float *k = reinterpret_cast<float *>(psm + kPtK);
+    unsigned char *R1 = psm + kPtR1, *R2 = psm + kPtR2;
+    uint16_t *xqk = reinterpret_cast<uint16_t *>(R2);           // [C+3][2D] q | k inputs
+    uint16_t *xv = reinterpret_cast<uint16_t *>(psm + kPtR3);   // [C+3][D] v inputs of the head in hand
+    unsigned char *kq_hi = R1, *kq_lo = R1 + 32768;             // [K; Q] operand
+    unsigned char *v_hi = R1, *v_lo = R1 + 16384;               // (b V)^T [D][C]
+    unsigned char *y_hi = R1 + 32768, *y_lo = y_hi + 16384;     // (b gamma K)^T [D][C]
+    float *A = reinterpret_cast<float *>(R2);                   // M [C][AS]
+    float *QK = A + C * AS;                                     // P [C][AS]
+    float *T = QK + C * AS;                                     // T [C][AS]
+    unsigned char *t_hi = R2 + 49920, *t_lo = t_hi + 8192;      // T operand [C][C]
+    float *Wf = reinterpret_cast<float *>(R1);                  // W [C][LD] after MMA 2
+    float *Uf = reinterpret_cast<float *>(R2);                  // U~^T [D][AU] after MMA 2
+    float *g = reinterpret_cast<float *>(psm + kPtVec);
     float *beta = g + C, *Gc = beta + C, *eG = Gc + C, *eGC = eG + C;
     __shared__ int info[4];
     __shared__ __align__(8) uint64_t bar_mma;
     __shared__ uint32_t tmem_base;
 
-    const int h = blockIdx.x, gc = p.c_lo + blockIdx.y, tid = threadIdx.x;
+    const int kh = blockIdx.x, gc = p.c_lo + blockIdx.y, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
-    const int kh = h / p.G;
     const size_t CH = (size_t)p.CH;
     if (tid == 0) {
         int seq = -1, start = 0, n = 0, seq_start = 0, bad = 0;
         const bool ok = locate_chunk(p, C, gc, seq, start, n, seq_start, bad);
         const int sl = ok ? __ldg(p.slot + seq) : -1;
         if (ok && (sl < 0 || sl >= p.n_slots)) bad |= 2;
-        if (bad && h == 0) raise_error(p.err, (bad & 1 ? GDN_DERR_SEQLENS : 0) | (bad & 2 ? GDN_DERR_SLOT : 0));
+        if (bad && kh == 0) raise_error(p.err, (bad & 1 ? GDN_DERR_SEQLENS : 0) | (bad & 2 ? GDN_DERR_SLOT : 0));
         info[0] = (ok && !bad) ? n : 0;
         info[1] = start;
         info[2] = seq_start;
@@ -676,29 +683,25 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     const int n = info[0], start = info[1], seq_start = info[2], sl = info[3];
     if (n == 0) return;
 
-    // gates (rows >= n: beta = 0, log decay 0)
-    if (tid < C) {
-        float gg = 0.0f, bb = 0.0f;
-        if (tid < n) {
-            const size_t gi = (size_t)(start + tid) * p.Hv + h;
-            gg = -__fmul_rn(expf(p.A_log[h]), softplusf_rn(__fadd_rn(bf_bits(p.a[gi]), p.dt_bias[h])));
-            bb = sigmoidf_rn(bf_bits(p.b[gi]));
-        }
-        g[tid] = gg;
-        beta[tid] = bb;
-    }
-    // stage the conv inputs: rows start-3 .. start+n-1 (the slot's kept tail
-    // before the sequence), this head's q | k | v channels
-    constexpr int SEG = D * 2 / 16, CHUNKS = 3 * SEG;
-    for (int i = tid; i < (n + 3) * CHUNKS; i += kPrepTcThreads) {
-        const int row = i / CHUNKS, ch = i - row * CHUNKS;
-        const int part = ch / SEG, off = (ch - part * SEG) * 8;
-        const int c = pchannel<D>(part, off, p.Hk, kh, h);
+    // conv inputs: rows start-3 .. start+n-1 (the slot's kept tail before the
+    // sequence), 16 bytes per copy
+    auto src_of = [&](int row, int c) -> const uint16_t * {
         const int tok = start - 3 + row;
-        const uint16_t *src = tok >= seq_start ? p.mixed + (size_t)tok * CH + c
-                                               : p.tail + ((size_t)sl * 3 + (3 - (seq_start - tok))) * CH + c;
-        cp_async16(xin + (size_t)row * 3 * D + part * D + off, src);
+        return tok >= seq_start ? p.mixed + (size_t)tok * CH + c
+                                : p.tail + ((size_t)sl * 3 + (3 - (seq_start - tok))) * CH + c;
+    };
+    auto stage_v = [&](int h) {   // head h's v channels into xv
+        for (int i = tid; i < (n + 3) * (D / 8); i += kPrepTcThreads) {
+            const int row = i / (D / 8), off = (i - row * (D / 8)) * 8;
+            cp_async16(xv + (size_t)row * D + off, src_of(row, pchannel<D>(2, off, p.Hk, kh, h)));
+        }
+    };
+    for (int i = tid; i < (n + 3) * (2 * D / 8); i += kPrepTcThreads) {   // the key head's q | k channels
+        const int row = i / (2 * D / 8), ch = i - row * (2 * D / 8);
+        const int part = ch / (D / 8), off = (ch - part * (D / 8)) * 8;
+        cp_async16(xqk + (size_t)row * 2 * D + part * D + off, src_of(row, pchannel<D>(part, off, p.Hk, kh, 0)));
     }
+    stage_v(kh * p.G);
     if (warp == 0) tc::tmem_alloc(&tmem_base, 256);
     if (tid == 0) {
         tc::mbar_init(&bar_mma, 1);
@@ -706,37 +709,19 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     }
     cp_async_wait_all();
     __syncthreads();
-    if (warp == 0) {   // inclusive prefix sum of the log decays, two rows per lane
-        const float a0 = g[2 * lane], a1 = g[2 * lane + 1];
-        float run = __fadd_rn(a0, a1);
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float o = __shfl_up_sync(kFull, run, off);
-            if (lane >= off) run = __fadd_rn(run, o);
-        }
-        const float excl = __shfl_up_sync(kFull, run, 1);
-        Gc[2 * lane] = __fadd_rn(lane == 0 ? 0.0f : excl, a0);
-        Gc[2 * lane + 1] = run;
-    }
 
-    // conv + SiLU: work item (16-row piece, channel), a sliding window of the
-    // four taps down the piece; q and k to fp32 rows, v straight into
-    // (diag(b) V)^T.  Rows >= n read unstaged inputs and are replaced by 0
-    // with a select, so the 16 rows carry no branches.
+    // conv + SiLU of q and k: work item (16-row piece, channel), a sliding
+    // window of the four taps down the piece.  Rows >= n read unstaged inputs
+    // and are replaced by 0 with a select, so the 16 rows carry no branches.
     constexpr int PR = 16;
-    for (int it = tid; it < (C / PR) * 3 * D; it += kPrepTcThreads) {
-        const int cc = it % (3 * D), t0 = (it / (3 * D)) * PR;   // warp-uniform part and t0
-        const int part = cc / D, e = cc - part * D;
-        const int c = pchannel<D>(part, e, p.Hk, kh, h);
+    auto conv_piece = [&](const uint16_t *x, int stride, int c, int t0, float (&act)[PR]) {
         const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + (size_t)c * 4));
         const float w0 = bf_bits(wv.x & 0xffffu), w1 = bf_bits(wv.x >> 16);
         const float w2 = bf_bits(wv.y & 0xffffu), w3 = bf_bits(wv.y >> 16);
-        const uint16_t *x = xin + (size_t)t0 * 3 * D + cc;
-        float x0 = bf_bits(x[0]), x1 = bf_bits(x[3 * D]), x2 = bf_bits(x[6 * D]);
-        float act[PR];
+        float x0 = bf_bits(x[0]), x1 = bf_bits(x[stride]), x2 = bf_bits(x[2 * stride]);
 #pragma unroll
         for (int r = 0; r < PR; ++r) {
-            const float x3 = bf_bits(x[(size_t)(r + 3) * 3 * D]);
+            const float x3 = bf_bits(x[(size_t)(r + 3) * stride]);
             float acc = __fmul_rn(w0, x0);
             acc = __fmaf_rn(w1, x1, acc);
             acc = __fmaf_rn(w2, x2, acc);
@@ -747,41 +732,33 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
             x1 = x2;
             x2 = x3;
         }
-        if (part < 2) {
-            float *dst = (part == 0 ? q : k) + e;
+    };
+    for (int it = tid; it < (C / PR) * 2 * D; it += kPrepTcThreads) {
+        const int cc = it % (2 * D), t0 = (it / (2 * D)) * PR;   // warp-uniform part and t0
+        const int part = cc / D, e = cc - part * D;
+        float act[PR];
+        conv_piece(xqk + (size_t)t0 * 2 * D + cc, 2 * D, pchannel<D>(part, e, p.Hk, kh, 0), t0, act);
+        float *dst = (part == 0 ? q : k) + e;
 #pragma unroll
-            for (int r = 0; r < PR; ++r) dst[(t0 + r) * LD] = act[r];
-        } else {
-#pragma unroll
-            for (int h8 = 0; h8 < PR; h8 += 8) {
-                float vb[8];
-#pragma unroll
-                for (int e8 = 0; e8 < 8; ++e8) vb[e8] = __fmul_rn(beta[t0 + h8 + e8], act[h8 + e8]);
-                store_split8(v_hi, v_lo, e, t0 + h8, C, vb);
-            }
-        }
+        for (int r = 0; r < PR; ++r) dst[(t0 + r) * LD] = act[r];
     }
     __syncthreads();
-    if (tid < C) {
-        eG[tid] = __expf(Gc[tid]);
-        eGC[tid] = __expf(__fsub_rn(Gc[n - 1], Gc[tid]));
-    }
     // L2 norms of q and k rows, q scaled: warp w takes rows 8w .. 8w+7 of the
     // interleaved list (q row j/2 for even j, k row j/2 for odd j); one
     // reduce-scatter leaves row 8w + (lane >> 2)'s sum of squares in lane
     // `lane`.  Rows >= n are zero and stay zero.
     {
-        float4 xv[8];
+        float4 xv4[8];
         float ss[8];
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
             const int j = warp * 8 + m;
             const float *x = (j & 1) ? k + (j >> 1) * LD : q + (j >> 1) * LD;
-            xv[m] = *reinterpret_cast<const float4 *>(x + lane * 4);
-            float a2 = __fmul_rn(xv[m].x, xv[m].x);
-            a2 = __fmaf_rn(xv[m].y, xv[m].y, a2);
-            a2 = __fmaf_rn(xv[m].z, xv[m].z, a2);
-            ss[m] = __fmaf_rn(xv[m].w, xv[m].w, a2);
+            xv4[m] = *reinterpret_cast<const float4 *>(x + lane * 4);
+            float a2 = __fmul_rn(xv4[m].x, xv4[m].x);
+            a2 = __fmaf_rn(xv4[m].y, xv4[m].y, a2);
+            a2 = __fmaf_rn(xv4[m].z, xv4[m].z, a2);
+            ss[m] = __fmaf_rn(xv4[m].w, xv4[m].w, a2);
         }
         const float tot = reduce_scatter<8>(ss, lane);
         const int jl = warp * 8 + (lane >> 2);
@@ -791,36 +768,23 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
             const int j = warp * 8 + m;
             const float sc = __shfl_sync(kFull, mine, m * 4);
             float *x = (j & 1) ? k + (j >> 1) * LD : q + (j >> 1) * LD;
-            *reinterpret_cast<float4 *>(x + lane * 4) =
-                make_float4(__fmul_rn(xv[m].x, sc), __fmul_rn(xv[m].y, sc), __fmul_rn(xv[m].z, sc), __fmul_rn(xv[m].w, sc));
+            *reinterpret_cast<float4 *>(x + lane * 4) = make_float4(__fmul_rn(xv4[m].x, sc), __fmul_rn(xv4[m].y, sc),
+                                                                    __fmul_rn(xv4[m].z, sc), __fmul_rn(xv4[m].w, sc));
         }
     }
     __syncthreads();
-
-    // operands of MMA 1 and 2, and the Q~ / K~^T outputs (rows fastest across
-    // threads: 8 threads fill one 128-byte core matrix)
-    unsigned char *blk = reinterpret_cast<unsigned char *>(p.ws_chunks) + ((size_t)gc * p.Hv + h) * TcBlock::kBytes;
-    for (int it = tid; it < 2 * C * (D / 8); it += kPrepTcThreads) {   // [K; Q] rows r, 8 columns j; Q~ rows
-        const int r = it % (2 * C), j0 = (it / (2 * C)) * 8;   // r < C is warp-uniform
+    for (int it = tid; it < 2 * C * (D / 8); it += kPrepTcThreads) {   // [K; Q] rows r, 8 columns j
+        const int r = it % (2 * C), j0 = (it / (2 * C)) * 8;
         const float *src = r < C ? k + r * LD + j0 : q + (r - C) * LD + j0;
         const float4 a4 = *reinterpret_cast<const float4 *>(src), b4 = *reinterpret_cast<const float4 *>(src + 4);
         const float x[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
         store_split8(kq_hi, kq_lo, r, j0, D, x);
-        if (r >= C) {   // Q~ = diag(gamma) Q, zero past the chunk's rows
-            const int t = r - C;
-            const float a = t < n ? eG[t] : 0.0f;
-            float xq[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) xq[e] = __fmul_rn(a, x[e]);
-            store_split8(blk + TcBlock::kWQ, blk + TcBlock::kWQ + TcBlock::kWQLo, C + t, j0, D, xq);
-        }
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-
-    // MMA 1: [A; QK] = [K; Q] K^T  (TMEM columns 0..63)
+    // MMA 1: [A; QK] = [K; Q] K^T (TMEM columns 0..63), kept for every head
     if (tid == 0) {
         constexpr uint32_t idn = tc::idesc_bf16(128, C);
         const uint32_t ah = tc::smem_u32(kq_hi), al = tc::smem_u32(kq_lo);
@@ -829,205 +793,260 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         tc::mma_bf16<D>(tmem_base, al, ah, idn, true);
         tc::mma_commit(&bar_mma);
     }
-    // while MMA 1 runs: the (b gamma K)^T operand of MMA 2 and K~^T for the scan
-    for (int it = tid; it < D * (C / 8); it += kPrepTcThreads) {   // (b gamma K)^T and K~^T: rows j, 8 t
-        const int j = it % D, t0 = (it / D) * 8;
-        float y[8], kt[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float kv = k[(t0 + e) * LD + j];
-            y[e] = __fmul_rn(__fmul_rn(beta[t0 + e], eG[t0 + e]), kv);
-            kt[e] = (t0 + e) < n ? __fmul_rn(eGC[t0 + e], kv) : 0.0f;
-        }
-        store_split8(y_hi, y_lo, j, t0, C, y);
-        store_split8(blk + TcBlock::kPK, blk + TcBlock::kPK + TcBlock::kPKLo, C + j, t0, C, kt);
-    }
     bool ok = tc::mbar_wait(&bar_mma, 0, kPrepWaitLimit);
+    uint32_t ph = 1;   // parity of the next bar_mma completion
     tc::fence_after_sync();
     const int quarter = warp & 3, part = warp >> 2;   // 16 warps: lane quarter x column part
-    {   // lane r holds row r of [A; QK]; the four warps on a lane quarter take
-        // 16 columns each and form M = strict_lower(diag(b) Gamma o A) and
-        // P = lower(Gamma o QK) in registers
-        const int r = quarter * 32 + lane;
-        uint32_t v[16];
-        tc::tmem_ld16_nowait(tmem_base + ((uint32_t)(quarter * 32) << 16) + part * 16, v);
-        tc::tmem_wait_ld();
-        __syncthreads();   // every MMA-1 read of the [K; Q] operand is long done; A / QK overwrite it
-        const bool isA = r < C;   // warp-uniform
-        const int t = isA ? r : r - C;
-        const float Gt = Gc[t], bt = isA ? beta[t] : 1.0f;
-        float *dst = (isA ? A : QK) + t * AS + part * 16;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int sc = part * 16 + e;
-            const bool keep = t < n && sc < n && (isA ? sc < t : sc <= t);
-            const float gam = __expf(__fsub_rn(Gt, Gc[sc]));
-            dst[e] = keep ? __fmul_rn(__fmul_rn(bt, gam), __uint_as_float(v[e])) : 0.0f;
+
+#pragma unroll 1
+    for (int gi = 0; gi < p.G; ++gi) {
+        const int h = kh * p.G + gi;
+        unsigned char *blk = reinterpret_cast<unsigned char *>(p.ws_chunks) + ((size_t)gc * p.Hv + h) * TcBlock::kBytes;
+        if (gi > 0) cp_async_wait_all();   // this head's v inputs
+        // gates (rows >= n: beta = 0, log decay 0)
+        if (tid < C) {
+            float gg = 0.0f, bb = 0.0f;
+            if (tid < n) {
+                const size_t gi2 = (size_t)(start + tid) * p.Hv + h;
+                gg = -__fmul_rn(expf(p.A_log[h]), softplusf_rn(__fadd_rn(bf_bits(p.a[gi2]), p.dt_bias[h])));
+                bb = sigmoidf_rn(bf_bits(p.b[gi2]));
+            }
+            g[tid] = gg;
+            beta[tid] = bb;
         }
-    }
-    __syncthreads();
-    // T = (I + M)^-1 by 16 x 16 blocks.  Threads < C invert the four diagonal
-    // blocks by forward substitution (one column each) while the others
-    // write P to the workspace.
-    if (tid < C) {
-        const int b0 = (tid / 16) * 16, c = tid % 16;
-        float x[16];
+        __syncthreads();
+        if (warp == 0) {   // inclusive prefix sum of the log decays, two rows per lane
+            const float a0 = g[2 * lane], a1 = g[2 * lane + 1];
+            float run = __fadd_rn(a0, a1);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = r == c ? 1.0f : 0.0f;
-#pragma unroll
-            for (int kk = 0; kk < r; ++kk) acc = __fmaf_rn(-A[(b0 + r) * AS + b0 + kk], x[kk], acc);
-            x[r] = r < c ? 0.0f : acc;
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_up_sync(kFull, run, off);
+                if (lane >= off) run = __fadd_rn(run, o);
+            }
+            const float excl = __shfl_up_sync(kFull, run, 1);
+            Gc[2 * lane] = __fadd_rn(lane == 0 ? 0.0f : excl, a0);
+            Gc[2 * lane + 1] = run;
         }
+        // conv + SiLU of h's v channels straight into (diag(b) V)^T
+        for (int it = tid; it < (C / PR) * D; it += kPrepTcThreads) {
+            const int e = it % D, t0 = (it / D) * PR;
+            float act[PR];
+            conv_piece(xv + (size_t)t0 * D + e, D, pchannel<D>(2, e, p.Hk, kh, h), t0, act);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) T[(b0 + r) * AS + b0 + c] = x[r];
-    } else {
-        for (int it = tid - C; it < C * (C / 8); it += kPrepTcThreads - C) {   // P: rows t, 8 columns s
+            for (int h8 = 0; h8 < PR; h8 += 8) {
+                float vb[8];
+#pragma unroll
+                for (int e8 = 0; e8 < 8; ++e8) vb[e8] = __fmul_rn(beta[t0 + h8 + e8], act[h8 + e8]);
+                store_split8(v_hi, v_lo, e, t0 + h8, C, vb);
+            }
+        }
+        __syncthreads();   // xv consumed; Gc complete
+        if (gi + 1 < p.G) stage_v(h + 1);   // in flight while this head is worked on
+        if (tid < C) {
+            eG[tid] = __expf(Gc[tid]);
+            eGC[tid] = __expf(__fsub_rn(Gc[n - 1], Gc[tid]));
+        }
+        __syncthreads();
+        // (diag(b gamma) K)^T operand, K~^T and Q~ for the scan
+        for (int it = tid; it < D * (C / 8); it += kPrepTcThreads) {   // rows j, 8 t
+            const int j = it % D, t0 = (it / D) * 8;
+            float y[8], kt[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float kv = k[(t0 + e) * LD + j];
+                y[e] = __fmul_rn(__fmul_rn(beta[t0 + e], eG[t0 + e]), kv);
+                kt[e] = (t0 + e) < n ? __fmul_rn(eGC[t0 + e], kv) : 0.0f;
+            }
+            store_split8(y_hi, y_lo, j, t0, C, y);
+            store_split8(blk + TcBlock::kPK, blk + TcBlock::kPK + TcBlock::kPKLo, C + j, t0, C, kt);
+        }
+        for (int it = tid; it < C * (D / 8); it += kPrepTcThreads) {   // Q~ = diag(gamma) Q, rows t, 8 columns j
+            const int t = it % C, j0 = (it / C) * 8;
+            const float a = t < n ? eG[t] : 0.0f;
+            const float4 a4 = *reinterpret_cast<const float4 *>(q + t * LD + j0);
+            const float4 b4 = *reinterpret_cast<const float4 *>(q + t * LD + j0 + 4);
+            const float xq[8] = {__fmul_rn(a, a4.x), __fmul_rn(a, a4.y), __fmul_rn(a, a4.z), __fmul_rn(a, a4.w),
+                                 __fmul_rn(a, b4.x), __fmul_rn(a, b4.y), __fmul_rn(a, b4.z), __fmul_rn(a, b4.w)};
+            store_split8(blk + TcBlock::kWQ, blk + TcBlock::kWQ + TcBlock::kWQLo, C + t, j0, D, xq);
+        }
+        {   // lane r holds row r of [A; QK]; the four warps on a lane quarter take
+            // 16 columns each and form M = strict_lower(diag(b) Gamma o A) and
+            // P = lower(Gamma o QK) in registers with this head's gates
+            const int r = quarter * 32 + lane;
+            uint32_t v[16];
+            tc::tmem_ld16_nowait(tmem_base + ((uint32_t)(quarter * 32) << 16) + part * 16, v);
+            tc::tmem_wait_ld();
+            const bool isA = r < C;   // warp-uniform
+            const int t = isA ? r : r - C;
+            const float Gt = Gc[t], bt = isA ? beta[t] : 1.0f;
+            float *dst = (isA ? A : QK) + t * AS + part * 16;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int sc = part * 16 + e;
+                const bool keep = t < n && sc < n && (isA ? sc < t : sc <= t);
+                const float gam = __expf(__fsub_rn(Gt, Gc[sc]));
+                dst[e] = keep ? __fmul_rn(__fmul_rn(bt, gam), __uint_as_float(v[e])) : 0.0f;
+            }
+        }
+        __syncthreads();
+        // T = (I + M)^-1 by 16 x 16 blocks.  Threads < C invert the four diagonal
+        // blocks by forward substitution (one column each) while the others
+        // write P to the workspace.
+        if (tid < C) {
+            const int b0 = (tid / 16) * 16, c = tid % 16;
+            float x[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float acc = r == c ? 1.0f : 0.0f;
+#pragma unroll
+                for (int kk = 0; kk < r; ++kk) acc = __fmaf_rn(-A[(b0 + r) * AS + b0 + kk], x[kk], acc);
+                x[r] = r < c ? 0.0f : acc;
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) T[(b0 + r) * AS + b0 + c] = x[r];
+        } else {
+            for (int it = tid - C; it < C * (C / 8); it += kPrepTcThreads - C) {   // P: rows t, 8 columns s
+                const int t = it % C, s0 = (it / C) * 8;
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = QK[t * AS + s0 + e];
+                store_split8(blk + TcBlock::kPK, blk + TcBlock::kPK + TcBlock::kPKLo, t, s0, C, x);
+            }
+        }
+        for (int i = tid; i < C * C; i += kPrepTcThreads) {   // zero the strictly upper blocks
+            const int t = i / C, s2 = i - t * C;
+            if (s2 / 16 > t / 16) T[t * AS + s2] = 0.0f;
+        }
+        __syncthreads();
+        // Off-diagonal blocks by doubling: for a block lower-triangular
+        // L = [L11 0; L21 L22], L^-1 has lower-left block -L22^-1 L21 L11^-1.
+        // Level 1 (16-blocks): T10 = -T11 (M10 T00), T32 = -T33 (M32 T22);
+        // level 2 (32-blocks): T[32:, :32] = -T[32:, 32:] (M[32:, :32] T[:32, :32]).
+        // The zero upper halves of the diagonal blocks let every sum run full length.
+        float *X = QK;   // scratch once P is out
+        {
+            const int pr = tid >> 8, rr = (tid >> 4) & 15, cc = tid & 15;
+            const int bi = 2 * pr + 1, bj = 2 * pr;
+            const float *m = A + (bi * 16 + rr) * AS + bj * 16;
+            const float *tb = T + (bj * 16) * AS + bj * 16 + cc;
+            float acc = 0.0f;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) acc = __fmaf_rn(m[kk], tb[kk * AS], acc);
+            X[(pr * 16 + rr) * AS + cc] = acc;
+            __syncthreads();
+            const float *td = T + (bi * 16 + rr) * AS + bi * 16;
+            const float *xc = X + (pr * 16) * AS + cc;
+            acc = 0.0f;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) acc = __fmaf_rn(td[kk], xc[kk * AS], acc);
+            T[(bi * 16 + rr) * AS + bj * 16 + cc] = -acc;
+        }
+        __syncthreads();
+        constexpr int H = C / 2;
+        constexpr int NU = H * H / kPrepTcThreads;
+        {   // level 2, X = M[32:, :32] T[:32, :32]: warp-uniform column c, lane row r;
+            // T[:32, :32] is lower triangular, so the sum starts at kk = c
+            // (columns c and 31 - c pair up to balance the threads)
+#pragma unroll
+            for (int u = 0; u < NU; ++u) {
+                const int c = u == 0 ? warp : H - 1 - warp, r = lane;
+                const float *m = A + (H + r) * AS;
+                float acc = 0.0f;
+                for (int kk = c; kk < H; ++kk) acc = __fmaf_rn(m[kk], T[kk * AS + c], acc);
+                X[r * AS + c] = acc;
+            }
+        }
+        __syncthreads();
+        {   // T[32:, :32] = -T[32:, 32:] X: warp-uniform row r, lane column c;
+            // T[32:, 32:] is lower triangular, so the sum stops at kk = r
+#pragma unroll
+            for (int u = 0; u < NU; ++u) {
+                const int r = u == 0 ? warp : H - 1 - warp, c = lane;
+                const float *td = T + (H + r) * AS + H;
+                float acc = 0.0f;
+                for (int kk = 0; kk <= r; ++kk) acc = __fmaf_rn(td[kk], X[kk * AS + c], acc);
+                T[(H + r) * AS + c] = -acc;
+            }
+        }
+        __syncthreads();
+        // T operand (rows t, K = s)
+        for (int it = tid; it < C * (C / 8); it += kPrepTcThreads) {
             const int t = it % C, s0 = (it / C) * 8;
             float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = QK[t * AS + s0 + e];
-            store_split8(blk + TcBlock::kPK, blk + TcBlock::kPK + TcBlock::kPKLo, t, s0, C, x);
+            for (int e = 0; e < 8; ++e) x[e] = T[t * AS + s0 + e];
+            store_split8(t_hi, t_lo, t, s0, C, x);
         }
-    }
-    for (int i = tid; i < C * C; i += kPrepTcThreads) {   // zero the strictly upper blocks
-        const int t = i / C, s = i - t * C;
-        if (s / 16 > t / 16) T[t * AS + s] = 0.0f;
-    }
-    __syncthreads();
-    // Off-diagonal blocks by doubling: for a block lower-triangular
-    // L = [L11 0; L21 L22], L^-1 has lower-left block -L22^-1 L21 L11^-1.
-    // Level 1 (16-blocks): T10 = -T11 (M10 T00), T32 = -T33 (M32 T22);
-    // level 2 (32-blocks): T[32:, :32] = -T[32:, 32:] (M[32:, :32] T[:32, :32]).
-    // The zero upper halves of the diagonal blocks let every sum run full length.
-    float *X = QK;   // scratch once P is out
-    {
-        const int pr = tid >> 8, rr = (tid >> 4) & 15, cc = tid & 15;
-        const int bi = 2 * pr + 1, bj = 2 * pr;
-        const float *m = A + (bi * 16 + rr) * AS + bj * 16;
-        const float *tb = T + (bj * 16) * AS + bj * 16 + cc;
-        float acc = 0.0f;
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) acc = __fmaf_rn(m[kk], tb[kk * AS], acc);
-        X[(pr * 16 + rr) * AS + cc] = acc;
+        tc::fence_async_smem();
+        tc::fence_before_sync();
         __syncthreads();
-        const float *td = T + (bi * 16 + rr) * AS + bi * 16;
-        const float *xc = X + (pr * 16) * AS + cc;
-        acc = 0.0f;
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) acc = __fmaf_rn(td[kk], xc[kk * AS], acc);
-        T[(bi * 16 + rr) * AS + bj * 16 + cc] = -acc;
-    }
-    __syncthreads();
-    constexpr int H = C / 2;
-#pragma unroll
-    for (int it = tid; it < H * H; it += kPrepTcThreads) {
-        const int r = it / H, c = it % H;
-        const float *m = A + (H + r) * AS;
-        float acc = 0.0f;
-#pragma unroll
-        for (int kk = 0; kk < H; ++kk) acc = __fmaf_rn(m[kk], T[kk * AS + c], acc);
-        X[r * AS + c] = acc;
-    }
-    __syncthreads();
-    {
-        float res[H * H / kPrepTcThreads];
-#pragma unroll
-        for (int u = 0; u < H * H / kPrepTcThreads; ++u) {
-            const int it = tid + u * kPrepTcThreads, r = it / H, c = it % H;
-            const float *td = T + (H + r) * AS + H;
-            float acc = 0.0f;
-#pragma unroll
-            for (int kk = 0; kk < H; ++kk) acc = __fmaf_rn(td[kk], X[kk * AS + c], acc);
-            res[u] = -acc;
-        }
-#pragma unroll
-        for (int u = 0; u < H * H / kPrepTcThreads; ++u) {
-            const int it = tid + u * kPrepTcThreads, r = it / H, c = it % H;
-            T[(H + r) * AS + c] = res[u];
-        }
-    }
-    __syncthreads();
-    // T operand (rows t, K = s); A and QK are no longer read
-    for (int it = tid; it < C * (C / 8); it += kPrepTcThreads) {
-        const int t = it % C, s0 = (it / C) * 8;
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = T[t * AS + s0 + e];
-        store_split8(t_hi, t_lo, t, s0, C, x);
-    }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
+        tc::fence_after_sync();
 
-    // MMA 2: W^T = (b gamma K)^T T^T (columns 64..127), U~^T = (b V)^T T^T (128..191)
-    if (tid == 0) {
-        constexpr uint32_t idn = tc::idesc_bf16(128, C);
-        const uint32_t th = tc::smem_u32(t_hi), tl = tc::smem_u32(t_lo);
-        const uint32_t yh = tc::smem_u32(y_hi), yl = tc::smem_u32(y_lo);
-        const uint32_t vh = tc::smem_u32(v_hi), vl = tc::smem_u32(v_lo);
-        tc::mma_bf16<C>(tmem_base + 64, yh, th, idn, false);
-        tc::mma_bf16<C>(tmem_base + 64, yh, tl, idn, true);
-        tc::mma_bf16<C>(tmem_base + 64, yl, th, idn, true);
-        tc::mma_bf16<C>(tmem_base + 128, vh, th, idn, false);
-        tc::mma_bf16<C>(tmem_base + 128, vh, tl, idn, true);
-        tc::mma_bf16<C>(tmem_base + 128, vl, th, idn, true);
-        tc::mma_commit(&bar_mma);
-    }
-    ok = tc::mbar_wait(&bar_mma, 1, kPrepWaitLimit) && ok;
-    tc::fence_after_sync();
-    float *Wf = reinterpret_cast<float *>(B);             // W fp32 [64][LD]
-    float *Uf = reinterpret_cast<float *>(B + 34816);     // U~^T fp32 [128][AU]
-    constexpr int AU = C + 4;
-    {
-        // lane j of W^T: W[t][j] for every t (warps 0-7); lane i of U~^T: U~^T[i][t] (warps 8-15);
-        // two warps per lane quarter and matrix, 32 columns each, into fp32 stages
-        const int r = quarter * 32 + lane;
-        const bool isU = part >= 2;
-        const int c0 = (part & 1) * (C / 2);
-        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (isU ? 128 : 64) + c0;
-        uint32_t v[C / 32][16];
-#pragma unroll
-        for (int q2 = 0; q2 < C / 32; ++q2) tc::tmem_ld16_nowait(taddr + q2 * 16, v[q2]);
-        tc::tmem_wait_ld();
-        if (!isU) {   // column r of W: consecutive lanes, consecutive banks
-#pragma unroll
-            for (int q2 = 0; q2 < C / 32; ++q2)
-#pragma unroll
-                for (int e = 0; e < 16; ++e) Wf[(c0 + q2 * 16 + e) * LD + r] = __uint_as_float(v[q2][e]);
-        } else {      // row r of U~^T as float4s (eight lanes cover the 32 banks)
-            float4 *ur = reinterpret_cast<float4 *>(Uf + r * AU + c0);
-#pragma unroll
-            for (int q2 = 0; q2 < C / 32; ++q2)
-#pragma unroll
-                for (int e = 0; e < 16; e += 4)
-                    ur[q2 * 4 + e / 4] = make_float4(__uint_as_float(v[q2][e]), __uint_as_float(v[q2][e + 1]),
-                                                     __uint_as_float(v[q2][e + 2]), __uint_as_float(v[q2][e + 3]));
+        // MMA 2: W^T = (b gamma K)^T T^T (columns 64..127), U~^T = (b V)^T T^T (128..191)
+        if (tid == 0) {
+            constexpr uint32_t idn = tc::idesc_bf16(128, C);
+            const uint32_t th = tc::smem_u32(t_hi), tl = tc::smem_u32(t_lo);
+            const uint32_t yh = tc::smem_u32(y_hi), yl = tc::smem_u32(y_lo);
+            const uint32_t vh = tc::smem_u32(v_hi), vl = tc::smem_u32(v_lo);
+            tc::mma_bf16<C>(tmem_base + 64, yh, th, idn, false);
+            tc::mma_bf16<C>(tmem_base + 64, yh, tl, idn, true);
+            tc::mma_bf16<C>(tmem_base + 64, yl, th, idn, true);
+            tc::mma_bf16<C>(tmem_base + 128, vh, th, idn, false);
+            tc::mma_bf16<C>(tmem_base + 128, vh, tl, idn, true);
+            tc::mma_bf16<C>(tmem_base + 128, vl, th, idn, true);
+            tc::mma_commit(&bar_mma);
         }
-    }
-    __syncthreads();
-    for (int it = tid; it < C * (D / 8); it += kPrepTcThreads) {   // -W hi | lo, rows t, 8 columns j
-        const int t = it % C, j0 = (it / C) * 8;
-        const float4 a4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0);
-        const float4 b4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0 + 4);
-        const float x[8] = {-a4.x, -a4.y, -a4.z, -a4.w, -b4.x, -b4.y, -b4.z, -b4.w};
-        store_split8(blk + TcBlock::kWQ, blk + TcBlock::kWQ + TcBlock::kWQLo, t, j0, D, x);
-    }
-    {   // U~^T [128][64] fp32, row-major, coalesced 16-byte stores
-        float4 *dst = reinterpret_cast<float4 *>(blk + TcBlock::kUt);
-        for (int it = tid; it < D * C / 4; it += kPrepTcThreads) {
-            const int i = it / (C / 4), t4 = it % (C / 4);
-            dst[it] = *reinterpret_cast<const float4 *>(Uf + i * AU + t4 * 4);
+        ok = tc::mbar_wait(&bar_mma, ph, kPrepWaitLimit) && ok;
+        ph ^= 1;
+        tc::fence_after_sync();
+        {
+            // lane j of W^T: W[t][j] for every t (warps 0-7); lane i of U~^T: U~^T[i][t] (warps 8-15);
+            // two warps per lane quarter and matrix, 32 columns each, into fp32 stages
+            const int r = quarter * 32 + lane;
+            const bool isU = part >= 2;
+            const int c0 = (part & 1) * (C / 2);
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (isU ? 128 : 64) + c0;
+            uint32_t v[C / 32][16];
+#pragma unroll
+            for (int q2 = 0; q2 < C / 32; ++q2) tc::tmem_ld16_nowait(taddr + q2 * 16, v[q2]);
+            tc::tmem_wait_ld();
+            if (!isU) {   // column r of W: consecutive lanes, consecutive banks
+#pragma unroll
+                for (int q2 = 0; q2 < C / 32; ++q2)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) Wf[(c0 + q2 * 16 + e) * LD + r] = __uint_as_float(v[q2][e]);
+            } else {      // row r of U~^T as float4s (eight lanes cover the 32 banks)
+                float4 *ur = reinterpret_cast<float4 *>(Uf + r * AU + c0);
+#pragma unroll
+                for (int q2 = 0; q2 < C / 32; ++q2)
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4)
+                        ur[q2 * 4 + e / 4] = make_float4(__uint_as_float(v[q2][e]), __uint_as_float(v[q2][e + 1]),
+                                                         __uint_as_float(v[q2][e + 2]), __uint_as_float(v[q2][e + 3]));
+            }
         }
+        __syncthreads();
+        for (int it = tid; it < C * (D / 8); it += kPrepTcThreads) {   // -W hi | lo, rows t, 8 columns j
+            const int t = it % C, j0 = (it / C) * 8;
+            const float4 a4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0);
+            const float4 b4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0 + 4);
+            const float x[8] = {-a4.x, -a4.y, -a4.z, -a4.w, -b4.x, -b4.y, -b4.z, -b4.w};
+            store_split8(blk + TcBlock::kWQ, blk + TcBlock::kWQ + TcBlock::kWQLo, t, j0, D, x);
+        }
+        {   // U~^T [128][64] fp32, row-major, coalesced 16-byte stores
+            float4 *dst = reinterpret_cast<float4 *>(blk + TcBlock::kUt);
+            for (int it = tid; it < D * C / 4; it += kPrepTcThreads) {
+                const int i = it / (C / 4), t4 = it % (C / 4);
+                dst[it] = *reinterpret_cast<const float4 *>(Uf + i * AU + t4 * 4);
+            }
+        }
+        if (tid == 0) *reinterpret_cast<float *>(blk + TcBlock::kMisc) = eG[n - 1];
+        __syncthreads();   // the stages are read; the next head reuses regions 1 and 2
     }
     if (tid == 0) {
-        *reinterpret_cast<float *>(blk + TcBlock::kMisc) = eG[n - 1];
         if (!ok) raise_error(p.err, GDN_DERR_TIMEOUT);
-    }
-    if (tid == 0) {   // no MMA may still write TMEM when it is freed
-        tc::mma_commit(&bar_mma);
-        tc::mbar_wait(&bar_mma, 0, kPrepWaitLimit);
+        tc::mma_commit(&bar_mma);   // no MMA may still write TMEM when it is freed
+        tc::mbar_wait(&bar_mma, ph, kPrepWaitLimit);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -1367,21 +1386,42 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
 template <int D>
 __device__ __forceinline__ void norm_item(const PrefillParams &p, size_t item, int lane) {
     constexpr int CPL = D / 32;
-    const float *o = p.ws_out + item * D + lane * CPL;
+    static_assert(CPL == 1 || CPL == 2 || CPL == 4, "lane slices of 1, 2 or 4 elements");
     float ov[CPL];
+    uint16_t zb[CPL], wb[CPL];
+    const size_t at = item * D + lane * CPL;
+    if constexpr (CPL == 4) {   // 16-byte O, 8-byte z and w per lane
+        const float4 o4 = *reinterpret_cast<const float4 *>(p.ws_out + at);
+        ov[0] = o4.x; ov[1] = o4.y; ov[2] = o4.z; ov[3] = o4.w;
+        const uint2 z2 = *reinterpret_cast<const uint2 *>(p.z + at);
+        const uint2 w2 = *reinterpret_cast<const uint2 *>(p.norm_w + lane * CPL);
+        zb[0] = z2.x & 0xffffu; zb[1] = z2.x >> 16; zb[2] = z2.y & 0xffffu; zb[3] = z2.y >> 16;
+        wb[0] = w2.x & 0xffffu; wb[1] = w2.x >> 16; wb[2] = w2.y & 0xffffu; wb[3] = w2.y >> 16;
+    } else {
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) ov[c] = o[c];
+        for (int c = 0; c < CPL; ++c) {
+            ov[c] = p.ws_out[at + c];
+            zb[c] = p.z[at + c];
+            wb[c] = p.norm_w[lane * CPL + c];
+        }
+    }
     float ss = __fmul_rn(ov[0], ov[0]);
 #pragma unroll
     for (int c = 1; c < CPL; ++c) ss = __fmaf_rn(ov[c], ov[c], ss);
     ss = warp_sum(ss);
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.0f / D), p.eps_rms)));
+    uint16_t yb[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
-        const float zz = bf_bits(p.z[item * D + lane * CPL + c]);
-        const float wn = bf_bits(p.norm_w[lane * CPL + c]);
-        const float yv = __fmul_rn(__fmul_rn(__fmul_rn(ov[c], inv), wn), silu(zz));
-        p.y[item * D + lane * CPL + c] = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
+        const float yv = __fmul_rn(__fmul_rn(__fmul_rn(ov[c], inv), bf_bits(wb[c])), silu(bf_bits(zb[c])));
+        yb[c] = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
+    }
+    if constexpr (CPL == 4) {
+        *reinterpret_cast<uint2 *>(p.y + at) =
+            make_uint2((uint32_t)yb[0] | ((uint32_t)yb[1] << 16), (uint32_t)yb[2] | ((uint32_t)yb[3] << 16));
+    } else {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) p.y[at + c] = yb[c];
     }
 }
 
