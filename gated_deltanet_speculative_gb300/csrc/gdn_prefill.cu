@@ -15,20 +15,24 @@ namespace {
 // soon as that prep is done, so the scan (one CTA per head and sequence, far
 // fewer than the SMs) overlaps the prep of the groups after it; the norm of
 // group g runs on a third stream after that scan, so it never holds up the
-// next scan.
-// Only the last group's scan and norm cannot overlap any prep, so the groups
-// shrink: each takes kGroupShare of the chunks left (at least kGroupMin).
-// The scan keeps up as long as a group's scan is no longer than the next
-// group's prep: on GB300, 27B-like heads, a chunk costs ~4.8 us of scan and
-// ~7.5 us of (shared-SM) prep, which a share of 0.35 leaves room for.
+// next scan.  Only the last group's scan and norm cannot overlap any prep,
+// so after an optional first group of kGroupFirst chunks the groups shrink:
+// each takes kGroupShare of the chunks left (at least kGroupMin).  (Holding
+// the prep grid below the SM count, so that scan CTAs never wait for an SM,
+// measured slower: the prep lost more than the scan gained.)
+constexpr int kGroupFirst = 0;
 constexpr double kGroupShare = 0.35;
 constexpr int kGroupMin = 4;
-constexpr int kMaxGroups = 32;
+constexpr int kMaxGroups = 64;
 
 // Group boundaries of `chunks` chunks into b[0..n]; returns n.
 int chunk_groups(int chunks, int (&b)[kMaxGroups + 1]) {
     int n = 0, at = 0;
     b[0] = 0;
+    if (kGroupFirst > 0 && chunks > kGroupFirst + kGroupMin) {
+        at = kGroupFirst;
+        b[++n] = at;
+    }
     while (at < chunks && n < kMaxGroups) {
         const int left = chunks - at;
         int take = (int)(left * kGroupShare + 0.999);
@@ -38,6 +42,19 @@ int chunk_groups(int chunks, int (&b)[kMaxGroups + 1]) {
         b[++n] = at;
     }
     return n;
+}
+
+// SMs of the current device (0 if unknown).
+int sm_count() {
+    static int n_sm[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (n_sm[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        n_sm[dev] = v;
+    }
+    return n_sm[dev];
 }
 
 struct SideStream {
@@ -97,8 +114,14 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
         if (e != cudaSuccess) return e;
         int bounds[kMaxGroups + 1];
         const int groups = pipelined ? chunk_groups(p.max_chunks, bounds) : 1;
+        const int n_sm = sm_count() > 0 ? sm_count() : 1;
+        auto prep_grid = [&](int reserve) {
+            const int items = (p.c_hi - p.c_lo) * p.Hk;
+            const int ctas = n_sm - reserve > 1 ? n_sm - reserve : 1;
+            return items < ctas ? items : ctas;
+        };
         if (groups <= 1) {
-            gdn_prefill_prep_tc_kernel<C><<<dim3(p.Hk, p.max_chunks), kPrepTcThreads, kPrepTcSmem, st>>>(p);
+            gdn_prefill_prep_tc_kernel<C><<<prep_grid(0), kPrepTcThreads, kPrepTcSmem, st>>>(p);
             gdn_prefill_scan_tc_kernel<C><<<dim3(p.Hv, p.n_seqs), kScanTcThreads, kScanTcSmem, st>>>(p);
             gdn_prefill_norm_kernel<D><<<norm_blocks, kNormThreads, 0, st>>>(p);
             return cudaGetLastError();
@@ -113,7 +136,7 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
         for (int g = 0; g < groups; ++g) {
             p.c_lo = bounds[g];
             p.c_hi = bounds[g + 1];
-            gdn_prefill_prep_tc_kernel<C><<<dim3(p.Hk, p.c_hi - p.c_lo), kPrepTcThreads, kPrepTcSmem, st>>>(p);
+            gdn_prefill_prep_tc_kernel<C><<<(p.c_hi - p.c_lo) * p.Hk, kPrepTcThreads, kPrepTcSmem, st>>>(p);
             // (a recorded event may be recorded again once a wait on it is enqueued)
             if ((e = cudaEventRecord(ss->ready, st)) != cudaSuccess) return e;
             if ((e = cudaStreamWaitEvent(ss->stream, ss->ready, 0)) != cudaSuccess) return e;

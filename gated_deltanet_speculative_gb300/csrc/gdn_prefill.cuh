@@ -603,9 +603,11 @@ __global__ void __launch_bounds__(NT, 1) gdn_prefill_scan_kernel(const PrefillPa
 }
 
 // ---------------------------------------------------------------------------
-// prep on the tensor cores (d = 128, C = 64): one CTA of 512 threads per
-// (key head, global chunk), all chunks in parallel.  It writes the chunk
-// block (TcBlock) of each of the G value heads that share the key head.
+// prep on the tensor cores (d = 128, C = 64): a persistent grid of CTAs of
+// 512 threads, each taking (key head, global chunk) items of [c_lo, c_hi)
+// in turn (the grid may be held below the SM count so that a concurrent
+// scan finds free SMs).  An item writes the chunk block (TcBlock) of each
+// of the G value heads that share the key head.
 // Once per key head:
 //   conv + SiLU of the q and k channels (16-row pieces of one channel, no
 //   per-row branches); L2 norms, eight rows per warp in one reduce-scatter;
@@ -665,23 +667,39 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     __shared__ __align__(8) uint64_t bar_mma;
     __shared__ uint32_t tmem_base;
 
-    const int kh = blockIdx.x, gc = p.c_lo + blockIdx.y, tid = threadIdx.x;
+    const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const size_t CH = (size_t)p.CH;
+    if (warp == 0) tc::tmem_alloc(&tmem_base, 256);
+    if (tid == 0) {
+        tc::mbar_init(&bar_mma, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    bool ok = true;
+    uint32_t ph = 0;   // parity of the next bar_mma completion
+    const int items = (p.c_hi - p.c_lo) * p.Hk;
+
+#pragma unroll 1
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int kh = item % p.Hk, gc = p.c_lo + item / p.Hk;
+    __syncthreads();   // every thread has read the previous item's info
     if (tid == 0) {
         int seq = -1, start = 0, n = 0, seq_start = 0, bad = 0;
-        const bool ok = locate_chunk(p, C, gc, seq, start, n, seq_start, bad);
-        const int sl = ok ? __ldg(p.slot + seq) : -1;
-        if (ok && (sl < 0 || sl >= p.n_slots)) bad |= 2;
+        const bool found = locate_chunk(p, C, gc, seq, start, n, seq_start, bad);
+        const int sl = found ? __ldg(p.slot + seq) : -1;
+        if (found && (sl < 0 || sl >= p.n_slots)) bad |= 2;
         if (bad && kh == 0) raise_error(p.err, (bad & 1 ? GDN_DERR_SEQLENS : 0) | (bad & 2 ? GDN_DERR_SLOT : 0));
-        info[0] = (ok && !bad) ? n : 0;
+        info[0] = (found && !bad) ? n : 0;
         info[1] = start;
         info[2] = seq_start;
         info[3] = sl;
     }
     __syncthreads();
     const int n = info[0], start = info[1], seq_start = info[2], sl = info[3];
-    if (n == 0) return;
+    if (n == 0) continue;   // uniform over the CTA
 
     // conv inputs: rows start-3 .. start+n-1 (the slot's kept tail before the
     // sequence), 16 bytes per copy
@@ -702,11 +720,6 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         cp_async16(xqk + (size_t)row * 2 * D + part * D + off, src_of(row, pchannel<D>(part, off, p.Hk, kh, 0)));
     }
     stage_v(kh * p.G);
-    if (warp == 0) tc::tmem_alloc(&tmem_base, 256);
-    if (tid == 0) {
-        tc::mbar_init(&bar_mma, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
     cp_async_wait_all();
     __syncthreads();
 
@@ -793,8 +806,8 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         tc::mma_bf16<D>(tmem_base, al, ah, idn, true);
         tc::mma_commit(&bar_mma);
     }
-    bool ok = tc::mbar_wait(&bar_mma, 0, kPrepWaitLimit);
-    uint32_t ph = 1;   // parity of the next bar_mma completion
+    ok = tc::mbar_wait(&bar_mma, ph, kPrepWaitLimit) && ok;
+    ph ^= 1;
     tc::fence_after_sync();
     const int quarter = warp & 3, part = warp >> 2;   // 16 warps: lane quarter x column part
 
@@ -1043,6 +1056,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         if (tid == 0) *reinterpret_cast<float *>(blk + TcBlock::kMisc) = eG[n - 1];
         __syncthreads();   // the stages are read; the next head reuses regions 1 and 2
     }
+    }   // items
     if (tid == 0) {
         if (!ok) raise_error(p.err, GDN_DERR_TIMEOUT);
         tc::mma_commit(&bar_mma);   // no MMA may still write TMEM when it is freed
