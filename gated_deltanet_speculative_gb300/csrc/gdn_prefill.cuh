@@ -636,8 +636,10 @@ constexpr int kPtR2 = kPtR1 + 65536;           // 66304: q | k conv inputs [67][
                                                //   head M, P, T fp32 [64][65] and the T operand
                                                //   (at + 49920), then the U~^T fp32 stage [128][68]
 constexpr int kPtR3 = kPtR2 + 66304;           // 17152: v conv inputs [67][128] bf16 of one head
-constexpr int kPtVec = kPtR3 + 17152;          // g, beta, G, eG, eGC [64] each
-constexpr size_t kPrepTcSmem = kPtVec + 5 * 64 * 4;
+constexpr int kPrepMaxG = 8;                   // value heads per key head (the ABI's limit)
+constexpr int kPtVec = kPtR3 + 17152;          // beta, G, eG, eGC [kPrepMaxG][64] each
+constexpr int kPtCw = kPtVec + 4 * kPrepMaxG * 64 * 4;   // conv weights: q | k channels [256][4], then one head's v [128][4]
+constexpr size_t kPrepTcSmem = kPtCw + 384 * 4 * 2;
 
 template <int C>
 __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(const PrefillParams p) {
@@ -661,8 +663,12 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     unsigned char *t_hi = R2 + 49920, *t_lo = t_hi + 8192;      // T operand [C][C]
     float *Wf = reinterpret_cast<float *>(R1);                  // W [C][LD] after MMA 2
     float *Uf = reinterpret_cast<float *>(R2);                  // U~^T [D][AU] after MMA 2
-    float *g = reinterpret_cast<float *>(psm + kPtVec);
-    float *beta = g + C, *Gc = beta + C, *eG = Gc + C, *eGC = eG + C;
+    float *beta_all = reinterpret_cast<float *>(psm + kPtVec);      // [G][C], every head of the key head
+    float *Gc_all = beta_all + kPrepMaxG * C;                        // log decays, then their prefix sums
+    float *eG_all = Gc_all + kPrepMaxG * C;
+    float *eGC_all = eG_all + kPrepMaxG * C;
+    uint16_t *cw_qk = reinterpret_cast<uint16_t *>(psm + kPtCw);   // [2D][4]
+    uint16_t *cw_v = cw_qk + 2 * D * 4;                              // [D][4] of the head in hand
     __shared__ int info[4];
     __shared__ __align__(8) uint64_t bar_mma;
     __shared__ uint32_t tmem_base;
@@ -708,27 +714,57 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         return tok >= seq_start ? p.mixed + (size_t)tok * CH + c
                                 : p.tail + ((size_t)sl * 3 + (3 - (seq_start - tok))) * CH + c;
     };
-    auto stage_v = [&](int h) {   // head h's v channels into xv
+    auto stage_v = [&](int h) {   // head h's v channels into xv and their conv weights into cw_v
         for (int i = tid; i < (n + 3) * (D / 8); i += kPrepTcThreads) {
             const int row = i / (D / 8), off = (i - row * (D / 8)) * 8;
             cp_async16(xv + (size_t)row * D + off, src_of(row, pchannel<D>(2, off, p.Hk, kh, h)));
         }
+        if (tid < D / 2) cp_async16(cw_v + tid * 8, p.conv_w + (size_t)pchannel<D>(2, tid * 2, p.Hk, kh, h) * 4);
     };
     for (int i = tid; i < (n + 3) * (2 * D / 8); i += kPrepTcThreads) {   // the key head's q | k channels
         const int row = i / (2 * D / 8), ch = i - row * (2 * D / 8);
         const int part = ch / (D / 8), off = (ch - part * (D / 8)) * 8;
         cp_async16(xqk + (size_t)row * 2 * D + part * D + off, src_of(row, pchannel<D>(part, off, p.Hk, kh, 0)));
     }
+    if (tid < D) {   // q | k conv weights, two channels per copy
+        const int part = tid / (D / 2), e0 = (tid - part * (D / 2)) * 2;
+        cp_async16(cw_qk + (part * D + e0) * 4, p.conv_w + (size_t)pchannel<D>(part, e0, p.Hk, kh, 0) * 4);
+    }
     stage_v(kh * p.G);
+    // gates of every value head of the key head (rows >= n: beta = 0, log decay 0)
+    for (int i = tid; i < p.G * C; i += kPrepTcThreads) {
+        const int gi = i / C, t = i - gi * C, h = kh * p.G + gi;
+        float gg = 0.0f, bb = 0.0f;
+        if (t < n) {
+            const size_t ai = (size_t)(start + t) * p.Hv + h;
+            gg = -__fmul_rn(expf(p.A_log[h]), softplusf_rn(__fadd_rn(bf_bits(p.a[ai]), p.dt_bias[h])));
+            bb = sigmoidf_rn(bf_bits(p.b[ai]));
+        }
+        Gc_all[gi * C + t] = gg;
+        beta_all[gi * C + t] = bb;
+    }
     cp_async_wait_all();
     __syncthreads();
+    for (int gi = warp; gi < p.G; gi += kPrepTcThreads / 32) {   // inclusive prefix sums, two rows per lane
+        float *Gc = Gc_all + gi * C;
+        const float a0 = Gc[2 * lane], a1 = Gc[2 * lane + 1];
+        float run = __fadd_rn(a0, a1);
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_up_sync(kFull, run, off);
+            if (lane >= off) run = __fadd_rn(run, o);
+        }
+        const float excl = __shfl_up_sync(kFull, run, 1);
+        Gc[2 * lane] = __fadd_rn(lane == 0 ? 0.0f : excl, a0);
+        Gc[2 * lane + 1] = run;
+    }
 
     // conv + SiLU of q and k: work item (16-row piece, channel), a sliding
     // window of the four taps down the piece.  Rows >= n read unstaged inputs
     // and are replaced by 0 with a select, so the 16 rows carry no branches.
     constexpr int PR = 16;
-    auto conv_piece = [&](const uint16_t *x, int stride, int c, int t0, float (&act)[PR]) {
-        const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(p.conv_w + (size_t)c * 4));
+    auto conv_piece = [&](const uint16_t *x, int stride, const uint16_t *wsm, int t0, float (&act)[PR]) {
+        const uint2 wv = *reinterpret_cast<const uint2 *>(wsm);
         const float w0 = bf_bits(wv.x & 0xffffu), w1 = bf_bits(wv.x >> 16);
         const float w2 = bf_bits(wv.y & 0xffffu), w3 = bf_bits(wv.y >> 16);
         float x0 = bf_bits(x[0]), x1 = bf_bits(x[stride]), x2 = bf_bits(x[2 * stride]);
@@ -750,10 +786,16 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         const int cc = it % (2 * D), t0 = (it / (2 * D)) * PR;   // warp-uniform part and t0
         const int part = cc / D, e = cc - part * D;
         float act[PR];
-        conv_piece(xqk + (size_t)t0 * 2 * D + cc, 2 * D, pchannel<D>(part, e, p.Hk, kh, 0), t0, act);
+        conv_piece(xqk + (size_t)t0 * 2 * D + cc, 2 * D, cw_qk + cc * 4, t0, act);
         float *dst = (part == 0 ? q : k) + e;
 #pragma unroll
         for (int r = 0; r < PR; ++r) dst[(t0 + r) * LD] = act[r];
+    }
+    for (int i = tid; i < p.G * C; i += kPrepTcThreads) {   // gamma and gamma_C / gamma of every head
+        const int gi = i / C, t = i - gi * C;
+        const float *Gc = Gc_all + gi * C;
+        eG_all[i] = __expf(Gc[t]);
+        eGC_all[i] = __expf(__fsub_rn(Gc[n - 1], Gc[t]));
     }
     __syncthreads();
     // L2 norms of q and k rows, q scaled: warp w takes rows 8w .. 8w+7 of the
@@ -815,36 +857,16 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     for (int gi = 0; gi < p.G; ++gi) {
         const int h = kh * p.G + gi;
         unsigned char *blk = reinterpret_cast<unsigned char *>(p.ws_chunks) + ((size_t)gc * p.Hv + h) * TcBlock::kBytes;
-        if (gi > 0) cp_async_wait_all();   // this head's v inputs
-        // gates (rows >= n: beta = 0, log decay 0)
-        if (tid < C) {
-            float gg = 0.0f, bb = 0.0f;
-            if (tid < n) {
-                const size_t gi2 = (size_t)(start + tid) * p.Hv + h;
-                gg = -__fmul_rn(expf(p.A_log[h]), softplusf_rn(__fadd_rn(bf_bits(p.a[gi2]), p.dt_bias[h])));
-                bb = sigmoidf_rn(bf_bits(p.b[gi2]));
-            }
-            g[tid] = gg;
-            beta[tid] = bb;
-        }
-        __syncthreads();
-        if (warp == 0) {   // inclusive prefix sum of the log decays, two rows per lane
-            const float a0 = g[2 * lane], a1 = g[2 * lane + 1];
-            float run = __fadd_rn(a0, a1);
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float o = __shfl_up_sync(kFull, run, off);
-                if (lane >= off) run = __fadd_rn(run, o);
-            }
-            const float excl = __shfl_up_sync(kFull, run, 1);
-            Gc[2 * lane] = __fadd_rn(lane == 0 ? 0.0f : excl, a0);
-            Gc[2 * lane + 1] = run;
+        const float *beta = beta_all + gi * C, *Gc = Gc_all + gi * C, *eG = eG_all + gi * C, *eGC = eGC_all + gi * C;
+        if (gi > 0) {   // this head's v inputs and weights
+            cp_async_wait_all();
+            __syncthreads();
         }
         // conv + SiLU of h's v channels straight into (diag(b) V)^T
         for (int it = tid; it < (C / PR) * D; it += kPrepTcThreads) {
             const int e = it % D, t0 = (it / D) * PR;
             float act[PR];
-            conv_piece(xv + (size_t)t0 * D + e, D, pchannel<D>(2, e, p.Hk, kh, h), t0, act);
+            conv_piece(xv + (size_t)t0 * D + e, D, cw_v + e * 4, t0, act);
 #pragma unroll
             for (int h8 = 0; h8 < PR; h8 += 8) {
                 float vb[8];
@@ -853,13 +875,8 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
                 store_split8(v_hi, v_lo, e, t0 + h8, C, vb);
             }
         }
-        __syncthreads();   // xv consumed; Gc complete
+        __syncthreads();   // xv and cw_v consumed
         if (gi + 1 < p.G) stage_v(h + 1);   // in flight while this head is worked on
-        if (tid < C) {
-            eG[tid] = __expf(Gc[tid]);
-            eGC[tid] = __expf(__fsub_rn(Gc[n - 1], Gc[tid]));
-        }
-        __syncthreads();
         // (diag(b gamma) K)^T operand, K~^T and Q~ for the scan
         for (int it = tid; it < D * (C / 8); it += kPrepTcThreads) {   // rows j, 8 t
             const int j = it % D, t0 = (it / D) * 8;
