@@ -173,3 +173,49 @@ def test_pipelined_prefill_equals_single_stream_bitwise():
     assert np.array_equal(host_bits(out["tail"]), host_bits(cache2["tail"]))
     # and against the oracle
     compare(c, {"y": host_bits(out["y"]), "state": out["state"].cpu().numpy(), "tail": host_bits(out["tail"])})
+
+
+def test_pipelined_prefill_captured_in_a_graph_equals_eager_bitwise():
+    """The d = 128 prefill forks onto the library's side streams and joins
+    back with events; captured in a CUDA graph on a caller stream, replays
+    must equal eager calls bit for bit (new inputs copied in between)."""
+    g = synth.Geometry(4, 12, 128, 128)
+    c = Case(g, [700, 130, 64, 1], seed=73, n_slots=6)
+    d = c.dims_gpu()
+    T = c.R
+    w = c.dev_weights()
+    slot, cu = dev(c.slots), dev(c.row_ptr)
+    base = c.dev_cache()
+    cache = {"state": base["state"].clone(), "tail": base["tail"].clone()}
+    rows = c.dev_rows(poison=False)
+    ws = torch.empty(gdn.prefill_workspace_size(d, c.S, T), dtype=torch.uint8, device="cuda")
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        gdn.prefill(d, w, cache, slot, cu, rows, ws, stream=side)   # warm-up (makes the side streams)
+        side.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            gdn.prefill(d, w, cache, slot, cu, rows, ws, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+
+    rng = np.random.default_rng(74)
+    for trial in range(2):
+        mixed = synth.to_bf16_bits(rng.standard_normal(c.rows["mixed"].shape).astype(np.float32))
+        rows["mixed"].copy_(torch.from_numpy(mixed.view(np.int16)).view(torch.bfloat16))
+        cache["state"].copy_(base["state"])
+        cache["tail"].copy_(base["tail"])
+        rows["y"].zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert gdn.get_device_error() == 0
+        got = (host_bits(rows["y"]), cache["state"].cpu().numpy().view(np.uint32), host_bits(cache["tail"]))
+        e_cache = {"state": base["state"].clone(), "tail": base["tail"].clone()}
+        e_rows = dict(rows, y=torch.zeros_like(rows["y"]))
+        gdn.prefill(d, w, e_cache, slot, cu, e_rows, ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(got[0], host_bits(e_rows["y"]))
+        assert np.array_equal(got[1], e_cache["state"].cpu().numpy().view(np.uint32))
+        assert np.array_equal(got[2], host_bits(e_cache["tail"]))
