@@ -140,6 +140,15 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
+// The two halves of a cluster barrier, for a CTA that only needs to know
+// that every CTA of its cluster has started.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
 // Global conv channel of element e of part (0 = q, 1 = k, 2 = v) of value head h.
 template <int D>
 __device__ __forceinline__ int channel_of(int part, int e, int Hk, int kh, int h) {
@@ -170,6 +179,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
     const int h = blockIdx.x / P, s = blockIdx.y;
     const int sli = blockIdx.x % P;               // row slice: state rows [row0, row0 + D/P)
     const int row0 = sli * (D / P);
+    if constexpr (P > 1) cluster_arrive_relaxed();   // "started"; waited on before the first remote store
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kh = h / p.G;
     const size_t CH = (size_t)p.CH;
@@ -306,10 +316,12 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
     }
     __syncthreads();
 
-    if (MODE == kStep) {
-        // Every CTA of this key-head group has staged the old tail; now shift
-        // it in place: the lead CTA moves the shared q/k channels, each CTA its v.
-        cluster_sync_all();
+    // The in-place tail shift of a step: every CTA of the cluster (the key
+    // head's value heads, and their row slices) must have staged the old tail
+    // before the lead slices overwrite it.  Unsliced steps wait for that here;
+    // sliced steps shift after the cluster barrier that gathers o, which every
+    // slice reaches only after its staging.
+    auto shift_tail = [&]() {
         for (int i = tid; i < (sli == 0 ? 3 * per_row : 0); i += kRowThreads) {   // slice 0 of each head
             const int m = i / per_row;
             const int ch = own_lo + i - m * per_row;
@@ -318,6 +330,10 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
             *reinterpret_cast<uint4 *>(p.tail + ((size_t)sl * 3 + m) * CH + c) =
                 *reinterpret_cast<const uint4 *>(&sm.u.xin[m + 1][part * D + off]);
         }
+    };
+    if (MODE == kStep && P == 1) {
+        cluster_sync_all();
+        shift_tail();
     }
 
     // ---- a3: L2 norm of q and k ------------------------------------------------
@@ -351,6 +367,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
                 p.log_k[((size_t)(r0 + i / D) * p.Hk + kh) * D + i % D] = sm.k[i / D][i % D];
     }
     __syncthreads();
+    if constexpr (P > 1) cluster_wait();   // every slice has started: remote stores are safe
 
     // ---- a5 + a6: the recurrence, row by row; no CTA barrier inside --------
     const int vi = lane >> SHIFT;
@@ -409,8 +426,12 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
             p.log_u[((size_t)(r0 + t) * p.Hv + h) * D + warp * RPW + vi] = u;
     }
     if (MODE == kStep) store_tile<D, RPW, CPL>(slot_tile + (size_t)row0 * D, S, warp, lane, false);
-    if constexpr (P > 1) cluster_sync_all();   // every slice's o rows have landed in every slice
-    else __syncthreads();
+    if constexpr (P > 1) {
+        cluster_sync_all();   // every slice's o rows have landed in every slice
+        shift_tail();         // and every slice has staged the old tail long ago
+    } else {
+        __syncthreads();
+    }
 
     // ---- a7: gated RMSNorm, y in bf16 ----------------------------------------
     for (int t = warp; t < n; t += kRowWarps) {
