@@ -219,3 +219,37 @@ def test_pipelined_prefill_captured_in_a_graph_equals_eager_bitwise():
         assert np.array_equal(got[0], host_bits(e_rows["y"]))
         assert np.array_equal(got[1], e_cache["state"].cpu().numpy().view(np.uint32))
         assert np.array_equal(got[2], host_bits(e_cache["tail"]))
+
+
+def test_single_stream_prefill_with_several_items_per_cta_equals_pipelined_bitwise():
+    """On the single-stream plan (gdn_prefill_noalloc) the prep grid is at
+    most one CTA per SM, so with more (key head, chunk) items than SMs a CTA
+    takes several items in turn, carrying its TMEM and barrier phases across
+    them: 5000 tokens with 2 key heads are 158 items.  The pipelined plan
+    gives every item its own CTA; the two must agree bit for bit."""
+    import ctypes
+    from gated_deltanet_speculative_gb300 import _binding as B
+    g = synth.Geometry(2, 4, 128, 128)
+    c = Case(g, [5000], seed=79, zero_state=True)
+    d = c.dims_gpu()
+    T = c.R
+    assert gdn.prefill_workspace_size(d, 1, T) <= 64 << 20
+    out = run_prefill(c)
+
+    fn = gdn.load().gdn_prefill_noalloc
+    fn.argtypes = [ctypes.POINTER(B.c_dims), ctypes.POINTER(B.c_weights), ctypes.POINTER(B.c_cache),
+                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(B.c_rows),
+                   ctypes.c_int32, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    w, cache, rows = c.dev_weights(), c.dev_cache(), c.dev_rows()
+    cw, cc, cr = B._weights(d, w), B._cache(d, cache), B._rows(d, rows, T)
+    slot, cu = dev(c.slots), dev(c.row_ptr)
+    rc = fn(ctypes.byref(d.c()), ctypes.byref(cw), ctypes.byref(cc), ctypes.c_void_p(slot.data_ptr()),
+            ctypes.c_void_p(cu.data_ptr()), 1, T, ctypes.byref(cr), 64,
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert gdn.get_device_error() == 0
+    assert np.array_equal(out["y"], host_bits(rows["y"]))
+    assert np.array_equal(out["state"].view(np.uint32), cache["state"].cpu().numpy().view(np.uint32))
+    assert np.array_equal(out["tail"], host_bits(cache["tail"]))
