@@ -90,7 +90,9 @@ struct __align__(16) RowSmem {
     // the ancestor's staged row is 3 + e
     int anc[kMaxRows][3];
     int parent[kMaxRows];
-    int reused[kMaxRows];   // tree: re-read later by a non-adjacent child
+    int reused[kMaxRows];   // tree: re-read later by a child that does not follow it
+    int order[kMaxRows];    // tree: depth-first preorder (children in row order); else 0, 1, ...
+    int nsub[kMaxRows];     // tree: subtree sizes, then each node's next free preorder slot
     int bad;
 };
 
@@ -264,7 +266,35 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
                     --tail_next;
                 }
             }
-            if (MODE == kTree && sm.parent[t] >= 0 && sm.parent[t] != t - 1) sm.reused[sm.parent[t]] = 1;
+        }
+        // Visit order: a chain in row order; a tree depth first, so that a node
+        // follows its parent wherever it can and the parent's state is still
+        // in registers (only a node's later children reload it).  Preorder
+        // without a stack: subtree sizes bottom-up (parents precede
+        // children), then each node takes its parent's next free slot.
+        for (int t = 0; t < n; ++t) sm.order[t] = t;
+        if (MODE == kTree && !bad) {
+            for (int t = 0; t < n; ++t) sm.nsub[t] = 1;
+            for (int t = n - 1; t > 0; --t)
+                if (sm.parent[t] >= 0) sm.nsub[sm.parent[t]] += sm.nsub[t];
+            int root_next = 0;
+            for (int t = 0; t < n; ++t) {
+                const int par = sm.parent[t];
+                int pre;
+                if (par < 0) {
+                    pre = root_next;
+                    root_next += sm.nsub[t];
+                } else {
+                    pre = sm.nsub[par];   // the parent's next free slot (set below when it was placed)
+                    sm.nsub[par] = pre + sm.nsub[t];
+                }
+                sm.order[pre] = t;
+                sm.nsub[t] = pre + 1;     // from here on: this node's next free slot
+            }
+            for (int j = 1; j < n; ++j) {
+                const int par = sm.parent[sm.order[j]];
+                if (par >= 0 && par != sm.order[j - 1]) sm.reused[par] = 1;
+            }
         }
         if (bad && h == 0) raise_error(p.err, bad);
         sm.bad = bad;
@@ -371,10 +401,11 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
 
     // ---- a5 + a6: the recurrence, row by row; no CTA barrier inside --------
     const int vi = lane >> SHIFT;
-    for (int t = 0; t < n; ++t) {
-        if (MODE == kTree && t > 0) {
+    for (int j = 0; j < n; ++j) {
+        const int t = MODE == kTree ? sm.order[j] : j;   // the row (node) in hand
+        if (MODE == kTree && j > 0) {
             const int par = sm.parent[t];
-            if (par != t - 1)
+            if (par != sm.order[j - 1])
                 load_tile<D, RPW, CPL>(S, par < 0 ? slot_tile : p.rec_state + ((size_t)(r0 + par) * p.Hv + h) * tile,
                                        warp, lane);
         }
