@@ -278,10 +278,59 @@ def run_ours(args, rank, world, local_rank):
         ev2[i][1].record(stream)
     torch.cuda.synchronize()
     barrier()
-    t2 = time.time()
     if sampler:
         sampler.stop()
-    e2e_ms = sum(ev2[i][0].elapsed_time(ev2[i][1]) for i in range(K)) / K
+    e2e_serial_ms = sum(ev2[i][0].elapsed_time(ev2[i][1]) for i in range(K)) / K
+
+    # end to end as a serving loop runs it: the same copies and calls, with
+    # two device input sets, so step i+1's host->device copies (one copy
+    # stream) and step i's y read-back (another) overlap the GPU work of the
+    # steps around them.  The timed region spans all K steps, every copy
+    # included; no L2 flush (each step writes 805 MB of records, far past L2).
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    bufs = [dict(dr), {k: torch.empty_like(v) for k, v in dr.items()}]
+    keeps = [keep_t, torch.empty_like(keep_t)]
+    host_ys = [host_y, torch.empty_like(host_y).pin_memory()]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_win = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_y = [torch.cuda.Event() for _ in range(2)]
+
+    def copy_in(b):
+        with torch.cuda.stream(h2d_s):
+            for k in ("mixed", "z", "a", "b"):
+                bufs[b][k].copy_(host_in[k], non_blocking=True)
+            keeps[b].copy_(host_keep, non_blocking=True)
+        ev_in[b].record(h2d_s)
+
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    h2d_s.wait_stream(stream)
+    copy_in(0)
+    for i in range(K):
+        b = i & 1
+        stream.wait_event(ev_in[b])
+        gdn.window(d, dw, dc, slot_t, rp_t, bufs[b], rec_state, rec_tail, stream)
+        ev_win[b].record(stream)
+        gdn.commit(d, dc, slot_t, keeps[b], rec_state, rec_tail, stream)
+        ev_done[b].record(stream)
+        d2h_s.wait_event(ev_win[b])
+        with torch.cuda.stream(d2h_s):
+            host_ys[b].copy_(bufs[b]["y"], non_blocking=True)
+        ev_y[b].record(d2h_s)
+        if i + 1 < K:
+            nb = (i + 1) & 1   # last used by step i - 1: its calls and its y read-back must be done
+            h2d_s.wait_event(ev_done[nb])
+            h2d_s.wait_event(ev_y[nb])
+            copy_in(nb)
+    stream.wait_event(ev_y[(K - 1) & 1])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t2 = time.time()
+    e2e_ms = t_start.elapsed_time(t_end) / K
     if gdn.get_device_error() != 0:
         raise RuntimeError("device error word set during the timed steps")
     extra = None
@@ -291,7 +340,8 @@ def run_ours(args, rank, world, local_rank):
         if gdn.get_device_error() != 0:
             raise RuntimeError("device error word set during the secondary measurements")
 
-    step_ms, e2e_ms, win_avg = reduce_max([step_ms, e2e_ms, statistics.mean(win_ms)], world, dev)
+    step_ms, e2e_ms, e2e_serial_ms, win_avg = reduce_max([step_ms, e2e_ms, e2e_serial_ms, statistics.mean(win_ms)],
+                                                         world, dev)
     if rank != 0:
         return None
 
@@ -328,7 +378,12 @@ def run_ours(args, rank, world, local_rank):
         "commit": {"ms_per_launch": statistics.mean(com_ms), "bytes_per_launch": commit_bytes(g, n_committed),
                    "gbs": commit_bytes(g, n_committed) / (statistics.mean(com_ms) * 1e-3) / 1e9},
         "e2e": {"value": world * R / (e2e_ms * 1e-3), "unit": "rows/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "method": "pinned host inputs copied in and y read back every step through the public API; "
+                          "two device input sets, step i+1's copies overlap step i's calls; one event pair "
+                          "around all steps, no L2 flush (805 MB of records a step)",
+                "serial": {"value": world * R / (e2e_serial_ms * 1e-3), "ms_per_step": e2e_serial_ms,
+                           "method": "each step timed alone: copies in, calls, y back, in sequence"}},
         "gpu_launches": 2 * K,
         "clocks": sampler.summary(t0, t1) if sampler else None,
         "wall_s": {"timed": t1 - t0, "e2e": t2 - t1},
