@@ -3,6 +3,8 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "gdn_rows.cuh"
 
 namespace gdn {
@@ -37,16 +39,16 @@ cudaError_t launch_step(const RowParams &p, int n_streams, cudaStream_t st) {
 // every warp keeps at least one state row, and the grid stays within two
 // CTAs per SM.
 inline int step_slices(int D, int G, int Hv, int n_streams) {
-    static int n_sm[64] = {0};
+    static std::atomic<int> n_sm[64];   // per device, 0 until first asked (any thread may fill it)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-    if (n_sm[dev] == 0) {
-        int v = 0;
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 1;
-        n_sm[dev] = v;
+    int sms = n_sm[dev].load(std::memory_order_relaxed);
+    if (sms == 0) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 1;
+        n_sm[dev].store(sms, std::memory_order_relaxed);
     }
     int P = 1;
-    while (P * 2 * G <= 8 && P * 2 <= D / 8 && (long long)Hv * n_streams * P * 2 <= 2LL * n_sm[dev]) P *= 2;
+    while (P * 2 * G <= 8 && P * 2 <= D / 8 && (long long)Hv * n_streams * P * 2 <= 2LL * sms) P *= 2;
     return P;
 }
 

@@ -1,6 +1,7 @@
 // gdn_prefill.cu -- launchers of the chunked prefill kernels (prep, scan, norm).
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "gdn_prefill.cuh"
@@ -46,15 +47,15 @@ int chunk_groups(int chunks, int (&b)[kMaxGroups + 1]) {
 
 // SMs of the current device (0 if unknown).
 int sm_count() {
-    static int n_sm[64] = {0};
+    static std::atomic<int> n_sm[64];   // per device, 0 until first asked (any thread may fill it)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (n_sm[dev] == 0) {
-        int v = 0;
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        n_sm[dev] = v;
+    int sms = n_sm[dev].load(std::memory_order_relaxed);
+    if (sms == 0) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 0;
+        n_sm[dev].store(sms, std::memory_order_relaxed);
     }
-    return n_sm[dev];
+    return sms;
 }
 
 struct SideStream {
@@ -78,11 +79,18 @@ cudaError_t side_stream(SideStream **out) {
         int lo = 0, hi = 0;
         if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess) return e;
         cudaStream_t s = nullptr, sn = nullptr;
-        if ((e = cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, hi)) != cudaSuccess) return e;
-        if ((e = cudaStreamCreateWithPriority(&sn, cudaStreamNonBlocking, lo)) != cudaSuccess) return e;
         cudaEvent_t ev[4] = {};
+        e = cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, hi);
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&sn, cudaStreamNonBlocking, lo);
         for (auto &x : ev)
-            if ((e = cudaEventCreateWithFlags(&x, cudaEventDisableTiming)) != cudaSuccess) return e;
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&x, cudaEventDisableTiming);
+        if (e != cudaSuccess) {   // give back what was made; the next call tries again
+            for (auto &x : ev)
+                if (x) cudaEventDestroy(x);
+            if (sn) cudaStreamDestroy(sn);
+            if (s) cudaStreamDestroy(s);
+            return e;
+        }
         ss.start = ev[0];
         ss.ready = ev[1];
         ss.scanned = ev[2];
