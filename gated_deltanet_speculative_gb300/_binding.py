@@ -63,6 +63,8 @@ _SIGS = {
     "gdn_prefill": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _I, _I,
                     ctypes.POINTER(c_rows), _I, _P, ctypes.c_size_t, _P],
     "gdn_prefill_workspace_size": [ctypes.POINTER(c_dims), _I, _I, _I],
+    "gdn_prefill_noalloc": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _I,
+                            _I, ctypes.POINTER(c_rows), _I, _P],
     "gdn_window_log": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _I, _I,
                        ctypes.POINTER(c_rows), _P, _P, _P, _P, _P],
     "gdn_commit_replay": [ctypes.POINTER(c_dims), ctypes.POINTER(c_cache), _P, _P, _P, _I, _I, _P, _P, _P, _P, _P],
@@ -280,6 +282,26 @@ def prefill(dims: Dims, weights: dict, cache: dict, slot, cu_seqlens, rows: dict
     _check("gdn_prefill", lib.gdn_prefill(ctypes.byref(dims.c()), ctypes.byref(cw), ctypes.byref(cc), _ptr(slot),
                                           _ptr(cu_seqlens), S, T, ctypes.byref(cr), int(chunk), _ptr(workspace),
                                           workspace.numel(), _stream_ptr(stream)))
+
+
+def prefill_noalloc(dims: Dims, weights: dict, cache: dict, slot, cu_seqlens, rows: dict,
+                    chunk: int = PREFILL_CHUNK, stream=None):
+    """gdn_prefill without a workspace: the library's fixed device scratch
+    (PREFILL_NOALLOC_SCRATCH_BYTES) stands in for it, and every launch goes
+    on the given stream.  Calls whose work overlaps on the GPU share that
+    scratch and must be serialised by the caller."""
+    lib = load()
+    _need(slot, "slot", torch.int32)
+    S = slot.numel()
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (S + 1,))
+    T = rows["mixed"].shape[0]
+    cw, cc, cr = _weights(dims, weights), _cache(dims, cache), _rows(dims, rows, T)
+    _check("gdn_prefill_noalloc", lib.gdn_prefill_noalloc(ctypes.byref(dims.c()), ctypes.byref(cw), ctypes.byref(cc),
+                                                          _ptr(slot), _ptr(cu_seqlens), S, T, ctypes.byref(cr),
+                                                          int(chunk), _stream_ptr(stream)))
+
+
+PREFILL_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 def get_device_error(stream=None) -> int:

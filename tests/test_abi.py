@@ -32,6 +32,16 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(lib, n), f"libgdn.so does not export {n}"
 
 
+def test_binding_declares_every_entry_point():
+    """The ctypes binding gives every declared entry point its argument
+    types, and the package exposes a wrapper of the same name (without the
+    gdn_ prefix) for each compute call."""
+    names = declared_functions()
+    assert names == set(B._SIGS), f"declared but not bound: {names - set(B._SIGS)}"
+    for n in names - {"gdn_status_string", "gdn_get_device_error"}:
+        assert callable(getattr(gdn, n[len("gdn_"):], None)), f"no wrapper for {n}"
+
+
 def test_status_strings():
     lib = gdn.load()
     for code in (0, -1, -2, -3, -4, -5):

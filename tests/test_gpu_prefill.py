@@ -136,13 +136,11 @@ def test_pipelined_prefill_equals_single_stream_bitwise():
     norm on the caller's stream; the two must agree bit for bit, with
     sequences that straddle group boundaries and a one-token sequence, and
     the caller's stream must see the finished result."""
-    import ctypes
-    from gated_deltanet_speculative_gb300 import _binding as B
     g = synth.Geometry(4, 12, 128, 128)
     c = Case(g, [700, 130, 64, 1], seed=67, n_slots=6)
     d = c.dims_gpu()
     T = c.R
-    assert gdn.prefill_workspace_size(d, c.S, T) <= 64 << 20
+    assert gdn.prefill_workspace_size(d, c.S, T) <= gdn.PREFILL_NOALLOC_SCRATCH_BYTES
 
     side = torch.cuda.Stream()   # a caller stream other than the default one
     w, cache, rows = c.dev_weights(), c.dev_cache(), c.dev_rows()
@@ -155,17 +153,8 @@ def test_pipelined_prefill_equals_single_stream_bitwise():
     side.synchronize()
     assert gdn.get_device_error() == 0
 
-    fn = gdn.load().gdn_prefill_noalloc
-    fn.argtypes = [ctypes.POINTER(B.c_dims), ctypes.POINTER(B.c_weights), ctypes.POINTER(B.c_cache),
-                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(B.c_rows),
-                   ctypes.c_int32, ctypes.c_void_p]
-    fn.restype = ctypes.c_int
     w2, cache2, rows2 = c.dev_weights(), c.dev_cache(), c.dev_rows()
-    cw, cc, cr = B._weights(d, w2), B._cache(d, cache2), B._rows(d, rows2, T)
-    rc = fn(ctypes.byref(d.c()), ctypes.byref(cw), ctypes.byref(cc), ctypes.c_void_p(slot.data_ptr()),
-            ctypes.c_void_p(cu.data_ptr()), c.S, T, ctypes.byref(cr), 64,
-            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
-    assert rc == 0
+    gdn.prefill_noalloc(d, w2, cache2, slot, cu, rows2)
     torch.cuda.synchronize()
     assert gdn.get_device_error() == 0
     assert np.array_equal(host_bits(out["y"]), host_bits(rows2["y"]))
@@ -227,27 +216,15 @@ def test_single_stream_prefill_with_several_items_per_cta_equals_pipelined_bitwi
     takes several items in turn, carrying its TMEM and barrier phases across
     them: 5000 tokens with 2 key heads are 158 items.  The pipelined plan
     gives every item its own CTA; the two must agree bit for bit."""
-    import ctypes
-    from gated_deltanet_speculative_gb300 import _binding as B
     g = synth.Geometry(2, 4, 128, 128)
     c = Case(g, [5000], seed=79, zero_state=True)
     d = c.dims_gpu()
     T = c.R
-    assert gdn.prefill_workspace_size(d, 1, T) <= 64 << 20
+    assert gdn.prefill_workspace_size(d, 1, T) <= gdn.PREFILL_NOALLOC_SCRATCH_BYTES
     out = run_prefill(c)
 
-    fn = gdn.load().gdn_prefill_noalloc
-    fn.argtypes = [ctypes.POINTER(B.c_dims), ctypes.POINTER(B.c_weights), ctypes.POINTER(B.c_cache),
-                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(B.c_rows),
-                   ctypes.c_int32, ctypes.c_void_p]
-    fn.restype = ctypes.c_int
     w, cache, rows = c.dev_weights(), c.dev_cache(), c.dev_rows()
-    cw, cc, cr = B._weights(d, w), B._cache(d, cache), B._rows(d, rows, T)
-    slot, cu = dev(c.slots), dev(c.row_ptr)
-    rc = fn(ctypes.byref(d.c()), ctypes.byref(cw), ctypes.byref(cc), ctypes.c_void_p(slot.data_ptr()),
-            ctypes.c_void_p(cu.data_ptr()), 1, T, ctypes.byref(cr), 64,
-            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
-    assert rc == 0
+    gdn.prefill_noalloc(d, w, cache, dev(c.slots), dev(c.row_ptr), rows)
     torch.cuda.synchronize()
     assert gdn.get_device_error() == 0
     assert np.array_equal(out["y"], host_bits(rows["y"]))
