@@ -13,14 +13,19 @@
 // which equals the row-by-row recurrence in exact arithmetic.
 //
 // Three kernels:
-//   prep  (chunk x value head, all chunks in parallel): conv + SiLU, L2 norms,
-//         gates, A, Q K^T, the forward substitution; writes the chunk's
-//         Q~ = diag(gamma) Q, K~ = diag(gamma_C / gamma) K, W, U~,
-//         P = lower(Gamma o Q K^T) and gamma_C to the workspace.
-//   scan  (sequence x value head x d_v slice, chunks in order): U, O and the
-//         state update; writes O (fp32) to the workspace, and the final state
-//         and conv tail to the slot.
+//   prep  (all chunks in parallel): conv + SiLU, L2 norms, gates, A, Q K^T,
+//         the inverse T; writes each chunk's Q~ = diag(gamma) Q,
+//         K~ = diag(gamma_C / gamma) K, W, U~, P = lower(Gamma o Q K^T) and
+//         gamma_C to the workspace.  d = 128 (tensor cores): one CTA per
+//         (key head, chunk) item serves the G value heads of the key head;
+//         d = 32, 64 (CUDA cores): one CTA per (value head, chunk).
+//   scan  (chunks in order): U, O and the state update; writes O (fp32) to
+//         the workspace, and the final state and conv tail to the slot.
+//         d = 128: one CTA per (value head, sequence), the state in TMEM;
+//         d = 32, 64: one CTA per (value head, sequence, d_v slice).
 //   norm  (token x value head): gated RMSNorm of O, y in bf16.
+// For d = 128 the launcher runs them per chunk group on three streams (see
+// gdn_prefill.cu).
 #pragma once
 
 #include "gdn_common.cuh"
