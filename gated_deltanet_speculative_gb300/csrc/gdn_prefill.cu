@@ -19,8 +19,9 @@ namespace {
 // next scan.  Only the last group's scan and norm cannot overlap any prep,
 // so after an optional first group of kGroupFirst chunks the groups shrink:
 // each takes kGroupShare of the chunks left (at least kGroupMin).  (Holding
-// the prep grid below the SM count, so that scan CTAs never wait for an SM,
-// measured slower: the prep lost more than the scan gained.)
+// every later prep grid below the SM count, so that scan CTAs never wait for
+// an SM, measured slower: the prep lost more than the scan gained.  Only the
+// first launch of the second group's prep is held so; see the launch loop.)
 constexpr int kGroupFirst = 0;
 constexpr double kGroupShare = 0.35;
 constexpr int kGroupMin = 4;
@@ -144,7 +145,22 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
         for (int g = 0; g < groups; ++g) {
             p.c_lo = bounds[g];
             p.c_hi = bounds[g + 1];
-            gdn_prefill_prep_tc_kernel<C><<<(p.c_hi - p.c_lo) * p.Hk, kPrepTcThreads, kPrepTcSmem, st>>>(p);
+            // When the first group's prep ends, its scan and the second group's
+            // prep become ready together, and the prep's CTAs, dispatched first,
+            // would take every SM while the scan waits out a whole prep item.  So
+            // the second group's prep starts with a launch of only as many
+            // chunks as leave one sequence's scan (Hv CTAs) its SMs.
+            PrefillParams pp = p;
+            if (g == 1) {
+                const int a = (n_sm - p.Hv) / p.Hk;
+                if (a >= 1 && p.c_lo + a < p.c_hi) {
+                    pp.c_hi = p.c_lo + a;
+                    gdn_prefill_prep_tc_kernel<C><<<a * p.Hk, kPrepTcThreads, kPrepTcSmem, st>>>(pp);
+                    pp.c_lo = pp.c_hi;
+                    pp.c_hi = p.c_hi;
+                }
+            }
+            gdn_prefill_prep_tc_kernel<C><<<(pp.c_hi - pp.c_lo) * p.Hk, kPrepTcThreads, kPrepTcSmem, st>>>(pp);
             // (a recorded event may be recorded again once a wait on it is enqueued)
             if ((e = cudaEventRecord(ss->ready, st)) != cudaSuccess) return e;
             if ((e = cudaStreamWaitEvent(ss->stream, ss->ready, 0)) != cudaSuccess) return e;
