@@ -18,10 +18,8 @@ namespace {
 // group g runs on a third stream after that scan, so it never holds up the
 // next scan.  Only the last group's scan and norm cannot overlap any prep,
 // so after an optional first group of kGroupFirst chunks the groups shrink:
-// each takes kGroupShare of the chunks left (at least kGroupMin).  (Holding
-// every later prep grid below the SM count, so that scan CTAs never wait for
-// an SM, measured slower: the prep lost more than the scan gained.  Only the
-// first launch of the second group's prep is held so; see the launch loop.)
+// each takes kGroupShare of the chunks left (at least kGroupMin).  How much
+// of the GPU a prep may take while a scan runs is set in the launch loop.
 constexpr int kGroupFirst = 0;
 constexpr double kGroupShare = 0.35;
 constexpr int kGroupMin = 4;
@@ -142,25 +140,35 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
         if ((e = cudaEventRecord(ss->start, st)) != cudaSuccess) return e;
         if ((e = cudaStreamWaitEvent(ss->stream, ss->start, 0)) != cudaSuccess) return e;
         if ((e = cudaStreamWaitEvent(ss->norm, ss->start, 0)) != cudaSuccess) return e;
+        const bool hold_one = p.n_seqs == 1 && n_sm - p.Hv >= p.Hk;
         for (int g = 0; g < groups; ++g) {
             p.c_lo = bounds[g];
             p.c_hi = bounds[g + 1];
-            // When the first group's prep ends, its scan and the second group's
-            // prep become ready together, and the prep's CTAs, dispatched first,
-            // would take every SM while the scan waits out a whole prep item.  So
-            // the second group's prep starts with a launch of only as many
-            // chunks as leave one sequence's scan (Hv CTAs) its SMs.
+            // A prep launched while a scan runs must leave the scan its SMs: when
+            // a scan launch ends, the next one is dispatched a few microseconds
+            // later, and prep CTAs still waiting for an SM would take the freed
+            // ones and keep them for a whole prep item.  With one sequence the
+            // scan is Hv CTAs, so every prep after the first runs as a
+            // persistent grid of the other SMs.  With several, the number of
+            // scan CTAs per group depends on the lengths (device data), so only
+            // the second group's prep, which becomes ready together with the
+            // first scan, starts with a launch small enough to leave one
+            // sequence's scan its SMs.
             PrefillParams pp = p;
-            if (g == 1) {
+            int grid = (p.c_hi - p.c_lo) * p.Hk;
+            if (g >= 1 && hold_one) {
+                grid = grid < n_sm - p.Hv ? grid : n_sm - p.Hv;
+            } else if (g == 1) {
                 const int a = (n_sm - p.Hv) / p.Hk;
                 if (a >= 1 && p.c_lo + a < p.c_hi) {
                     pp.c_hi = p.c_lo + a;
                     gdn_prefill_prep_tc_kernel<C><<<a * p.Hk, kPrepTcThreads, kPrepTcSmem, st>>>(pp);
                     pp.c_lo = pp.c_hi;
                     pp.c_hi = p.c_hi;
+                    grid = (pp.c_hi - pp.c_lo) * p.Hk;
                 }
             }
-            gdn_prefill_prep_tc_kernel<C><<<(pp.c_hi - pp.c_lo) * p.Hk, kPrepTcThreads, kPrepTcSmem, st>>>(pp);
+            gdn_prefill_prep_tc_kernel<C><<<grid, kPrepTcThreads, kPrepTcSmem, st>>>(pp);
             // (a recorded event may be recorded again once a wait on it is enqueued)
             if ((e = cudaEventRecord(ss->ready, st)) != cudaSuccess) return e;
             if ((e = cudaStreamWaitEvent(ss->stream, ss->ready, 0)) != cudaSuccess) return e;
