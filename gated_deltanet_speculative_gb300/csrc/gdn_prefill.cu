@@ -17,9 +17,10 @@ namespace {
 // fewer than the SMs) overlaps the prep of the groups after it; the norm of
 // group g runs on a third stream after that scan, so it never holds up the
 // next scan.  Only the last group's scan and norm cannot overlap any prep,
-// so after an optional first group of kGroupFirst chunks the groups shrink:
-// each takes kGroupShare of the chunks left (at least kGroupMin).  How much
-// of the GPU a prep may take while a scan runs is set in the launch loop.
+// so with several sequences, after an optional first group of kGroupFirst
+// chunks, the groups shrink: each takes kGroupShare of the chunks left (at
+// least kGroupMin).  One sequence uses round_groups below.  How much of the
+// GPU a prep may take while a scan runs is set in the launch loop.
 constexpr int kGroupFirst = 0;
 constexpr double kGroupShare = 0.35;
 constexpr int kGroupMin = 4;
@@ -38,6 +39,28 @@ int chunk_groups(int chunks, int (&b)[kMaxGroups + 1]) {
         int take = (int)(left * kGroupShare + 0.999);
         take = take < kGroupMin ? kGroupMin : take;
         if (left - take < kGroupMin || n == kMaxGroups - 1) take = left;
+        at += take;
+        b[++n] = at;
+    }
+    return n;
+}
+
+// Groups for one sequence, sized in whole prep rounds (a round = one item
+// per CTA of the prep grid, a prep item taking about as long as a scan
+// launch needs for one round's chunks): the first group fills kRounds0
+// rounds of all n_sm SMs, each later one kRounds rounds of the n_sm - Hv SMs
+// a prep keeps while a scan runs; the last takes what is left.
+constexpr int kRounds0 = 2;
+constexpr int kRounds = 2;
+int round_groups(int chunks, int n_sm, int Hk, int Hv, int (&b)[kMaxGroups + 1]) {
+    int first = kRounds0 * n_sm / Hk, later = kRounds * (n_sm - Hv) / Hk;
+    first = first < 1 ? 1 : first;
+    later = later < 1 ? 1 : later;
+    int n = 0, at = 0;
+    b[0] = 0;
+    while (at < chunks && n < kMaxGroups) {
+        int take = n == 0 ? first : later;
+        if (chunks - at < take || n == kMaxGroups - 1) take = chunks - at;
         at += take;
         b[++n] = at;
     }
@@ -120,8 +143,11 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
                                  (int)kScanTcSmem);
         if (e != cudaSuccess) return e;
         int bounds[kMaxGroups + 1];
-        const int groups = pipelined ? chunk_groups(p.max_chunks, bounds) : 1;
         const int n_sm = sm_count() > 0 ? sm_count() : 1;
+        const bool hold_one = p.n_seqs == 1 && n_sm - p.Hv >= p.Hk;
+        const int groups = !pipelined ? 1
+                           : hold_one ? round_groups(p.max_chunks, n_sm, p.Hk, p.Hv, bounds)
+                                      : chunk_groups(p.max_chunks, bounds);
         auto prep_grid = [&](int reserve) {
             const int items = (p.c_hi - p.c_lo) * p.Hk;
             const int ctas = n_sm - reserve > 1 ? n_sm - reserve : 1;
@@ -140,7 +166,6 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
         if ((e = cudaEventRecord(ss->start, st)) != cudaSuccess) return e;
         if ((e = cudaStreamWaitEvent(ss->stream, ss->start, 0)) != cudaSuccess) return e;
         if ((e = cudaStreamWaitEvent(ss->norm, ss->start, 0)) != cudaSuccess) return e;
-        const bool hold_one = p.n_seqs == 1 && n_sm - p.Hv >= p.Hk;
         for (int g = 0; g < groups; ++g) {
             p.c_lo = bounds[g];
             p.c_hi = bounds[g + 1];
