@@ -1260,6 +1260,23 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
     bool ok = true;
     int issued = 1;   // chunks (counted from c_first) whose copies have been issued
     const int n_run = c_end - c_first;
+    // A chunk's O^T row leaves TMEM at the chunk's end but goes to the
+    // workspace only after the next chunk's group-1 MMAs are issued: the
+    // stores (32 KB a chunk, bound by the SM's store rate) then drain while
+    // the tensor core works instead of delaying the next issue.
+    uint32_t o_r[C / 32][16];
+    int o_start = 0, o_n = 0;
+    auto store_o = [&]() {
+        float *ocol = p.ws_out + ((size_t)o_start * p.Hv + h) * D + i;
+#pragma unroll
+        for (int q = 0; q < C / 32; ++q)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int t = half * (C / 2) + q * 16 + e;
+                if (t < o_n) ocol[(size_t)t * p.Hv * D] = __uint_as_float(o_r[q][e]);
+            }
+        o_n = 0;
+    };
 #pragma unroll 1
     for (int c = 0; c < n_run && ok; ++c) {   // c counts from c_first
         const unsigned char *blk = blk0 + (size_t)c * blk_stride;
@@ -1294,7 +1311,8 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
                 tc::mma_commit(&bar_u);
             }
         }
-        // while the MMAs run: the next chunk's gamma_C and U~^T row
+        // while the MMAs run: the previous chunk's O, the next chunk's gamma_C and U~^T row
+        if (o_n > 0) store_o();
         float gC_nx = 0.0f;
         if (more) {
             gC_nx = *reinterpret_cast<const float *>(blk + blk_stride + TcBlock::kMisc);
@@ -1346,23 +1364,15 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
             split_and_scale_state(tl, half, gC);   // the next chunk's S operand
         }
 
-        // O^T row i -> O[t][i] for the chunk's live rows
-        {
-            uint32_t r[C / 32][16];
+        // O^T row i out of TMEM (stored to O[t][i] during the next chunk's group 1)
 #pragma unroll
-            for (int q = 0; q < C / 32; ++q) tc::tmem_ld16_nowait(tl + 64 + half * (C / 2) + q * 16, r[q]);
-            tc::tmem_wait_ld();
-            float *ocol = p.ws_out + ((size_t)start * p.Hv + h) * D + i;
-#pragma unroll
-            for (int q = 0; q < C / 32; ++q)
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int t = half * (C / 2) + q * 16 + e;
-                    if (t < n) ocol[(size_t)t * p.Hv * D] = __uint_as_float(r[q][e]);
-                }
-        }
+        for (int q = 0; q < C / 32; ++q) tc::tmem_ld16_nowait(tl + 64 + half * (C / 2) + q * 16, o_r[q]);
+        tc::tmem_wait_ld();
+        o_start = start;
+        o_n = n;
         if (more && !fail) seed_group1<C>(tl, half, ut);   // after this lane's U and O columns are read
     }
+    if (ok && o_n > 0) store_o();   // the last chunk's O
     __syncthreads();
     ok = fail == 0;
 
