@@ -659,7 +659,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     unsigned char *R1 = psm + kPtR1, *R2 = psm + kPtR2;
     uint16_t *xqk = reinterpret_cast<uint16_t *>(R2);           // [C+3][2D] q | k inputs
     uint16_t *xv = reinterpret_cast<uint16_t *>(psm + kPtR3);   // [C+3][D] v inputs of the head in hand
-    unsigned char *kq_hi = R1, *kq_lo = R1 + 32768;             // [K; Q] operand
+    unsigned char *kq_hi = R2, *kq_lo = R2 + 32768;             // [K; Q] operand (after the conv)
     unsigned char *v_hi = R1, *v_lo = R1 + 16384;               // (b V)^T [D][C]
     unsigned char *y_hi = R1 + 32768, *y_lo = y_hi + 16384;     // (b gamma K)^T [D][C]
     float *A = reinterpret_cast<float *>(R2);                   // M [C][AS]
@@ -853,9 +853,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         tc::mma_bf16<D>(tmem_base, al, ah, idn, true);
         tc::mma_commit(&bar_mma);
     }
-    ok = tc::mbar_wait(&bar_mma, ph, kPrepWaitLimit) && ok;
-    ph ^= 1;
-    tc::fence_after_sync();
+    // (waited for before the first head's M, P: its v conv and operands overlap MMA 1)
     const int quarter = warp & 3, part = warp >> 2;   // 16 warps: lane quarter x column part
 
 #pragma unroll 1
@@ -903,6 +901,11 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
             const float xq[8] = {__fmul_rn(a, a4.x), __fmul_rn(a, a4.y), __fmul_rn(a, a4.z), __fmul_rn(a, a4.w),
                                  __fmul_rn(a, b4.x), __fmul_rn(a, b4.y), __fmul_rn(a, b4.z), __fmul_rn(a, b4.w)};
             store_split8(blk + TcBlock::kWQ, blk + TcBlock::kWQ + TcBlock::kWQLo, C + t, j0, D, xq);
+        }
+        if (gi == 0) {   // MMA 1 done: [A; QK] in TMEM, region 2 free for M, P, T
+            ok = tc::mbar_wait(&bar_mma, ph, kPrepWaitLimit) && ok;
+            ph ^= 1;
+            tc::fence_after_sync();
         }
         {   // lane r holds row r of [A; QK]; the four warps on a lane quarter take
             // 16 columns each and form M = strict_lower(diag(b) Gamma o A) and
