@@ -214,8 +214,11 @@ def test_single_stream_prefill_with_several_items_per_cta_equals_pipelined_bitwi
     """On the single-stream plan (gdn_prefill_noalloc) the prep grid is at
     most one CTA per SM, so with more (key head, chunk) items than SMs a CTA
     takes several items in turn, carrying its TMEM and barrier phases across
-    them: 5000 tokens with 2 key heads are 158 items.  The pipelined plan
-    gives every item its own CTA; the two must agree bit for bit."""
+    them: 5000 tokens with 2 key heads are 158 items.  gdn_prefill must give
+    the same bits.  (With one sequence gdn_prefill cuts groups in whole prep
+    rounds, and with 2 key heads the first group already holds all 79
+    chunks; the persistent preps of its later groups are covered by the
+    4722-token test against the oracle.)"""
     g = synth.Geometry(2, 4, 128, 128)
     c = Case(g, [5000], seed=79, zero_state=True)
     d = c.dims_gpu()
