@@ -1,6 +1,7 @@
 // gdn_commit.cuh -- commit of each stream's accepted path (TensorFold #747,
-// first note: "commit only each stream's accepted path"; TensorFold #932,
-// Qwen3.5 CUDA note: recorded rows let the lane core "keep partial copies").
+// first note: of a shared round, each stream keeps only its accepted rows;
+// TensorFold #932, Qwen3.5 CUDA note: the recorded rows are what lets the
+// engine keep a stream's partially accepted window).
 //
 // One CTA per (value head h, stream s) copies the recorded [D x D] fp32 tile
 // of the kept row into the stream's slot, plus 1/Hv of the kept row's conv
@@ -69,8 +70,8 @@ __global__ void __launch_bounds__(kCommitThreads) gdn_commit_kernel(const Commit
 // update per row,  S <- u k^T + a S  with the same rounding as the window
 // (fma(u_i, k_j, a * S_ij)), so the result equals the state the window would
 // have recorded for the kept row, bit for bit.  The conv tail is the kept
-// row's recorded tail.  (TensorFold #932, tree note: "keep replays the kept
-// path onto the recurrence in one pass".)
+// row's recorded tail.  (TensorFold #932, tree note: the commit re-applies
+// the accepted rows' logs to the committed state in a single pass.)
 struct ReplayParams {
     int Hk, Hv, G, CH;
     float *state;

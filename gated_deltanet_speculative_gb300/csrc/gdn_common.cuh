@@ -4,10 +4,10 @@
 // and the norms is written with explicit round-to-nearest intrinsics
 // (__fmul_rn / __fadd_rn / __fmaf_rn / __fdiv_rn / __fsqrt_rn), so no
 // compiler contraction can make two kernels that share these helpers round
-// differently.  That is what lets a window's rows equal one-row steps bit
-// for bit, and a tree node equal the chain along its path (TensorFold #932,
-// note on the Qwen3.5 CUDA engine: "a window's rows equal one-row steps bit
-// for bit").
+// differently.  That is what makes every row of a window identical, bit for
+// bit, to the same row run as a single step, and a tree node identical to
+// the chain along its path (TensorFold #932, note on the Qwen3.5 CUDA
+// engine, which asks exactly that of windows).
 #pragma once
 
 #include <cuda_bf16.h>

@@ -1,6 +1,6 @@
 // gdn_prefill.cuh -- chunked prompt prefill of the GDN layer (TensorFold
-// #747, first note: the engine's "prompt chain" kernel; prompts that arrive
-// together share one prefill pass).
+// #747, first note: the engine has a kernel for prompts, and prompts that
+// come in together are prefilled in one pass).
 //
 // The recurrence S_t = a_t S_{t-1} + u_t k_t^T with u_t = b_t (v_t - a_t
 // S_{t-1} k_t) is evaluated chunk by chunk (C rows).  Inside a chunk, with

@@ -33,8 +33,9 @@
 namespace gdn {
 
 // kWindowLog: a chain window that logs each row's decay, write u and key
-// instead of recording its state (TensorFold #932, tree note: each stream
-// logs its rows' decay, write and key, and keep replays the kept path).
+// instead of recording its state (TensorFold #932, tree note: per-row logs
+// of the decay, the write vector and the key replace the recorded states,
+// and the commit replays them).
 enum RowMode : int { kStep = 0, kWindow = 1, kTree = 2, kWindowLog = 3 };
 
 struct RowParams {

@@ -9,27 +9,29 @@
  * and the gated RMSNorm  y = RMSNorm(o) * w_norm * SiLU(z).
  *
  * Sources, by page:
- *  [P932]  TensorFold #932 "perf(qwen3_5 cuda): deliver the first token
- *          before drafting".  Commit notes on the Qwen3.5 CUDA engine:
- *          - "MLX affine 4-bit checkpoint on the native CUDA server": the
- *            layer glue is the gated delta rule and a causal convolution;
- *            windows of up to 16 rows record each row's recurrence and
- *            convolution tail; a window's rows equal one-row steps bit for
- *            bit.
- *          - "The 2B's CUDA engine now reads its widths": value heads over
- *            fewer key heads; A_log per value head.
- *          - "A verify window's rows may form a tree": each row's parent is
- *            given, and the convolution taps and the delta rule follow the
- *            row's own branch; one-row steps and prompts update in place.
- *  [P747]  TensorFold #747 "perf(qwen27 cuda): reduce repeated-prompt
- *          TTFT", first commit note: verify rounds take every stream's
- *          window together, up to 16 streams of 16 rows, and commit only
- *          each stream's accepted path; the engine's kernels include the
- *          GDN tree, replay and prompt-chain kernels; prompts that arrive
- *          together share one prefill pass.
- *  [P888]  TensorFold #888 "Qwen3.5/3.8 on CUDA: kept prompt states in host
- *          memory": a kept state is a stream's DeltaNet recurrences and
- *          conv windows, whole.
+ *  [P932]  TensorFold #932, titled "perf(qwen3_5 cuda): deliver the first
+ *          token before drafting".  Its commit notes on the Qwen3.5 CUDA
+ *          engine:
+ *          - the note on the MLX affine 4-bit checkpoint: the layer's glue
+ *            is a causal conv and the gated delta rule; a verify window of
+ *            at most 16 rows keeps every row's state and conv tail, and
+ *            each of its rows must match the same row run as a single step,
+ *            bit for bit;
+ *          - the note on the 2B engine's widths: fewer key heads than value
+ *            heads, one A_log per value head;
+ *          - the tree note: a window's rows can form a tree given by each
+ *            row's parent, the conv taps and the recurrence following each
+ *            row's own branch; single steps and prompts write the slot
+ *            directly.
+ *  [P747]  TensorFold #747, titled "perf(qwen27 cuda): reduce repeated-prompt
+ *          TTFT", first commit note: one verify round serves the windows of
+ *          all streams (at most 16 streams of 16 rows) and keeps only each
+ *          stream's accepted rows; the engine has kernels for trees, for
+ *          replays and for prompts, and prompts that come in together are
+ *          prefilled in one pass.
+ *  [P888]  TensorFold #888, titled "Qwen3.5/3.8 on CUDA: kept prompt states
+ *          in host memory": a kept state is the full recurrent state of a
+ *          stream together with its conv history.
  *
  * Conventions shared by every entry point
  *  - Every pointer argument named "device" is a CUDA device pointer owned by
@@ -130,10 +132,9 @@ int gdn_step(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
              void *stream);
 
 /*
- * gdn_window -- chain verify windows of up to 16 rows per stream, recorded
- * row by row ([P932] "Windows of up to 16 rows record each row's recurrence
- * and convolution tail"; [P747] shared rounds of up to 16 streams of 16
- * rows).  Stream s owns packed rows [row_ptr[s], row_ptr[s+1]) of `rows`;
+ * gdn_window -- chain verify windows (at most 16 rows a stream), recorded
+ * row by row ([P932] MLX checkpoint note: every row's state and conv tail
+ * are kept; [P747] one round for at most 16 streams x 16 rows).  Stream s owns packed rows [row_ptr[s], row_ptr[s+1]) of `rows`;
  * its first row follows the committed state and tail of slot[s], each later
  * row the row before it.  The committed slot is NOT modified.
  *   slot       device int32 [n_streams]
@@ -153,9 +154,9 @@ int gdn_window(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cach
                void *rec_tail, void *stream);
 
 /*
- * gdn_tree -- tree verify windows ([P932] "A verify window's rows may form
- * a tree (each row's parent given): the convolution taps, the delta rule
- * and attention follow each row's own branch").  As gdn_window, plus
+ * gdn_tree -- tree verify windows ([P932] tree note: a row's parent is
+ * given, and its conv taps and recurrence follow its own branch).  As
+ * gdn_window, plus
  *   parent  device int32 [n_rows]: for packed row r of stream s, the
  *           window-local index (0-based within the stream's rows) of its
  *           parent, which must be smaller than its own index, or -1 for a
@@ -170,8 +171,9 @@ int gdn_tree(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
              float *rec_state, void *rec_tail, void *stream);
 
 /*
- * gdn_commit -- keep each stream's accepted path ([P747] "commit only each
- * stream's accepted path"; [P932] recorded rows "keep partial copies").
+ * gdn_commit -- keep each stream's accepted path ([P747] first note: each
+ * stream keeps only its accepted rows; [P932] MLX checkpoint note: the
+ * recorded rows are what let a partially accepted window be kept).
  * For stream s with keep_row[s] = r >= 0 (a packed row index, normally the
  * last accepted row of the stream's window or the chosen tree node),
  * slot[s]'s state and tail become rec_state[r] and rec_tail[r].
@@ -185,9 +187,9 @@ int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot
                const float *rec_state, const void *rec_tail, void *stream);
 
 /*
- * gdn_prefill -- chunked prompt prefill ([P747] "prompt chain" kernel and
- * prompts that "arrive together share one prefill pass"; [P932] tree note:
- * prompts update in place).  Sequence s owns packed tokens
+ * gdn_prefill -- chunked prompt prefill ([P747] the engine's prompt kernel,
+ * several prompts prefilled in one pass; [P932] tree note: a prompt writes
+ * its slot directly).  Sequence s owns packed tokens
  * [cu_seqlens[s], cu_seqlens[s+1]) of `rows`; it starts from slot[s]'s
  * committed state and tail (zero them for a fresh prompt; a nonzero state
  * resumes a kept one) and leaves the state and tail after its last token
@@ -249,10 +251,9 @@ int gdn_prefill_noalloc(const gdn_dims *dims, const gdn_weights *w, const gdn_ca
 
 /*
  * gdn_window_log -- chain verify windows that log instead of record
- * ([P932] tree note: "A verify no longer snapshots every row's state (1.3 GB
- * shared, which capped the 27B at 8 rows): each stream logs its rows'
- * decay, write and key, and keep replays the kept path onto the recurrence
- * in one pass").  As gdn_window (same y and rec_tail, bit for bit), but in
+ * ([P932] tree note: keeping a state per row took 1.3 GB and limited the
+ * 27B to 8-row windows, so each row now leaves a log of its decay, write
+ * vector and key, and the commit replays the accepted rows).  As gdn_window (same y and rec_tail, bit for bit), but in
  * place of rec_state it writes, for every row r:
  *   log_a  device fp32 [R, Hv]         the decay a_r
  *   log_u  device fp32 [R, Hv, d_v]    the write u_r = b_r (v_r - a_r S_{r-1} k_r)

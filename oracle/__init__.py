@@ -9,11 +9,11 @@ their raw ``uint16`` bit patterns, fp32 states as ``float32``; results are
 ``float64`` (states, outputs) or ``uint16`` (copied bf16 tails).
 
 Sources (by page title): TensorFold #932 "deliver the first token before
-drafting" (gated delta rule and causal convolution in the 2B's CUDA glue;
-recorded windows of up to 16 rows; tree windows whose taps and recurrence
-follow each row's branch) and TensorFold #747 "reduce repeated-prompt TTFT"
-(shared verify rounds of up to 16 streams x 16 rows; commit of the accepted
-path only).
+drafting" (a causal conv and the gated delta rule in the CUDA glue; verify
+windows of at most 16 rows with every row's state kept; tree windows whose
+taps and recurrence follow each row's branch) and TensorFold #747 "reduce
+repeated-prompt TTFT" (one verify round for at most 16 streams x 16 rows;
+only the accepted rows of each stream are kept).
 """
 from __future__ import annotations
 

@@ -9,16 +9,16 @@
  *
  * Sources of the operation (cited by page title and passage):
  *  - TensorFold #932 "deliver the first token before drafting", commit note
- *    on the 2B's CUDA engine: the layer's glue is the gated delta rule and a
- *    causal convolution; windows of up to 16 rows record each row's
- *    recurrence and convolution tail; a window's rows equal one-row steps.
+ *    on the MLX checkpoint for the CUDA engine: the layer's glue is a causal
+ *    conv and the gated delta rule; a verify window (at most 16 rows) keeps
+ *    every row's state and conv tail, and its rows must match single steps.
  *  - Same page, note on the 2B reading its widths from config.json: more
  *    linear value heads than key heads (grouped heads).
  *  - Same page, note on tree windows: each row has a parent, and the
- *    convolution taps and the delta rule follow the row's own branch.
- *  - TensorFold #747 "reduce repeated-prompt TTFT", first commit note: a
- *    verify round holds up to 16 streams of 16 rows, and only each stream's
- *    accepted path is committed.
+ *    conv taps and the recurrence follow the row's own branch.
+ *  - TensorFold #747 "reduce repeated-prompt TTFT", first commit note: one
+ *    verify round serves at most 16 streams of 16 rows, and each stream
+ *    keeps only its accepted rows.
  *  - The layer's arithmetic (the gated-DeltaNet layer of this model family):
  *      conv1d width 4 with a kept tail, SiLU, L2-normalised q and k,
  *      S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T,  o_t = S_t q_t,

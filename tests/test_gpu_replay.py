@@ -1,6 +1,6 @@
-"""Logged windows and replay commit (TensorFold #932, tree note: each stream
-logs its rows' decay, write and key, and keep replays the kept path onto the
-recurrence in one pass).
+"""Logged windows and replay commit (TensorFold #932, tree note: per-row logs
+of the decay, the write vector and the key replace the recorded states, and
+the commit re-applies the accepted rows to the committed state in one pass).
 
 gdn_window_log must give gdn_window's y and tails bit for bit, its logs must
 be the oracle's per-row decay and key (to tolerance) and satisfy

@@ -1,17 +1,19 @@
 """Shared verify rounds of every shape, one captured graph for all shapes, and
 prompt passes resumed at a chunk-grid point.
 
-* Randomised shared rounds (TensorFold #747, first note: 54 verify windows of
-  chains, trees and shared rounds of 2 to 16 streams, up to 256 rows, at every
-  alignment of the packed inputs): each round is compared with the oracle.
+* Randomised shared rounds (TensorFold #747, first note: the engine's checks
+  cover chain and tree windows and rounds shared by 2 to 16 streams, at most
+  256 rows, packed at every possible offset): each round is compared with the
+  oracle.
 * One CUDA graph of gdn_window / gdn_tree / gdn_commit captured for the
   largest shape serves every smaller shape: the kernels read the true row
-  counts from the device (TensorFold #932, drafter note: "the kernels read the
-  true counts from the device"), so replays with new row_ptr / parent /
+  counts from the device (TensorFold #932, drafter note: the row counts are
+  read on the device, not baked into the launch), so replays with new row_ptr / parent /
   keep_row contents equal eager calls bit for bit.
 * A prompt split at a multiple of the chunk (a grid point) and resumed from
   the kept state ends bit-identical to one pass (TensorFold #747, kept state
-  note: a pass resumed at a grid point computes what a fresh pass does).
+  note: resuming at a grid point gives the same result as an uninterrupted
+  pass).
 """
 import numpy as np
 import pytest
