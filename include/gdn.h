@@ -208,15 +208,17 @@ int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot
  * x d_v slice) and norm (token x head).  They run after the work enqueued
  * on `stream` before the call, and work enqueued on `stream` after the call
  * runs after them, so the call behaves as if all of it were on `stream`.
- * For d = 128 the chunks are taken in groups that shrink toward the end
- * (about 35% of the chunks left each, at least 4): prep of a group
- * runs on `stream`, its scan on a highest-priority side stream and its norm
- * on a third stream of the library (two streams and four events per device,
+ * For d = 128 the chunks are taken in groups: prep of a group runs on
+ * `stream`, its scan on a highest-priority side stream and its norm on a
+ * third stream of the library (two streams and four events per device,
  * made by the first such call on that device), forked from and joined back
- * to `stream` by events, so they overlap the prep of later groups.  The side stream is shared: calls made from
- * several host threads at once are serialised on it.  The fork and join
- * are ordinary event record / wait calls, so the call can be captured in
- * a CUDA graph.
+ * to `stream` by events, so they overlap the prep of later groups.  With
+ * one sequence the groups are sized in whole prep rounds of the SMs and
+ * every prep after the first leaves the scan's SMs free; with several they
+ * shrink toward the end (about 35% of the chunks left each, at least 4).
+ * The side streams are shared: calls made from several host threads at
+ * once are serialised on them.  The fork and join are ordinary event
+ * record / wait calls, so the call can be captured in a CUDA graph.
  */
 int gdn_prefill(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
                 const int32_t *slot, const int32_t *cu_seqlens, int32_t n_seqs,
