@@ -227,7 +227,7 @@ size_t prefill_chunk_floats(int D) {
     switch (D) {
         case 32: return ChunkBlock<32, kPrefillChunk>::kFloats;
         case 64: return ChunkBlock<64, kPrefillChunk>::kFloats;
-        default: return ChunkBlock<128, kPrefillChunk>::kFloats;
+        default: return TcBlock::kBytes / 4;   // d = 128: the tensor-core layout
     }
 }
 

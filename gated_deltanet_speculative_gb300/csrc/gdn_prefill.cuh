@@ -14,9 +14,10 @@
 //
 // Three kernels:
 //   prep  (all chunks in parallel): conv + SiLU, L2 norms, gates, A, Q K^T,
-//         the inverse T; writes each chunk's Q~ = diag(gamma) Q,
-//         K~ = diag(gamma_C / gamma) K, W, U~, P = lower(Gamma o Q K^T) and
-//         gamma_C to the workspace.  d = 128 (tensor cores): one CTA per
+//         the inverse T; writes each chunk's Q~ = diag(gamma) Q (d = 128:
+//         Q once per key head, gamma_t per value head), K~ = diag(gamma_C /
+//         gamma) K, W, U~, P = lower(Gamma o Q K^T) and gamma_C to the
+//         workspace.  d = 128 (tensor cores): one CTA per
 //         (key head, chunk) item serves the G value heads of the key head;
 //         d = 32, 64 (CUDA cores): one CTA per (value head, chunk).
 //   scan  (chunks in order): U, O and the state update; writes O (fp32) to
@@ -78,12 +79,15 @@ struct ChunkBlock {
 // bytes.  bf16 operands are pre-split (x = hi + lo, both bf16) and stored in
 // the K-major no-swizzle layout of gdn_tc.cuh, hi block then lo block.  Two
 // stacked operands, so that each group of the scan is one wide product:
-//   [-W; Q~]    rows 0..63 -W (rows t), 64..127 Q~ (rows t), K = j (128):
-//               B operand of [U^T | O^T] = [U~^T | 0] + S0 [-W; Q~]^T  (N = 128)
+//   [-W; Q]     rows 0..63 -W (rows t), 64..127 Q (rows t), K = j (128):
+//               B operand of [U^T | O1^T] = [U~^T | 0] + S0 [-W; Q]^T  (N = 128).
+//               Q is the key head's, so only the block of the first value
+//               head of a key head holds it; the scan takes it from there.
 //   [P; K~^T]   rows 0..63 P (rows t, K = s), 64..191 K~^T (rows j, K = t),
-//               K = 64:  B operand of [O^T | S] += U^T [P; K~^T]^T  (N = 192)
+//               K = 64:  B operand of [O2^T | S] += U^T [P; K~^T]^T  (N = 192)
+//               and O = diag(gamma) O1 + O2
 //   U~^T fp32 [128 i][64 t]           the group-1 accumulator's start
-//   gamma_C
+//   gamma_C, then gamma_t [64]
 struct TcBlock {
     static constexpr int kWQ = 0;           // [-W; Q~] hi; lo at + kWQLo
     static constexpr int kWQLo = 32768;
@@ -94,9 +98,10 @@ struct TcBlock {
     static constexpr int kOpBytes = 114688;
     static constexpr int kUt = 114688;
     static constexpr int kMisc = 147456;
-    static constexpr int kBytes = 147472;
+    static constexpr int kGam = 147472;     // gamma_t, fp32 [64]
+    static constexpr int kBytes = 147728;
+    static constexpr int kHalf = 16384;     // bytes of rows 0..63 of a 128-row operand with K = 128
 };
-static_assert(TcBlock::kBytes == ChunkBlock<128, 64>::kFloats * 4, "tensor-core block must match the fp32 block size");
 
 // Store 8 consecutive k (k0 multiple of 8) of row r of a K-major bf16
 // operand (K columns), split x = hi + lo: hi into `hi_base`, lo into
@@ -620,7 +625,8 @@ __global__ void __launch_bounds__(NT, 1) gdn_prefill_scan_kernel(const PrefillPa
 // Then for each value head h of the group (its v inputs staged while the
 // previous head is worked on):
 //   gates of h; conv + SiLU of h's v channels straight into (diag(b) V)^T;
-//   (diag(b gamma) K)^T, K~^T and Q~ = diag(gamma) Q;
+//   (diag(b gamma) K)^T and K~^T (Q, shared by the value heads, goes out
+//   once per item, with gamma_t of each head for the scan);
 //   M = strict_lower(diag(b) Gamma o A), P = lower(Gamma o Q K^T), formed
 //   from the TMEM readout of MMA 1 with h's gates;
 //   T = (I + M)^-1 on the CUDA cores (fp32): 16 x 16 diagonal blocks by
@@ -853,7 +859,21 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         tc::mma_bf16<D>(tmem_base, al, ah, idn, true);
         tc::mma_commit(&bar_mma);
     }
-    // (waited for before the first head's M, P: its v conv and operands overlap MMA 1)
+    {   // Q (rows 64..127 of the [K; Q] operand, hi and lo) into the block of the
+        // key head's first value head, where the scan of every value head of
+        // the key head takes it (rows >= n are zero)
+        unsigned char *lead = reinterpret_cast<unsigned char *>(p.ws_chunks) +
+                              ((size_t)gc * p.Hv + (size_t)kh * p.G) * TcBlock::kBytes;
+        constexpr int V4 = TcBlock::kHalf / 16;   // 16-byte pieces of one half
+        for (int it = tid; it < 2 * V4; it += kPrepTcThreads) {
+            const int lo_part = it / V4, e = it - lo_part * V4;
+            const unsigned char *src = (lo_part ? kq_lo : kq_hi) + TcBlock::kHalf;
+            unsigned char *dst = lead + (lo_part ? TcBlock::kWQLo : 0) + TcBlock::kHalf;
+            reinterpret_cast<float4 *>(dst)[e] = reinterpret_cast<const float4 *>(src)[e];
+        }
+    }
+    // (MMA 1 is waited for before the first head's M, P: its v conv and
+    // operands, and the Q copy, overlap it)
     const int quarter = warp & 3, part = warp >> 2;   // 16 warps: lane quarter x column part
 
 #pragma unroll 1
@@ -880,7 +900,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         }
         __syncthreads();   // xv and cw_v consumed
         if (gi + 1 < p.G) stage_v(h + 1);   // in flight while this head is worked on
-        // (diag(b gamma) K)^T operand, K~^T and Q~ for the scan
+        // (diag(b gamma) K)^T operand and K~^T for the scan
         for (int it = tid; it < D * (C / 8); it += kPrepTcThreads) {   // rows j, 8 t
             const int j = it % D, t0 = (it / D) * 8;
             float y[8], kt[8];
@@ -892,15 +912,6 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
             }
             store_split8(y_hi, y_lo, j, t0, C, y);
             store_split8(blk + TcBlock::kPK, blk + TcBlock::kPK + TcBlock::kPKLo, C + j, t0, C, kt);
-        }
-        for (int it = tid; it < C * (D / 8); it += kPrepTcThreads) {   // Q~ = diag(gamma) Q, rows t, 8 columns j
-            const int t = it % C, j0 = (it / C) * 8;
-            const float a = t < n ? eG[t] : 0.0f;
-            const float4 a4 = *reinterpret_cast<const float4 *>(q + t * LD + j0);
-            const float4 b4 = *reinterpret_cast<const float4 *>(q + t * LD + j0 + 4);
-            const float xq[8] = {__fmul_rn(a, a4.x), __fmul_rn(a, a4.y), __fmul_rn(a, a4.z), __fmul_rn(a, a4.w),
-                                 __fmul_rn(a, b4.x), __fmul_rn(a, b4.y), __fmul_rn(a, b4.z), __fmul_rn(a, b4.w)};
-            store_split8(blk + TcBlock::kWQ, blk + TcBlock::kWQ + TcBlock::kWQLo, C + t, j0, D, xq);
         }
         if (gi == 0) {   // MMA 1 done: [A; QK] in TMEM, region 2 free for M, P, T
             ok = tc::mbar_wait(&bar_mma, ph, kPrepWaitLimit) && ok;
@@ -1079,6 +1090,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
             }
         }
         if (tid == 0) *reinterpret_cast<float *>(blk + TcBlock::kMisc) = eG[n - 1];
+        if (tid < C) reinterpret_cast<float *>(blk + TcBlock::kGam)[tid] = eG[tid];   // gamma_t for O
         __syncthreads();   // the stages are read; the next head reuses regions 1 and 2
     }
     }   // items
@@ -1096,37 +1108,47 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
 // scan on the tensor cores (d = 128): one CTA of 256 threads per (value
 // head, sequence).  Threads i and i + 128 (warps w and w + 4) share TMEM lane
 // i, i.e. state row i, and split its columns.  TMEM (512 columns) holds
-//   0..127    [U^T | O^T] fp32 [128 x 64] each
-//   128..255  the state S fp32 [128 x 128], kept from chunk to chunk
-//   256..319  S0 hi, 320..383 S0 lo   (bf16 pairs: A operand of group 1)
-//   384..415  U^T hi, 416..447 U^T lo (bf16 pairs: A operand of group 2)
+//   0..127    [U^T | O1^T] fp32 [128 x 64] each
+//   128..319  [O2^T | S]: O2^T [128 x 64] and the state S fp32 [128 x 128],
+//             kept from chunk to chunk
+//   320..383  S0 hi, 384..447 S0 lo   (bf16 pairs: A operand of group 1)
+//   448..479  U^T hi, 480..511 U^T lo (bf16 pairs: A operand of group 2)
 // A operands in TMEM put row m in lane m and elements (m, 2c), (m, 2c + 1)
 // in the low and high half of column c.  Every product is three bf16 MMAs
 // (hi*hi + hi*lo + lo*hi) accumulating in fp32.  Per chunk:
-//   group 1: [U^T | O^T] = [U~^T | 0] + S0 [-W; Q~]^T   (N = 128, K = 128;
+//   group 1: [U^T | O1^T] = [U~^T | 0] + S0 [-W; Q]^T   (N = 128, K = 128;
 //            U~^T is stored into TMEM a chunk ahead, so U = U~ - S0 W^T
-//            leaves the tensor core finished)
+//            leaves the tensor core finished; Q is the key head's, shared
+//            by its value heads, so the decay gamma_t is applied after)
 //   U -> bf16 hi/lo A operand
-//   group 2: [O^T | S] += U^T [P; K~^T]^T         (N = 192, K = 64)
+//   group 2: [O2^T | S] += U^T [P; K~^T]^T        (N = 192, K = 64)
 //   S -> bf16 hi/lo A operand of the next chunk; S <- gamma_C' S
-//   O^T -> the workspace (fp32) for the norm pass
+//   O^T = diag(gamma) O1^T + O2^T -> the workspace (fp32) for the norm pass
 // With both A operands in TMEM a 128 x 128 x 16 step reads only its B tile
 // from shared memory.  The chunk operands are double-buffered in shared
-// memory: chunk c+1's two bulk copies (one per group; a bulk-copy issue costs
-// tens of cycles whatever its size) are issued by a thread of warp 1 when
-// chunk c starts, so the MMA-issuing thread never waits on them.
+// memory: chunk c+1's bulk copies (five for group 1 and gamma_t, one for
+// group 2; a bulk-copy issue costs tens of cycles whatever its size) are
+// issued by a thread of warp 1 when chunk c starts, so the MMA-issuing
+// thread never waits on them.
 // ---------------------------------------------------------------------------
 constexpr int kScanTcThreads = 256;   // two threads per TMEM lane, splitting the columns
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr size_t kScanTcSmem = 2 * (size_t)TcBlock::kOpBytes;
-constexpr uint32_t kTmemS = 128, kTmemShi = 256, kTmemSlo = 320, kTmemUhi = 384, kTmemUlo = 416;
+constexpr int kOpBuf = TcBlock::kOpBytes + 64 * 4;   // one chunk's operands, then its gamma_t
+constexpr size_t kScanTcSmem = 2 * (size_t)kOpBuf;
+constexpr uint32_t kTmemO2 = 128, kTmemS = 192, kTmemShi = 320, kTmemSlo = 384, kTmemUhi = 448, kTmemUlo = 480;
 
-// The chunk's [W; Q~] and [P; K~^T] operands into one buffer, each group
-// completing on its own barrier.
-__device__ __forceinline__ void issue_chunk_copies(unsigned char *ops, const unsigned char *blk, uint64_t *bar1,
-                                                   uint64_t *bar2) {
-    tc::mbar_expect_tx(bar1, TcBlock::kGroup1);
-    tc::bulk_g2s(ops, blk, TcBlock::kGroup1, bar1);
+// The chunk's [-W; Q] operand (-W from the head's block, Q from the key
+// head's lead block) and gamma_t, completing on bar1, and its [P; K~^T]
+// operand on bar2, into one buffer.
+__device__ __forceinline__ void issue_chunk_copies(unsigned char *ops, const unsigned char *blk,
+                                                   const unsigned char *lead, uint64_t *bar1, uint64_t *bar2) {
+    constexpr int H = TcBlock::kHalf, LO = TcBlock::kWQLo;
+    tc::mbar_expect_tx(bar1, TcBlock::kGroup1 + 64 * 4);
+    tc::bulk_g2s(ops, blk, H, bar1);                      // -W hi
+    tc::bulk_g2s(ops + H, lead + H, H, bar1);             // Q hi
+    tc::bulk_g2s(ops + LO, blk + LO, H, bar1);            // -W lo
+    tc::bulk_g2s(ops + LO + H, lead + LO + H, H, bar1);   // Q lo
+    tc::bulk_g2s(ops + TcBlock::kOpBytes, blk + TcBlock::kGam, 64 * 4, bar1);
     tc::mbar_expect_tx(bar2, TcBlock::kGroup2);
     tc::bulk_g2s(ops + TcBlock::kGroup1, blk + TcBlock::kGroup1, TcBlock::kGroup2, bar2);
 }
@@ -1155,8 +1177,8 @@ __device__ __forceinline__ void split_and_scale_state(uint32_t tmem_lane, int ha
     tc::tmem_wait_st();
 }
 
-// Seed the group-1 accumulator of this thread's lane: its half of the chunk's
-// U~^T row into the U columns, zeros into the O columns.
+// Seed the accumulators of this thread's lane: its half of the chunk's U~^T
+// row into the U columns, zeros into the O1 and O2 columns.
 template <int C>
 __device__ __forceinline__ void seed_group1(uint32_t tmem_lane, int half, const float4 (&ut)[C / 8]) {
 #pragma unroll
@@ -1171,6 +1193,7 @@ __device__ __forceinline__ void seed_group1(uint32_t tmem_lane, int half, const 
         for (int e = 0; e < 16; ++e) z[e] = 0.0f;
         tc::tmem_st16_nowait(tmem_lane + half * (C / 2) + q * 16, v);
         tc::tmem_st16_nowait(tmem_lane + 64 + half * (C / 2) + q * 16, z);
+        tc::tmem_st16_nowait(tmem_lane + kTmemO2 + half * (C / 2) + q * 16, z);
     }
     tc::tmem_wait_st();
 }
@@ -1215,6 +1238,7 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
     const size_t blk_stride = (size_t)p.Hv * TcBlock::kBytes;
     const unsigned char *blk0 = reinterpret_cast<const unsigned char *>(p.ws_chunks) +
                                 ((size_t)(base + c_first) * p.Hv + h) * TcBlock::kBytes;
+    const size_t lead_off = (size_t)(h % p.G) * TcBlock::kBytes;   // blk - lead: Q is in the key head's first block
 
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
@@ -1238,7 +1262,7 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
     constexpr uint32_t idN128 = tc::idesc_bf16(128, 128), idN192 = tc::idesc_bf16(128, 192);
 
     constexpr int kCopier = 32;   // lane 0 of warp 1 issues the bulk copies
-    if (tid == kCopier) issue_chunk_copies(tsm, blk0, &bar_g1[0], &bar_g2[0]);
+    if (tid == kCopier) issue_chunk_copies(tsm, blk0, blk0 - lead_off, &bar_g1[0], &bar_g2[0]);
     // the committed state row i into TMEM
     float *srow = p.state + ((size_t)sl * p.Hv + h) * D * D + (size_t)i * D;
 #pragma unroll 1
@@ -1283,7 +1307,7 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
 #pragma unroll 1
     for (int c = 0; c < n_run && ok; ++c) {   // c counts from c_first
         const unsigned char *blk = blk0 + (size_t)c * blk_stride;
-        unsigned char *ops = tsm + (c & 1) * TcBlock::kOpBytes;
+        unsigned char *ops = tsm + (c & 1) * kOpBuf;
         const uint32_t par = (c >> 1) & 1;   // fill count of this buffer, mod 2
         const bool more = c + 1 < n_run;
         const int start = lo + (c_first + c) * C;
@@ -1297,7 +1321,8 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
         }
         // the other buffer was last read by chunk c-1's MMAs, all complete
         if (tid == kCopier && more)
-            issue_chunk_copies(tsm + ((c + 1) & 1) * TcBlock::kOpBytes, blk + blk_stride, &bar_g1[(c + 1) & 1],
+            issue_chunk_copies(tsm + ((c + 1) & 1) * kOpBuf, blk + blk_stride, blk + blk_stride - lead_off,
+                               &bar_g1[(c + 1) & 1],
                                &bar_g2[(c + 1) & 1]);
         if (more) issued = c + 2;
 
@@ -1354,9 +1379,9 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
                 tc::mma_commit(&bar_s);
             } else {
                 const uint32_t b_hi = tc::smem_u32(ops + TcBlock::kPK), b_lo = b_hi + TcBlock::kPKLo;
-                tc::mma_bf16_ta<C>(tmem_base + 64, tmem_base + kTmemUhi, b_hi, idN192, true);
-                tc::mma_bf16_ta<C>(tmem_base + 64, tmem_base + kTmemUhi, b_lo, idN192, true);
-                tc::mma_bf16_ta<C>(tmem_base + 64, tmem_base + kTmemUlo, b_hi, idN192, true);
+                tc::mma_bf16_ta<C>(tmem_base + kTmemO2, tmem_base + kTmemUhi, b_hi, idN192, true);
+                tc::mma_bf16_ta<C>(tmem_base + kTmemO2, tmem_base + kTmemUhi, b_lo, idN192, true);
+                tc::mma_bf16_ta<C>(tmem_base + kTmemO2, tmem_base + kTmemUlo, b_hi, idN192, true);
                 tc::mma_commit(&bar_s);
             }
         }
@@ -1367,10 +1392,22 @@ __global__ void __launch_bounds__(kScanTcThreads, 1) gdn_prefill_scan_tc_kernel(
             split_and_scale_state(tl, half, gC);   // the next chunk's S operand
         }
 
-        // O^T row i out of TMEM (stored to O[t][i] during the next chunk's group 1)
+        // O^T row i = gamma_t O1^T + O2^T out of TMEM (stored to O[t][i] during
+        // the next chunk's group 1); gamma_t came with this chunk's group-1 copies
+        {
+            const float *gam = reinterpret_cast<const float *>(ops + TcBlock::kOpBytes) + half * (C / 2);
 #pragma unroll
-        for (int q = 0; q < C / 32; ++q) tc::tmem_ld16_nowait(tl + 64 + half * (C / 2) + q * 16, o_r[q]);
-        tc::tmem_wait_ld();
+            for (int q = 0; q < C / 32; ++q) {
+                uint32_t o2[16];
+                tc::tmem_ld16_nowait(tl + 64 + half * (C / 2) + q * 16, o_r[q]);
+                tc::tmem_ld16_nowait(tl + kTmemO2 + half * (C / 2) + q * 16, o2);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    o_r[q][e] = __float_as_uint(
+                        __fmaf_rn(gam[q * 16 + e], __uint_as_float(o_r[q][e]), __uint_as_float(o2[e])));
+            }
+        }
         o_start = start;
         o_n = n;
         if (more && !fail) seed_group1<C>(tl, half, ut);   // after this lane's U and O columns are read
