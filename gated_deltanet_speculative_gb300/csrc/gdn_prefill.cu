@@ -19,10 +19,14 @@ namespace {
 // next scan.  Only the last group's scan and norm cannot overlap any prep,
 // so with several sequences, after an optional first group of kGroupFirst
 // chunks, the groups shrink: each takes kGroupShare of the chunks left (at
-// least kGroupMin).  One sequence uses round_groups below.  How much of the
+// least kGroupMin).  A large share measured best there: a group's scan runs
+// one chain per sequence it touches, so the scans of mixed groups take many
+// SMs and starve a concurrent prep, and most of the prep is better done on
+// all SMs first (512/1024/2048/4096 tokens: share 0.35 -> 0.817 ms, 0.75 ->
+// 0.754 ms, one group 0.814 ms).  One sequence uses round_groups below.  How much of the
 // GPU a prep may take while a scan runs is set in the launch loop.
 constexpr int kGroupFirst = 0;
-constexpr double kGroupShare = 0.35;
+constexpr double kGroupShare = 0.75;
 constexpr int kGroupMin = 4;
 constexpr int kMaxGroups = 64;
 

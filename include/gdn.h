@@ -215,7 +215,7 @@ int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot
  * to `stream` by events, so they overlap the prep of later groups.  With
  * one sequence the groups are sized in whole prep rounds of the SMs and
  * every prep after the first leaves the scan's SMs free; with several they
- * shrink toward the end (about 35% of the chunks left each, at least 4).
+ * shrink toward the end (about 75% of the chunks left each, at least 4).
  * The side streams are shared: calls made from several host threads at
  * once are serialised on them.  The fork and join are ordinary event
  * record / wait calls, so the call can be captured in a CUDA graph.
