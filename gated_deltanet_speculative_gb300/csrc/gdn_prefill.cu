@@ -17,15 +17,14 @@ namespace {
 // fewer than the SMs) overlaps the prep of the groups after it; the norm of
 // group g runs on a third stream after that scan, so it never holds up the
 // next scan.  Only the last group's scan and norm cannot overlap any prep,
-// so with several sequences, after an optional first group of kGroupFirst
-// chunks, the groups shrink: each takes kGroupShare of the chunks left (at
-// least kGroupMin).  A large share measured best there: a group's scan runs
-// one chain per sequence it touches, so the scans of mixed groups take many
-// SMs and starve a concurrent prep, and most of the prep is better done on
-// all SMs first (512/1024/2048/4096 tokens: share 0.35 -> 0.817 ms, 0.75 ->
-// 0.754 ms, one group 0.814 ms).  One sequence uses round_groups below.  How much of the
-// GPU a prep may take while a scan runs is set in the launch loop.
-constexpr int kGroupFirst = 0;
+// so with several sequences the groups shrink: each takes kGroupShare of the
+// chunks left (at least kGroupMin).  A large share measured best there: a
+// group's scan runs one chain per sequence it touches, so the scans of mixed
+// groups take many SMs and starve a concurrent prep, and most of the prep is
+// better done on all SMs first (512/1024/2048/4096 tokens: share 0.35 ->
+// 0.817 ms, 0.75 -> 0.754 ms, one group 0.814 ms).  One sequence uses
+// round_groups below.  How much of the GPU a prep may take while a scan runs
+// is set in the launch loop.
 constexpr double kGroupShare = 0.75;
 constexpr int kGroupMin = 4;
 constexpr int kMaxGroups = 64;
@@ -34,10 +33,6 @@ constexpr int kMaxGroups = 64;
 int chunk_groups(int chunks, int (&b)[kMaxGroups + 1]) {
     int n = 0, at = 0;
     b[0] = 0;
-    if (kGroupFirst > 0 && chunks > kGroupFirst + kGroupMin) {
-        at = kGroupFirst;
-        b[++n] = at;
-    }
     while (at < chunks && n < kMaxGroups) {
         const int left = chunks - at;
         int take = (int)(left * kGroupShare + 0.999);
@@ -152,13 +147,9 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
         const int groups = !pipelined ? 1
                            : hold_one ? round_groups(p.max_chunks, n_sm, p.Hk, p.Hv, bounds)
                                       : chunk_groups(p.max_chunks, bounds);
-        auto prep_grid = [&](int reserve) {
+        if (groups <= 1) {   // one launch each; the prep grid takes at most one CTA per SM
             const int items = (p.c_hi - p.c_lo) * p.Hk;
-            const int ctas = n_sm - reserve > 1 ? n_sm - reserve : 1;
-            return items < ctas ? items : ctas;
-        };
-        if (groups <= 1) {
-            gdn_prefill_prep_tc_kernel<C><<<prep_grid(0), kPrepTcThreads, kPrepTcSmem, st>>>(p);
+            gdn_prefill_prep_tc_kernel<C><<<items < n_sm ? items : n_sm, kPrepTcThreads, kPrepTcSmem, st>>>(p);
             gdn_prefill_scan_tc_kernel<C><<<dim3(p.Hv, p.n_seqs), kScanTcThreads, kScanTcSmem, st>>>(p);
             gdn_prefill_norm_kernel<D><<<norm_blocks, kNormThreads, 0, st>>>(p);
             return cudaGetLastError();
