@@ -50,6 +50,16 @@ def test_prefill_ragged_prompts_resume_from_kept_state(g):
     compare(c, run_prefill(c))
 
 
+@pytest.mark.parametrize("hk,hv", [(4, 4), (2, 4), (2, 8), (1, 8)])
+def test_prefill_value_heads_per_key_head(hk, hv):
+    """d = 128 with 1, 2, 4 and 8 value heads per key head: the prep writes a
+    key head's Q once, into the block of its first value head, and every
+    value head's scan reads it from there (the rest of the workspace is NaN
+    poison)."""
+    c = Case(synth.Geometry(hk, hv, 128, 128), [1, 64, 65, 200], seed=59, n_slots=5)
+    compare(c, run_prefill(c))
+
+
 def test_prefill_27b_heads_zero_state():
     c = Case(synth.LIKE_27B, [200, 70, 1], seed=53, zero_state=True)
     compare(c, run_prefill(c))
