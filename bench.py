@@ -449,6 +449,7 @@ def run_extra(dev, stream, flush, reps=20, only=None):
         out["tree_round_16x16"] = _extra_tree(dev, stream, flush, reps, hbm)
     if only in (None, "replay"):
         out["logged_round_replay_commit_16x16"] = _extra_logged_round(dev, stream, flush, reps, hbm)
+        out["logged_tree_replay_commit_16x16"] = _extra_logged_tree(dev, stream, flush, reps, hbm)
     if only in (None, "decode"):
         out["decode_24_layers_2b_like"] = _extra_decode(dev, stream, flush, reps, hbm)
     if only in (None, "prefill"):
@@ -504,6 +505,69 @@ def _extra_logged_round(dev, stream, flush, reps, hbm):
     return {"ms_per_round": ms, "rows_per_s": R / (ms * 1e-3), "window_log_ms": ms_w,
             "algorithmic_gbs": b / (ms * 1e-3) / 1e9, "frac_hbm": b / (ms * 1e-3) / 1e9 / hbm,
             "algorithmic_bytes": b}
+
+
+def _tree_round_inputs(dev):
+    """The tree round's inputs: 16 streams x 16-node random trees, one random
+    leaf per stream kept."""
+    import torch
+    import gated_deltanet_speculative_gb300 as gdn
+    g = GEOM
+    R = N_STREAMS * WINDOW
+    w = synth.layer_weights(g, 3)
+    cache = synth.slot_cache(g, N_STREAMS, 3)
+    rows = synth.row_inputs(g, R, 3)
+    rng = np.random.default_rng([3, 9])
+    parent = np.concatenate([synth.random_tree(WINDOW, rng) for _ in range(N_STREAMS)]).astype(np.int32)
+    keep = np.array([s * WINDOW + synth.random_leaf(parent[s * WINDOW:(s + 1) * WINDOW], rng)
+                     for s in range(N_STREAMS)], np.int32)
+    d = gdn.Dims(g.n_k_heads, g.n_v_heads, g.d_k, g.d_v)
+    dw = {"conv_w": _bf(w["conv_w"]).to(dev), "A_log": torch.from_numpy(w["A_log"]).to(dev),
+          "dt_bias": torch.from_numpy(w["dt_bias"]).to(dev), "norm_w": _bf(w["norm_w"]).to(dev)}
+    dc = {"state": torch.from_numpy(cache["state"]).to(dev), "tail": _bf(cache["tail"]).to(dev)}
+    dr = {k: _bf(rows[k]).to(dev) for k in ("mixed", "z", "a", "b")}
+    dr["y"] = torch.empty((R, g.n_v_heads, g.d_v), dtype=torch.bfloat16, device=dev)
+    return {"d": d, "dw": dw, "dc": dc, "dr": dr, "keep": keep,
+            "slot": torch.arange(N_STREAMS, dtype=torch.int32, device=dev),
+            "rp": torch.from_numpy(synth.row_ptr([WINDOW] * N_STREAMS)).to(dev),
+            "par": torch.from_numpy(parent).to(dev), "keep_t": torch.from_numpy(keep).to(dev)}
+
+
+def _extra_logged_tree(dev, stream, flush, reps, hbm):
+    """The tree round with logged nodes and a replay commit of one random
+    leaf per stream, beside the recorded tree plus a copy commit."""
+    import torch
+    import gated_deltanet_speculative_gb300 as gdn
+    g = GEOM
+    R = N_STREAMS * WINDOW
+    t = _tree_round_inputs(dev)
+    d, dw, dc, dr = t["d"], t["dw"], t["dc"], t["dr"]
+    la = torch.empty((R, g.n_v_heads), dtype=torch.float32, device=dev)
+    lu = torch.empty((R, g.n_v_heads, g.d_v), dtype=torch.float32, device=dev)
+    lk = torch.empty((R, g.n_k_heads, g.d_k), dtype=torch.float32, device=dev)
+    rt = torch.empty((R, 3, g.channels), dtype=torch.bfloat16, device=dev)
+    rs = torch.empty((R, g.n_v_heads, g.d_v, g.d_k), dtype=torch.float32, device=dev)
+
+    def logged():
+        gdn.tree_log(d, dw, dc, t["slot"], t["rp"], t["par"], dr, la, lu, lk, rt, stream)
+        gdn.commit_replay_tree(d, dc, t["slot"], t["rp"], t["par"], t["keep_t"], la, lu, lk, rt, stream)
+
+    def recorded():
+        gdn.tree(d, dw, dc, t["slot"], t["rp"], t["par"], dr, rs, rt, stream)
+        gdn.commit(d, dc, t["slot"], t["keep_t"], rs, rt, stream)
+
+    ms = _timed(logged, reps, stream, flush)
+    ms_w = _timed(lambda: gdn.tree_log(d, dw, dc, t["slot"], t["rp"], t["par"], dr, la, lu, lk, rt, stream), reps,
+                  stream, flush)
+    ms_rec = _timed(recorded, reps, stream, flush)
+    del rs
+    b = logged_round_bytes(g, N_STREAMS, R, N_STREAMS)
+    return {"ms_per_round": ms, "rows_per_s": R / (ms * 1e-3), "tree_log_ms": ms_w,
+            "algorithmic_gbs": b / (ms * 1e-3) / 1e9, "frac_hbm": b / (ms * 1e-3) / 1e9 / hbm,
+            "algorithmic_bytes": b,
+            "recorded_tree_and_commit_ms": ms_rec, "recorded_rows_per_s": R / (ms_rec * 1e-3),
+            "note": "parent states rebuilt from the slot (an L2 re-read plus a replay of the logged path) "
+                    "are not counted"}
 
 
 def _extra_tree(dev, stream, flush, reps, hbm):

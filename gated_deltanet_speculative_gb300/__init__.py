@@ -2,13 +2,13 @@
 
 The C ABI of include/gdn.h (libgdn.so, hand-written sm_103a kernels) behind a
 thin ctypes binding: ``step``, ``window``, ``tree``, ``commit``,
-``window_log``, ``commit_replay``, ``prefill``, ``prefill_noalloc`` and
-``get_device_error`` take torch CUDA tensors and enqueue on the current
+``window_log``, ``commit_replay``, ``tree_log``, ``commit_replay_tree``,
+``prefill``, ``prefill_noalloc`` and ``get_device_error`` take torch CUDA tensors and enqueue on the current
 stream.  ``synth`` draws the seeded synthetic inputs.  Importing the package
 does not load the CUDA library; the first call does (and raises if it is
 missing).
 """
 from . import synth  # noqa: F401
 from ._binding import (Dims, GdnError, MAX_WINDOW, PREFILL_CHUNK, PREFILL_NOALLOC_SCRATCH_BYTES,  # noqa: F401
-                       commit, commit_replay, get_device_error, library_path, load, prefill, prefill_noalloc,
-                       prefill_workspace_size, step, tree, window, window_log)
+                       commit, commit_replay, commit_replay_tree, get_device_error, library_path, load, prefill,
+                       prefill_noalloc, prefill_workspace_size, step, tree, tree_log, window, window_log)

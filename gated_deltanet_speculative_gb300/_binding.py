@@ -68,6 +68,10 @@ _SIGS = {
     "gdn_window_log": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _I, _I,
                        ctypes.POINTER(c_rows), _P, _P, _P, _P, _P],
     "gdn_commit_replay": [ctypes.POINTER(c_dims), ctypes.POINTER(c_cache), _P, _P, _P, _I, _I, _P, _P, _P, _P, _P],
+    "gdn_tree_log": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _P, _I, _I,
+                     ctypes.POINTER(c_rows), _P, _P, _P, _P, _P],
+    "gdn_commit_replay_tree": [ctypes.POINTER(c_dims), ctypes.POINTER(c_cache), _P, _P, _P, _P, _I, _I, _P, _P, _P,
+                               _P, _P],
     "gdn_status_string": [ctypes.c_int],
     "gdn_get_device_error": [_P, ctypes.POINTER(ctypes.c_int32)],
 }
@@ -256,6 +260,46 @@ def commit_replay(dims: Dims, cache: dict, slot, row_ptr, keep_row, log_a, log_u
     _check("gdn_commit_replay", lib.gdn_commit_replay(ctypes.byref(dims.c()), ctypes.byref(cc), _ptr(slot),
                                                       _ptr(row_ptr), _ptr(keep_row), S, R, _ptr(log_a), _ptr(log_u),
                                                       _ptr(log_k), _ptr(rec_tail), _stream_ptr(stream)))
+
+
+def tree_log(dims: Dims, weights: dict, cache: dict, slot, row_ptr, parent, rows: dict, log_a, log_u, log_k,
+             rec_tail, stream=None):
+    """Tree verify windows logging each node's decay, write and key."""
+    lib = load()
+    _need(slot, "slot", torch.int32)
+    S = slot.numel()
+    R = rows["mixed"].shape[0]
+    _need(row_ptr, "row_ptr", torch.int32, (S + 1,))
+    _need(parent, "parent", torch.int32, (R,))
+    cw, cc, cr = _weights(dims, weights), _cache(dims, cache), _rows(dims, rows, R)
+    _need(log_a, "log_a", torch.float32, (R, dims.n_v_heads))
+    _need(log_u, "log_u", torch.float32, (R, dims.n_v_heads, dims.d_v))
+    _need(log_k, "log_k", torch.float32, (R, dims.n_k_heads, dims.d_k))
+    _need(rec_tail, "rec_tail", torch.bfloat16, (R, 3, dims.channels))
+    _check("gdn_tree_log", lib.gdn_tree_log(ctypes.byref(dims.c()), ctypes.byref(cw), ctypes.byref(cc), _ptr(slot),
+                                            _ptr(row_ptr), _ptr(parent), S, R, ctypes.byref(cr), _ptr(log_a),
+                                            _ptr(log_u), _ptr(log_k), _ptr(rec_tail), _stream_ptr(stream)))
+
+
+def commit_replay_tree(dims: Dims, cache: dict, slot, row_ptr, parent, keep_row, log_a, log_u, log_k, rec_tail,
+                       stream=None):
+    """Commit by replaying the logged root-to-node path of keep_row[s] (-1: untouched)."""
+    lib = load()
+    _need(slot, "slot", torch.int32)
+    S = slot.numel()
+    _need(row_ptr, "row_ptr", torch.int32, (S + 1,))
+    _need(keep_row, "keep_row", torch.int32, (S,))
+    cc = _cache(dims, cache)
+    R = log_a.shape[0]
+    _need(parent, "parent", torch.int32, (R,))
+    _need(log_a, "log_a", torch.float32, (R, dims.n_v_heads))
+    _need(log_u, "log_u", torch.float32, (R, dims.n_v_heads, dims.d_v))
+    _need(log_k, "log_k", torch.float32, (R, dims.n_k_heads, dims.d_k))
+    _need(rec_tail, "rec_tail", torch.bfloat16, (R, 3, dims.channels))
+    _check("gdn_commit_replay_tree",
+           lib.gdn_commit_replay_tree(ctypes.byref(dims.c()), ctypes.byref(cc), _ptr(slot), _ptr(row_ptr),
+                                      _ptr(parent), _ptr(keep_row), S, R, _ptr(log_a), _ptr(log_u), _ptr(log_k),
+                                      _ptr(rec_tail), _stream_ptr(stream)))
 
 
 PREFILL_CHUNK = 64

@@ -126,13 +126,13 @@ int rows_entry(int mode, const gdn_dims *dims, const gdn_weights *w, const gdn_c
     if (n_streams <= 0 || n_streams > 65535) return GDN_EINVAL;
     if (mode != gdn::kStep) {
         if (!row_ptr || !rec_tail) return GDN_ENULL;
-        if (mode == gdn::kWindowLog) {
+        if (mode == gdn::kWindowLog || mode == gdn::kTreeLog) {
             if (!logs.a || !logs.u || !logs.k) return GDN_ENULL;
             if (!aligned(logs.a, 4) || !aligned(logs.u, 16) || !aligned(logs.k, 16)) return GDN_EALIGN;
         } else if (!rec_state) {
             return GDN_ENULL;
         }
-        if (mode == gdn::kTree && !parent) return GDN_ENULL;
+        if ((mode == gdn::kTree || mode == gdn::kTreeLog) && !parent) return GDN_ENULL;
         if (n_rows <= 0) return GDN_EINVAL;
         if ((rec_state && !aligned(rec_state, 16)) || !aligned(rec_tail, 16)) return GDN_EALIGN;
     }
@@ -151,6 +151,56 @@ int rows_entry(int mode, const gdn_dims *dims, const gdn_weights *w, const gdn_c
     p.log_k = logs.k;
     return launch_rows(dims->d_k, mode, p, n_streams, stream);
 }
+
+// Replay commit of chains (parent == nullptr) or trees.
+int replay_entry(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot, const int32_t *row_ptr,
+                 const int32_t *parent, const int32_t *keep_row, int32_t n_streams, int32_t n_rows,
+                 const float *log_a, const float *log_u, const float *log_k, const void *rec_tail, void *stream) {
+    GDN_TRY(check_dims(dims));
+    GDN_TRY(check_cache(cache));
+    if (!slot || !row_ptr || !keep_row || !log_a || !log_u || !log_k || !rec_tail) return GDN_ENULL;
+    if (n_streams <= 0 || n_streams > 65535 || n_rows <= 0) return GDN_EINVAL;
+    if (!aligned(slot, 4) || !aligned(row_ptr, 4) || !aligned(keep_row, 4) || !aligned(log_a, 4) ||
+        !aligned(log_u, 16) || !aligned(log_k, 16) || !aligned(rec_tail, 16) || (parent && !aligned(parent, 4)))
+        return GDN_EALIGN;
+    int *err = error_word();
+    if (!err) return GDN_ECUDA;
+    gdn::ReplayParams p = {};
+    p.Hk = dims->n_k_heads;
+    p.Hv = dims->n_v_heads;
+    p.G = dims->n_v_heads / dims->n_k_heads;
+    p.CH = 2 * dims->n_k_heads * dims->d_k + dims->n_v_heads * dims->d_v;
+    p.state = cache->state;
+    p.tail = static_cast<uint16_t *>(cache->tail);
+    p.n_slots = cache->n_slots;
+    p.slot = slot;
+    p.row_ptr = row_ptr;
+    p.parent = parent;
+    p.keep_row = keep_row;
+    p.n_rows = n_rows;
+    p.log_a = log_a;
+    p.log_u = log_u;
+    p.log_k = log_k;
+    p.rec_tail = static_cast<const uint16_t *>(rec_tail);
+    p.err = err;
+    const dim3 grid(p.Hv, n_streams);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (parent) {
+        switch (dims->d_k) {
+            case 32: gdn::gdn_commit_replay_kernel<32, true><<<grid, gdn::kReplayThreads, 0, st>>>(p); break;
+            case 64: gdn::gdn_commit_replay_kernel<64, true><<<grid, gdn::kReplayThreads, 0, st>>>(p); break;
+            default: gdn::gdn_commit_replay_kernel<128, true><<<grid, gdn::kReplayThreads, 0, st>>>(p); break;
+        }
+    } else {
+        switch (dims->d_k) {
+            case 32: gdn::gdn_commit_replay_kernel<32><<<grid, gdn::kReplayThreads, 0, st>>>(p); break;
+            case 64: gdn::gdn_commit_replay_kernel<64><<<grid, gdn::kReplayThreads, 0, st>>>(p); break;
+            default: gdn::gdn_commit_replay_kernel<128><<<grid, gdn::kReplayThreads, 0, st>>>(p); break;
+        }
+    }
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ECUDA;
+}
+
 
 }  // namespace
 
@@ -290,40 +340,28 @@ int gdn_window_log(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *
 int gdn_commit_replay(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot, const int32_t *row_ptr,
                       const int32_t *keep_row, int32_t n_streams, int32_t n_rows, const float *log_a,
                       const float *log_u, const float *log_k, const void *rec_tail, void *stream) {
-    GDN_TRY(check_dims(dims));
-    GDN_TRY(check_cache(cache));
-    if (!slot || !row_ptr || !keep_row || !log_a || !log_u || !log_k || !rec_tail) return GDN_ENULL;
-    if (n_streams <= 0 || n_streams > 65535 || n_rows <= 0) return GDN_EINVAL;
-    if (!aligned(slot, 4) || !aligned(row_ptr, 4) || !aligned(keep_row, 4) || !aligned(log_a, 4) ||
-        !aligned(log_u, 16) || !aligned(log_k, 16) || !aligned(rec_tail, 16))
-        return GDN_EALIGN;
-    int *err = error_word();
-    if (!err) return GDN_ECUDA;
-    gdn::ReplayParams p = {};
-    p.Hk = dims->n_k_heads;
-    p.Hv = dims->n_v_heads;
-    p.G = dims->n_v_heads / dims->n_k_heads;
-    p.CH = 2 * dims->n_k_heads * dims->d_k + dims->n_v_heads * dims->d_v;
-    p.state = cache->state;
-    p.tail = static_cast<uint16_t *>(cache->tail);
-    p.n_slots = cache->n_slots;
-    p.slot = slot;
-    p.row_ptr = row_ptr;
-    p.keep_row = keep_row;
-    p.n_rows = n_rows;
-    p.log_a = log_a;
-    p.log_u = log_u;
-    p.log_k = log_k;
-    p.rec_tail = static_cast<const uint16_t *>(rec_tail);
-    p.err = err;
-    const dim3 grid(p.Hv, n_streams);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    switch (dims->d_k) {
-        case 32: gdn::gdn_commit_replay_kernel<32><<<grid, gdn::kReplayThreads, 0, st>>>(p); break;
-        case 64: gdn::gdn_commit_replay_kernel<64><<<grid, gdn::kReplayThreads, 0, st>>>(p); break;
-        default: gdn::gdn_commit_replay_kernel<128><<<grid, gdn::kReplayThreads, 0, st>>>(p); break;
-    }
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ECUDA;
+    return replay_entry(dims, cache, slot, row_ptr, nullptr, keep_row, n_streams, n_rows, log_a, log_u, log_k,
+                        rec_tail, stream);
+}
+
+int gdn_tree_log(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
+                 const int32_t *row_ptr, const int32_t *parent, int32_t n_streams, int32_t n_rows,
+                 const gdn_rows *rows, float *log_a, float *log_u, float *log_k, void *rec_tail, void *stream) {
+    LogBuffers logs;
+    logs.a = log_a;
+    logs.u = log_u;
+    logs.k = log_k;
+    return rows_entry(gdn::kTreeLog, dims, w, cache, slot, row_ptr, parent, n_streams, n_rows, rows, nullptr,
+                      rec_tail, stream, logs);
+}
+
+int gdn_commit_replay_tree(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot,
+                           const int32_t *row_ptr, const int32_t *parent, const int32_t *keep_row,
+                           int32_t n_streams, int32_t n_rows, const float *log_a, const float *log_u,
+                           const float *log_k, const void *rec_tail, void *stream) {
+    if (!parent) return GDN_ENULL;
+    return replay_entry(dims, cache, slot, row_ptr, parent, keep_row, n_streams, n_rows, log_a, log_u, log_k,
+                        rec_tail, stream);
 }
 
 const char *gdn_status_string(int status) {

@@ -65,13 +65,15 @@ __global__ void __launch_bounds__(kCommitThreads) gdn_commit_kernel(const Commit
     for (size_t i = lo + threadIdx.x; i < hi; i += kCommitThreads) tdst[i] = __ldcs(tsrc + i);
 }
 
-// Replay commit: slot[s] <- the committed state advanced along rows
-// row_ptr[s] .. keep_row[s] of the stream's logged chain window, one rank-1
-// update per row,  S <- u k^T + a S  with the same rounding as the window
-// (fma(u_i, k_j, a * S_ij)), so the result equals the state the window would
-// have recorded for the kept row, bit for bit.  The conv tail is the kept
-// row's recorded tail.  (TensorFold #932, tree note: the commit re-applies
-// the accepted rows' logs to the committed state in a single pass.)
+// Replay commit: slot[s] <- the committed state advanced along the kept path
+// of the stream's logged window, one rank-1 update per row,  S <- u k^T + a S
+// with the same rounding as the window (fma(u_i, k_j, a * S_ij)), so the
+// result equals the state the window would have recorded for the kept row,
+// bit for bit.  The path of a chain is rows row_ptr[s] .. keep_row[s]; that
+// of a tree (TREE) the kept node's root-to-node path through the parent
+// indices, root first.  The conv tail is the kept row's recorded tail.
+// (TensorFold #932, tree note: the commit re-applies the accepted rows' logs
+// to the committed state in a single pass, trees included.)
 struct ReplayParams {
     int Hk, Hv, G, CH;
     float *state;
@@ -79,6 +81,7 @@ struct ReplayParams {
     int n_slots;
     const int *slot;
     const int *row_ptr;
+    const int *parent;        // [R] window-local parents (trees only)
     const int *keep_row;
     int n_rows;
     const float *log_a;       // [R, Hv]
@@ -90,12 +93,14 @@ struct ReplayParams {
 
 constexpr int kReplayThreads = 256;
 
-template <int D>
+template <int D, bool TREE = false>
 __global__ void __launch_bounds__(kReplayThreads) gdn_commit_replay_kernel(const ReplayParams p) {
     constexpr int RPW = D / 8, CPL = D / 32;
     __shared__ __align__(16) float us[GDN_MAX_WINDOW][D];
     __shared__ __align__(16) float ks[GDN_MAX_WINDOW][D];
     __shared__ float as[GDN_MAX_WINDOW];
+    __shared__ int path[TREE ? GDN_MAX_WINDOW : 1];   // trees: window-local rows of the kept path, root first
+    __shared__ int path_len;
     const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kr = __ldg(p.keep_row + s);
     if (kr == -1) return;   // nothing accepted: the slot keeps its bits
@@ -106,13 +111,47 @@ __global__ void __launch_bounds__(kReplayThreads) gdn_commit_replay_kernel(const
         if (h == 0 && tid == 0) raise_error(p.err, bad_slot ? GDN_DERR_SLOT : GDN_DERR_KEEP);
         return;
     }
-    const int n = kr - r0 + 1, kh = h / p.G;
+    int n = kr - r0 + 1;
+    if constexpr (TREE) {
+        // the kept node's ancestors: parents lie below their children, so
+        // the walk ends within kr - r0 + 1 steps; the path's rows in
+        // ascending order are its rows from the root down
+        __shared__ int par[GDN_MAX_WINDOW];
+        if (tid < n) par[tid] = __ldg(p.parent + r0 + tid);
+        __syncthreads();
+        if (tid == 0) {
+            unsigned mask = 0;
+            int m = n - 1, ok = 1;
+            while (m >= 0) {
+                mask |= 1u << m;
+                const int pm = par[m];
+                if (pm < -1 || pm >= m) {
+                    ok = 0;
+                    break;
+                }
+                m = pm;
+            }
+            int len = 0;
+            for (int i = 0; i < n; ++i)
+                if ((mask >> i) & 1u) path[len++] = i;
+            path_len = ok ? len : -1;
+        }
+        __syncthreads();
+        n = path_len;
+        if (n < 0) {
+            if (h == 0 && tid == 0) raise_error(p.err, GDN_DERR_PARENT);
+            return;
+        }
+    }
+    const int kh = h / p.G;
+    auto row_of = [&](int t) { return TREE ? r0 + path[t] : r0 + t; };   // packed row of path step t
     for (int i = tid; i < n * D / 4; i += kReplayThreads) {   // the path's logs into shared memory
         const int t = i / (D / 4), c4 = (i - t * (D / 4)) * 4;
-        cp_async16(&us[t][c4], p.log_u + ((size_t)(r0 + t) * p.Hv + h) * D + c4);
-        cp_async16(&ks[t][c4], p.log_k + ((size_t)(r0 + t) * p.Hk + kh) * D + c4);
+        const size_t r = (size_t)row_of(t);
+        cp_async16(&us[t][c4], p.log_u + (r * p.Hv + h) * D + c4);
+        cp_async16(&ks[t][c4], p.log_k + (r * p.Hk + kh) * D + c4);
     }
-    if (tid < n) as[tid] = __ldg(p.log_a + (size_t)(r0 + tid) * p.Hv + h);
+    if (tid < n) as[tid] = __ldg(p.log_a + (size_t)row_of(tid) * p.Hv + h);
     float S[RPW][CPL];
     float *tile = p.state + ((size_t)sl * p.Hv + h) * D * D;
 #pragma unroll

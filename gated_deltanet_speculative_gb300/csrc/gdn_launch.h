@@ -65,6 +65,7 @@ cudaError_t launch_rows(int mode, const RowParams &p, int n_streams, cudaStream_
     }
     if (mode == kWindow) gdn_rows_kernel<D, kWindow><<<grid, block, 0, st>>>(p);
     else if (mode == kWindowLog) gdn_rows_kernel<D, kWindowLog><<<grid, block, 0, st>>>(p);
+    else if (mode == kTreeLog) gdn_rows_kernel<D, kTreeLog><<<grid, block, 0, st>>>(p);
     else gdn_rows_kernel<D, kTree><<<grid, block, 0, st>>>(p);
     return cudaGetLastError();
 }

@@ -32,11 +32,15 @@
 
 namespace gdn {
 
-// kWindowLog: a chain window that logs each row's decay, write u and key
-// instead of recording its state (TensorFold #932, tree note: per-row logs
-// of the decay, the write vector and the key replace the recorded states,
-// and the commit replays them).
-enum RowMode : int { kStep = 0, kWindow = 1, kTree = 2, kWindowLog = 3 };
+// kWindowLog / kTreeLog: a chain or tree window that logs each row's decay,
+// write u and key instead of recording its state (TensorFold #932, tree
+// note: per-row logs of the decay, the write vector and the key replace the
+// recorded states, and the commit replays them).  A logged tree node whose
+// parent is not the node visited just before it rebuilds the parent's state
+// from the committed slot by re-applying the logged rows of the path down to
+// the parent, with the forward pass's own rounding, so it continues from
+// the same bits the recorded tree would have re-read.
+enum RowMode : int { kStep = 0, kWindow = 1, kTree = 2, kWindowLog = 3, kTreeLog = 4 };
 
 struct RowParams {
     int Hk, Hv, G, CH;
@@ -59,9 +63,9 @@ struct RowParams {
     int n_rows;
     float *rec_state;         // [R, Hv, D, D]
     uint16_t *rec_tail;       // bf16 [R, 3, CH]
-    float *log_a;             // [R, Hv] decay (kWindowLog)
-    float *log_u;             // [R, Hv, D] write u = b (v - a S k) (kWindowLog)
-    float *log_k;             // [R, Hk, D] normalised key (kWindowLog)
+    float *log_a;             // [R, Hv] decay (logged modes)
+    float *log_u;             // [R, Hv, D] write u = b (v - a S k) (logged modes)
+    float *log_k;             // [R, Hk, D] normalised key (logged modes)
     int *err;                 // device error word
 };
 
@@ -176,9 +180,15 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
     constexpr int SEG = D * 2 / 16;               // 16-byte chunks in one q, k or v segment
     constexpr int CHUNKS = 3 * SEG;               // 16-byte chunks in a staged row
     static_assert(NV >= 2 && NV <= 32, "unsupported head width");
+    constexpr bool TREE = MODE == kTree || MODE == kTreeLog;
+    constexpr bool LOG = MODE == kWindowLog || MODE == kTreeLog;
 
     __shared__ RowSmem<D> sm;
     __shared__ float o_all[P > 1 ? D : 1];        // the whole o vector, gathered from the slices
+    // logged trees: every row's write u (to rebuild a parent's state) and,
+    // per node, the set of rows on its root-to-node path (bit m = row m)
+    __shared__ float u_rows[MODE == kTreeLog ? kMaxRows : 1][MODE == kTreeLog ? D : 1];
+    __shared__ int path_mask[MODE == kTreeLog ? kMaxRows : 1];
     const int h = blockIdx.x / P, s = blockIdx.y;
     const int sli = blockIdx.x % P;               // row slice: state rows [row0, row0 + D/P)
     const int row0 = sli * (D / P);
@@ -234,7 +244,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         const int t = i / SEG, ch = i - t * SEG;
         cp_async16(&sm.z[t][ch * 8], p.z + ((size_t)(r0 + t) * p.Hv + h) * D + ch * 8);
     }
-    if (MODE == kTree && tid < n) sm.parent[tid] = __ldg(p.parent + r0 + tid);
+    if (TREE && tid < n) sm.parent[tid] = __ldg(p.parent + r0 + tid);
     // ---- a4: gates
     if (tid < n) {
         const size_t gi = (size_t)(r0 + tid) * p.Hv + h;
@@ -251,7 +261,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
     if (tid == 0) {
         int bad = 0;
         for (int t = 0; t < n; ++t) {
-            const int par = MODE == kTree ? sm.parent[t] : t - 1;
+            const int par = TREE ? sm.parent[t] : t - 1;
             if (par < -1 || par >= t) bad = GDN_DERR_PARENT;
             sm.parent[t] = par;
             sm.reused[t] = 0;
@@ -274,7 +284,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         // without a stack: subtree sizes bottom-up (parents precede
         // children), then each node takes its parent's next free slot.
         for (int t = 0; t < n; ++t) sm.order[t] = t;
-        if (MODE == kTree && !bad) {
+        if (TREE && !bad) {
             for (int t = 0; t < n; ++t) sm.nsub[t] = 1;
             for (int t = n - 1; t > 0; --t)
                 if (sm.parent[t] >= 0) sm.nsub[sm.parent[t]] += sm.nsub[t];
@@ -296,6 +306,9 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
                 const int par = sm.parent[sm.order[j]];
                 if (par >= 0 && par != sm.order[j - 1]) sm.reused[par] = 1;
             }
+            if constexpr (MODE == kTreeLog)   // parents precede children
+                for (int t = 0; t < n; ++t)
+                    path_mask[t] = (1 << t) | (sm.parent[t] >= 0 ? path_mask[sm.parent[t]] : 0);
         }
         if (bad && h == 0) raise_error(p.err, bad);
         sm.bad = bad;
@@ -391,7 +404,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         acc = warp_sum(acc);
         if (lane == 0) sm.kq[t] = acc;
     }
-    if (MODE == kWindowLog) {   // the rows' decay (every head) and normalised key (lead head of the group)
+    if (LOG) {   // the rows' decay (every head) and normalised key (lead head of the group)
         if (tid < n) p.log_a[(size_t)(r0 + tid) * p.Hv + h] = sm.decay[tid];
         if (lead)
             for (int i = tid; i < n * D; i += kRowThreads)
@@ -403,12 +416,38 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
     // ---- a5 + a6: the recurrence, row by row; no CTA barrier inside --------
     const int vi = lane >> SHIFT;
     for (int j = 0; j < n; ++j) {
-        const int t = MODE == kTree ? sm.order[j] : j;   // the row (node) in hand
-        if (MODE == kTree && j > 0) {
+        const int t = TREE ? sm.order[j] : j;   // the row (node) in hand
+        if (TREE && j > 0) {
             const int par = sm.parent[t];
-            if (par != sm.order[j - 1])
-                load_tile<D, RPW, CPL>(S, par < 0 ? slot_tile : p.rec_state + ((size_t)(r0 + par) * p.Hv + h) * tile,
-                                       warp, lane);
+            if (par != sm.order[j - 1]) {
+                if constexpr (MODE == kTree) {
+                    load_tile<D, RPW, CPL>(S, par < 0 ? slot_tile : p.rec_state + ((size_t)(r0 + par) * p.Hv + h) * tile,
+                                           warp, lane);
+                } else {
+                    // the committed state, then the logged rows from the root
+                    // down to the parent (ancestors have smaller indices, so
+                    // ascending order is root first), each as in the forward
+                    // pass:  S <- fma(u, k, a S)
+                    load_tile<D, RPW, CPL>(S, slot_tile, warp, lane);
+                    if (par >= 0) {
+                        __syncwarp();   // this warp's rows of u_rows, written in earlier iterations
+                        const int mask = path_mask[par];
+                        for (int m = 0; m <= par; ++m) {
+                            if (!((mask >> m) & 1)) continue;
+                            const float dm = sm.decay[m];
+                            float km[CPL];
+#pragma unroll
+                            for (int c = 0; c < CPL; ++c) km[c] = sm.k[m][lane * CPL + c];
+#pragma unroll
+                            for (int r = 0; r < RPW; ++r) {
+                                const float ur = u_rows[m][warp * RPW + r];
+#pragma unroll
+                                for (int c = 0; c < CPL; ++c) S[r][c] = __fmaf_rn(ur, km[c], __fmul_rn(dm, S[r][c]));
+                            }
+                        }
+                    }
+                }
+            }
         }
         float kk[CPL], qq[CPL];
 #pragma unroll
@@ -454,8 +493,10 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
             const bool streaming = !(MODE == kTree && sm.reused[t]);
             store_tile<D, RPW, CPL>(p.rec_state + ((size_t)(r0 + t) * p.Hv + h) * tile, S, warp, lane, streaming);
         }
-        if (MODE == kWindowLog && lane < 16 && (lane & ((1 << SHIFT) - 1)) == 0)
+        if (LOG && lane < 16 && (lane & ((1 << SHIFT) - 1)) == 0) {
             p.log_u[((size_t)(r0 + t) * p.Hv + h) * D + warp * RPW + vi] = u;
+            if constexpr (MODE == kTreeLog) u_rows[t][warp * RPW + vi] = u;
+        }
     }
     if (MODE == kStep) store_tile<D, RPW, CPL>(slot_tile + (size_t)row0 * D, S, warp, lane, false);
     if constexpr (P > 1) {

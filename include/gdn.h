@@ -281,6 +281,41 @@ int gdn_commit_replay(const gdn_dims *dims, const gdn_cache *cache, const int32_
                       int32_t n_rows, const float *log_a, const float *log_u,
                       const float *log_k, const void *rec_tail, void *stream);
 
+/*
+ * gdn_tree_log -- tree verify windows that log instead of record ([P932]
+ * tree note: the per-row logs of the decay, the write vector and the key,
+ * and the replay of the kept path, serve trees as well as chains).  As
+ * gdn_tree (same y and rec_tail, bit for bit), with gdn_window_log's logs
+ * (log_a [R, Hv], log_u [R, Hv, d_v], log_k [R, Hk, d_k]) in place of
+ * rec_state, so that S_r = a_r S_parent(r) + u_r k_r^T.  A node whose parent
+ * is not the node visited just before it (nodes are visited depth first,
+ * children in row order) rebuilds its parent's state from the committed
+ * slot by re-applying the logged rows of the root-to-parent path with the
+ * forward pass's rounding, so every state, and y, equals gdn_tree's bit for
+ * bit.  parent is as in gdn_tree.
+ */
+int gdn_tree_log(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
+                 const int32_t *slot, const int32_t *row_ptr, const int32_t *parent,
+                 int32_t n_streams, int32_t n_rows, const gdn_rows *rows, float *log_a,
+                 float *log_u, float *log_k, void *rec_tail, void *stream);
+
+/*
+ * gdn_commit_replay_tree -- commit after gdn_tree_log: for stream s with
+ * keep_row[s] = r in [row_ptr[s], row_ptr[s+1]) (the chosen node), the
+ * slot's state is advanced along the node's root-to-node path (found
+ * through `parent`, the same device array gdn_tree_log took), root first,
+ * with S <- a S + u k^T in the window's own rounding, so it equals bit for
+ * bit what gdn_tree would have recorded for node r; the tail becomes
+ * rec_tail[r].  keep_row[s] = -1 leaves the slot bit-unchanged.  A parent
+ * index on the path outside [-1, its own index) sets GDN_DERR_PARENT and
+ * skips the stream.  Slots must be distinct.
+ */
+int gdn_commit_replay_tree(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot,
+                           const int32_t *row_ptr, const int32_t *parent,
+                           const int32_t *keep_row, int32_t n_streams, int32_t n_rows,
+                           const float *log_a, const float *log_u, const float *log_k,
+                           const void *rec_tail, void *stream);
+
 /* Text for a status code (static storage). */
 const char *gdn_status_string(int status);
 

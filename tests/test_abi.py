@@ -126,3 +126,28 @@ def test_binding_checks_shapes_before_calling():
     with pytest.raises((TypeError, ValueError)):
         B._weights(d, {**bad, "A_log": torch.zeros(4), "dt_bias": torch.zeros(4),
                        "norm_w": torch.zeros(32, dtype=torch.bfloat16)})
+
+
+def test_logged_tree_entry_points_validate_on_the_host():
+    """gdn_tree_log and gdn_commit_replay_tree need the parent array (NULL is
+    GDN_ENULL, a misaligned one GDN_EALIGN) and the logs, like their chain
+    counterparts."""
+    lib = gdn.load()
+    d, w, c, r = _args()
+
+    def tree_log(parent=A16, log_u=A16):
+        return lib.gdn_tree_log(ctypes.byref(d), ctypes.byref(w), ctypes.byref(c), A16, A16, parent, 2, 4,
+                                ctypes.byref(r), A16, log_u, A16, A16, None)
+
+    def replay_tree(parent=A16, keep=A16, n_rows=4):
+        return lib.gdn_commit_replay_tree(ctypes.byref(d), ctypes.byref(c), A16, A16, parent, keep, 2, n_rows,
+                                          A16, A16, A16, A16, None)
+
+    assert tree_log(parent=None) == -2
+    assert tree_log(log_u=None) == -2
+    assert tree_log(parent=A16 + 2) == -3
+    assert tree_log(log_u=A16 + 4) == -3
+    assert replay_tree(parent=None) == -2
+    assert replay_tree(keep=None) == -2
+    assert replay_tree(parent=A16 + 2) == -3
+    assert replay_tree(n_rows=0) == -1

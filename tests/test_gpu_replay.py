@@ -14,7 +14,7 @@ import gated_deltanet_speculative_gb300 as gdn
 import oracle
 from gated_deltanet_speculative_gb300 import synth
 
-from harness import Case, dev, host_bits
+from harness import Case, check_state, check_y, dev, host_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -92,5 +92,121 @@ def test_replay_commit_rejects_keep_outside_the_stream_window():
     before = cache["state"].cpu().numpy().copy()
     bad = np.array([5, -1], np.int32)   # row 5 belongs to stream 1, not stream 0
     gdn.commit_replay(d, cache, dev(c.slots), dev(c.row_ptr), dev(bad), la, lu, lk, lt)
+    assert gdn.get_device_error() & 8
+    assert np.array_equal(cache["state"].cpu().numpy(), before)
+
+
+def _tree_case(g, seed):
+    """Trees of several shapes in one call: random recursive trees, a star, a
+    window with several roots (nodes that follow the committed slot), a
+    chain with late branches, a single node and an empty window."""
+    lengths = [16, 5, 1, 16, 9, 0, 12, 16]
+    c = Case(g, lengths, seed=seed, n_slots=10, tree=True)
+    shapes = {
+        3: [-1] + [0] * 15,                                   # star under node 0
+        4: [-1, 0, -1, 2, 1, -1, 5, 3, 0],                    # three roots
+        6: [-1, 0, 1, 2, 3, 4, 5, 6, 7, 8, 2, 10],            # chain, then a branch from node 2
+    }
+    for s, par in shapes.items():
+        lo, hi = c.stream_rows(s)
+        c.parent[lo:hi] = np.asarray(par, np.int32)
+    return c
+
+
+def _kept_nodes(c: Case, rng):
+    keep = np.full(c.S, -1, np.int32)
+    for s in range(c.S):
+        lo, hi = c.stream_rows(s)
+        if hi == lo or s == 2:          # stream 2 accepts nothing: its slot must keep its bits
+            continue
+        par = c.parent[lo:hi]
+        node = synth.random_leaf(par, rng) if s % 2 == 0 else int(rng.integers(0, hi - lo))
+        keep[s] = lo + node
+    return keep
+
+
+@pytest.mark.parametrize("g", [synth.LIKE_27B, synth.Geometry(2, 4, 64, 64), synth.Geometry(2, 2, 32, 32)])
+def test_logged_tree_and_replay_commit_equal_recorded_tree(g):
+    """gdn_tree_log gives gdn_tree's y and tails bit for bit (a node whose
+    parent is not the node visited before it rebuilds the parent's state by
+    replaying logs from the slot), and gdn_commit_replay_tree leaves every
+    slot exactly as gdn_commit of the recorded node does."""
+    c = _tree_case(g, 95)
+    d = c.dims_gpu()
+    w = c.dev_weights()
+    slot, rp, par = dev(c.slots), dev(c.row_ptr), dev(c.parent)
+    keep = _kept_nodes(c, np.random.default_rng(95))
+
+    cache_r, rows_r = c.dev_cache(), c.dev_rows()
+    rs, rt = c.dev_records()
+    gdn.tree(d, w, cache_r, slot, rp, par, rows_r, rs, rt)
+    gdn.commit(d, cache_r, slot, dev(keep), rs, rt)
+    cache_l, rows_l = c.dev_cache(), c.dev_rows()
+    la, lu, lk, lt = _logs(c)
+    gdn.tree_log(d, w, cache_l, slot, rp, par, rows_l, la, lu, lk, lt)
+    gdn.commit_replay_tree(d, cache_l, slot, rp, par, dev(keep), la, lu, lk, lt)
+    assert gdn.get_device_error() == 0
+
+    assert np.array_equal(host_bits(rows_l["y"])[:c.R], host_bits(rows_r["y"])[:c.R])
+    assert np.array_equal(host_bits(lt)[:c.R], host_bits(rt)[:c.R])
+    assert np.array_equal(cache_l["state"].cpu().numpy().view(np.uint32), cache_r["state"].cpu().numpy().view(np.uint32))
+    assert np.array_equal(host_bits(cache_l["tail"]), host_bits(cache_r["tail"]))
+
+    # each node's log is one rank-1 step from its parent's recorded state (or
+    # the committed slot) to its own
+    la_n, lu_n, lk_n, rs_n = la.cpu().numpy(), lu.cpu().numpy(), lk.cpu().numpy(), rs.cpu().numpy()
+    for s in range(c.S):
+        lo, hi = c.stream_rows(s)
+        sl = int(c.slots[s])
+        for t in range(lo, hi):
+            p_loc = int(c.parent[t])
+            prev = (c.cache["state"][sl] if p_loc < 0 else rs_n[lo + p_loc]).astype(np.float64)
+            kk = lk_n[t][np.arange(g.n_v_heads) // g.group]
+            step = la_n[t][:, None, None] * prev + lu_n[t][:, :, None] * kk[:, None, :]
+            assert np.abs(step - rs_n[t]).max() <= 1e-6 * np.abs(rs_n[t]).max()
+
+
+def test_logged_tree_round_16x16_against_oracle():
+    """The bench's tree round (16 streams x 16-node random trees, 27B-like
+    heads): y within tolerance of the oracle, and the replayed commit of a
+    random leaf per stream equal to the oracle's state at that node."""
+    g = synth.LIKE_27B
+    c = Case(g, [16] * 16, seed=97, tree=True)
+    d = c.dims_gpu()
+    slot, rp, par = dev(c.slots), dev(c.row_ptr), dev(c.parent)
+    rng = np.random.default_rng(97)
+    keep = np.array([c.row_ptr[s] + synth.random_leaf(c.parent[c.row_ptr[s]:c.row_ptr[s + 1]], rng)
+                     for s in range(c.S)], np.int32)
+    cache, rows = c.dev_cache(), c.dev_rows()
+    la, lu, lk, lt = _logs(c)
+    gdn.tree_log(d, c.dev_weights(), cache, slot, rp, par, rows, la, lu, lk, lt)
+    gdn.commit_replay_tree(d, cache, slot, rp, par, dev(keep), la, lu, lk, lt)
+    assert gdn.get_device_error() == 0
+    y = host_bits(rows["y"])
+    st = cache["state"].cpu().numpy()
+    for s in range(c.S):
+        lo, hi = c.stream_rows(s)
+        ref = c.oracle_stream(s)
+        check_y(y[lo:hi], ref["y"], f"stream {s} y")
+        check_state(st[c.slots[s]], ref["rec_state"][keep[s] - lo], f"stream {s} committed state")
+
+
+def test_tree_replay_commit_rejects_bad_parent_and_keep():
+    g = synth.Geometry(2, 4, 32, 32)
+    c = Case(g, [4, 3], seed=99, tree=True)
+    d = c.dims_gpu()
+    w, cache, rows = c.dev_weights(), c.dev_cache(), c.dev_rows()
+    la, lu, lk, lt = _logs(c)
+    par = dev(c.parent)
+    gdn.tree_log(d, w, cache, dev(c.slots), dev(c.row_ptr), par, rows, la, lu, lk, lt)
+    assert gdn.get_device_error() == 0
+    before = cache["state"].cpu().numpy().copy()
+    bad_par = c.parent.copy()
+    bad_par[3] = 3                          # node 3 of stream 0 names itself as its parent
+    gdn.commit_replay_tree(d, cache, dev(c.slots), dev(c.row_ptr), dev(bad_par), dev(np.array([3, -1], np.int32)),
+                           la, lu, lk, lt)
+    assert gdn.get_device_error() & 4
+    gdn.commit_replay_tree(d, cache, dev(c.slots), dev(c.row_ptr), par, dev(np.array([5, -1], np.int32)),
+                           la, lu, lk, lt)   # row 5 belongs to stream 1
     assert gdn.get_device_error() & 8
     assert np.array_equal(cache["state"].cpu().numpy(), before)
