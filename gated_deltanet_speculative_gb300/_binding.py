@@ -72,6 +72,7 @@ _SIGS = {
                      ctypes.POINTER(c_rows), _P, _P, _P, _P, _P],
     "gdn_commit_replay_tree": [ctypes.POINTER(c_dims), ctypes.POINTER(c_cache), _P, _P, _P, _P, _I, _I, _P, _P, _P,
                                _P, _P],
+    "gdn_debug_wait_timeout": [ctypes.c_uint32, _P],
     "gdn_status_string": [ctypes.c_int],
     "gdn_get_device_error": [_P, ctypes.POINTER(ctypes.c_int32)],
 }
@@ -300,6 +301,13 @@ def commit_replay_tree(dims: Dims, cache: dict, slot, row_ptr, parent, keep_row,
            lib.gdn_commit_replay_tree(ctypes.byref(dims.c()), ctypes.byref(cc), _ptr(slot), _ptr(row_ptr),
                                       _ptr(parent), _ptr(keep_row), S, R, _ptr(log_a), _ptr(log_u), _ptr(log_k),
                                       _ptr(rec_tail), _stream_ptr(stream)))
+
+
+def debug_wait_timeout(polls: int = 1000, stream=None):
+    """Run the kernels' bounded mbarrier wait on a phase nothing completes;
+    it gives up after ``polls`` polls and sets the timeout bit (32) of the
+    device error word."""
+    _check("gdn_debug_wait_timeout", load().gdn_debug_wait_timeout(int(polls), _stream_ptr(stream)))
 
 
 PREFILL_CHUNK = 64

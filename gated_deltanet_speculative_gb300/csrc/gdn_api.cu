@@ -364,6 +364,14 @@ int gdn_commit_replay_tree(const gdn_dims *dims, const gdn_cache *cache, const i
                         rec_tail, stream);
 }
 
+int gdn_debug_wait_timeout(uint32_t polls, void *stream) {
+    if (polls > (1u << 22)) return GDN_EINVAL;
+    int *err = error_word();
+    if (!err) return GDN_ECUDA;
+    return gdn::launch_wait_selftest(polls, err, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK
+                                                                                                   : GDN_ECUDA;
+}
+
 const char *gdn_status_string(int status) {
     switch (status) {
         case GDN_OK: return "ok";

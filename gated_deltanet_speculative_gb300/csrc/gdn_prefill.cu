@@ -9,6 +9,25 @@
 
 namespace gdn {
 
+// The bounded-wait failure path without a hang or a fault: the mbarrier is
+// initialised for one arrival that never comes, no copy or MMA refers to it,
+// so the wait runs out after `polls` polls, the error word records it, and
+// the CTA leaves with nothing in flight.
+__global__ void gdn_wait_selftest_kernel(uint32_t polls, int *err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !tc::mbar_wait(&bar, 0, polls)) raise_error(err, GDN_DERR_TIMEOUT);
+}
+
+cudaError_t launch_wait_selftest(unsigned polls, int *err, cudaStream_t st) {
+    gdn_wait_selftest_kernel<<<1, 32, 0, st>>>(polls, err);
+    return cudaGetLastError();
+}
+
 namespace {
 
 // Chunk groups of a pipelined tensor-core prefill: prep of group g runs on

@@ -17,6 +17,11 @@ size_t prefill_chunk_floats(int D);
 // device); otherwise everything runs on `st`.
 cudaError_t launch_prefill(int D, const PrefillParams &p, cudaStream_t st, bool pipelined);
 
+// One CTA waits, with the prefill kernels' bounded mbarrier wait, for a
+// phase that nothing completes; after `polls` polls it raises
+// GDN_DERR_TIMEOUT in *err and returns.  Nothing is in flight meanwhile.
+cudaError_t launch_wait_selftest(unsigned polls, int *err, cudaStream_t st);
+
 // gdn_prefill's validation and launch with the plan chosen by the caller
 // (gdn_prefill: pipelined; gdn_prefill_noalloc: everything on `stream`).
 int prefill_entry(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,

@@ -316,6 +316,21 @@ int gdn_commit_replay_tree(const gdn_dims *dims, const gdn_cache *cache, const i
                            const float *log_a, const float *log_u, const float *log_k,
                            const void *rec_tail, void *stream);
 
+/*
+ * gdn_debug_wait_timeout -- a test hook for the failure path of the bounded
+ * waits (no source passage; the pages name no such check).  Every wait of
+ * the prefill kernels on an mbarrier polls a fixed number of times; if the
+ * phase has not completed by then, the kernel sets GDN_DERR_TIMEOUT in the
+ * device error word, waits (again bounded) for anything it has in flight,
+ * and leaves, so a lost copy or MMA completion ends as an error status, not
+ * a hang.  This call launches one CTA that runs that same wait on an
+ * mbarrier nothing will ever complete, with nothing in flight: after
+ * `polls` polls (at most 2^22; GDN_EINVAL above) it sets GDN_DERR_TIMEOUT
+ * and returns, and the context stays usable.  Read the bit with
+ * gdn_get_device_error.
+ */
+int gdn_debug_wait_timeout(uint32_t polls, void *stream);
+
 /* Text for a status code (static storage). */
 const char *gdn_status_string(int status);
 

@@ -151,3 +151,10 @@ def test_logged_tree_entry_points_validate_on_the_host():
     assert replay_tree(keep=None) == -2
     assert replay_tree(parent=A16 + 2) == -3
     assert replay_tree(n_rows=0) == -1
+
+
+def test_debug_wait_timeout_bounds_its_polls():
+    """The timeout hook refuses a poll count above the kernels' own limit
+    (2^22) before launching anything."""
+    lib = gdn.load()
+    assert lib.gdn_debug_wait_timeout((1 << 22) + 1, None) == -1

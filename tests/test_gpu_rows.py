@@ -308,3 +308,16 @@ def test_device_index_errors_skip_the_stream():
     gdn.commit(d, cache, dev(c.slots), dev(keep), rs, rt)
     assert gdn.get_device_error() & 8
     assert np.array_equal(cache["state"].cpu().numpy(), c.cache["state"])
+
+
+@pytest.mark.parametrize("polls", [0, 1000])
+def test_bounded_wait_timeout_sets_the_error_word_and_the_context_stays_usable(polls):
+    """Failure detection without a hang or a fault: the kernels' bounded
+    mbarrier wait, run on a phase that nothing completes, gives up after
+    `polls` polls and sets the timeout bit; reading the word clears it, and
+    the next call on the same context still matches the oracle."""
+    gdn.debug_wait_timeout(polls)
+    assert gdn.get_device_error() & 32
+    assert gdn.get_device_error() == 0
+    c = Case(synth.Geometry(2, 4, 32, 32), [4, 2], seed=101)
+    compare_with_oracle(c, run_window(c))
