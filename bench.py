@@ -67,7 +67,7 @@ def source_digest() -> str:
     """sha256 of the window kernel's sources (ties ncu counters to a kernel version)."""
     csrc = os.path.join(ROOT, "gated_deltanet_speculative_gb300", "csrc")
     h = hashlib.sha256()
-    for fn in ("gdn_common.cuh", "gdn_rows.cuh", "gdn_launch.h", "gdn_rows_d128.cu"):
+    for fn in ("gdn_common.cuh", "gdn_tc.cuh", "gdn_rows.cuh", "gdn_launch.h", "gdn_rows_d128.cu"):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -2,6 +2,9 @@
 // configuration and status codes.  Nothing here allocates device memory;
 // every buffer belongs to the caller (the d = 128 prefill also uses two side
 // streams and four events of its own per device, made on first use).
+#include <cuda.h>
+
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -115,6 +118,63 @@ struct LogBuffers {
     float *a = nullptr, *u = nullptr, *k = nullptr;
 };
 
+// cuTensorMapEncodeTiled, fetched once through the runtime (the library does
+// not link the driver library itself); nullptr if the driver lacks it.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// Tensor map of a bf16 tensor of rank 2 or 3: dims and box innermost first,
+// strides in elements for dims 1.. (the innermost is contiguous).  Zeros
+// are read outside the tensor.
+bool bf16_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
+              const uint32_t *box) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    cuuint64_t d[3], st[2];
+    cuuint32_t b[3], es[3];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+        if (i > 0) st[i - 1] = strides[i - 1] * 2;
+    }
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), d, st, b, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The row kernel's TMA staging maps (windows and trees with d >= 64): the
+// packed rows [R][CH], the committed tails [n_slots * 3][CH] and z
+// [R][Hv][D], boxes of one head's D channels.
+int encode_row_maps(gdn::RowParams &p, int D, int n_rows) {
+    const uint64_t CH = (uint64_t)p.CH;
+    p.box_rows = std::min(n_rows, (int)GDN_MAX_WINDOW);
+    const uint64_t dm[2] = {CH, (uint64_t)n_rows}, sm_[1] = {CH};
+    const uint32_t bm[2] = {(uint32_t)D, (uint32_t)p.box_rows};
+    const uint64_t dt[2] = {CH, (uint64_t)p.n_slots * 3};
+    const uint32_t bt[2] = {(uint32_t)D, 3u};
+    const uint64_t dz[3] = {(uint64_t)D, (uint64_t)p.Hv, (uint64_t)n_rows}, sz[2] = {(uint64_t)D, (uint64_t)p.Hv * D};
+    const uint32_t bz[3] = {(uint32_t)D, 1u, (uint32_t)p.box_rows};
+    if (!bf16_map(&p.map_mixed, p.mixed, 2, dm, sm_, bm) || !bf16_map(&p.map_tail, p.tail, 2, dt, sm_, bt) ||
+        !bf16_map(&p.map_z, p.z, 3, dz, sz, bz))
+        return GDN_ECUDA;
+    return GDN_OK;
+}
+
 int rows_entry(int mode, const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
                const int32_t *row_ptr, const int32_t *parent, int32_t n_streams, int32_t n_rows,
                const gdn_rows *rows, float *rec_state, void *rec_tail, void *stream, LogBuffers logs = {}) {
@@ -149,6 +209,7 @@ int rows_entry(int mode, const gdn_dims *dims, const gdn_weights *w, const gdn_c
     p.log_a = logs.a;
     p.log_u = logs.u;
     p.log_k = logs.k;
+    if (mode != gdn::kStep && dims->d_k >= 64) GDN_TRY(encode_row_maps(p, dims->d_k, n_rows));
     return launch_rows(dims->d_k, mode, p, n_streams, stream);
 }
 

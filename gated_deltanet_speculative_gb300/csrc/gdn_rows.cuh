@@ -28,7 +28,10 @@
 //   a7  y = o / sqrt(mean o^2 + eps) * w_norm * SiLU(z), rounded to bf16
 #pragma once
 
+#include <cuda.h>
+
 #include "gdn_common.cuh"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 
@@ -67,24 +70,41 @@ struct RowParams {
     float *log_u;             // [R, Hv, D] write u = b (v - a S k) (logged modes)
     float *log_k;             // [R, Hk, D] normalised key (logged modes)
     int *err;                 // device error word
+    // d >= 64: tensor maps of the staged inputs (TMA), encoded per call on the host
+    int box_rows;             // rows of one mixed / z box: 1 for steps, min(16, R) otherwise
+    CUtensorMap map_mixed;    // [R rows][CH] bf16, box [box_rows][D]
+    CUtensorMap map_tail;     // [n_slots * 3 rows][CH] bf16, box [3][D]
+    CUtensorMap map_z;        // [R][Hv][D] bf16, box [box_rows][1][D]
 };
 
 constexpr int kRowThreads = 256;
 constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kMaxRows = GDN_MAX_WINDOW;
+constexpr uint32_t kRowWaitLimit = 1u << 22;   // polls of the staging mbarrier before giving up
+
+// Windows and trees of d >= 64 stage their inputs with TMA.  d = 32 (a
+// parity geometry, whose 3-row tail block is not a multiple of 128 bytes)
+// and steps use 16-byte cp.async: a step has one row to stage, and its CTAs
+// run in clusters, where a CTA leaving early on a staging timeout would
+// strand its partners at the cluster barriers.
+template <int D, int MODE>
+__host__ __device__ constexpr bool rows_use_tma() { return D >= 64 && MODE != kStep; }
 
 template <int D>
-struct __align__(16) RowSmem {
-    float q[kMaxRows][D];
-    float k[kMaxRows][D];
-    float v[kMaxRows][D];
+struct __align__(128) RowSmem {
+    // The staging areas come first: a TMA box lands on a 128-byte boundary
+    // (for d = 64 and 128 every box start below is one).
     union {
-        // staged bf16 conv inputs of this head's q | k | v channels: rows 0..2
-        // are the committed tail (oldest first), row 3 + t is window row t
-        uint16_t xin[kMaxRows + 3][3 * D];
+        // staged bf16 conv inputs of this head's q, k and v channels, part by
+        // part: rows 0..2 are the committed tail (oldest first), row 3 + t is
+        // window row t
+        uint16_t xin[3][kMaxRows + 3][D];
         float o[kMaxRows][D];   // written by the recurrence, after the conv
     } u;
     uint16_t z[kMaxRows][D];
+    float q[kMaxRows][D];
+    float k[kMaxRows][D];
+    float v[kMaxRows][D];
     uint16_t cw[3 * D][4];   // conv weights of this head's q | k | v channels
     uint16_t nw[D];          // RMSNorm weight
     float decay[kMaxRows];
@@ -171,7 +191,7 @@ __device__ __forceinline__ void st_cluster_f32(const float *local, uint32_t rank
 }
 
 template <int D, int MODE, int P = 1>
-__global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParams p) {
+__global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_constant__ RowParams p) {
     static_assert(P == 1 || MODE == kStep, "only steps split the state rows");
     constexpr int RPW = D / (kRowWarps * P);      // state rows per warp
     constexpr int CPL = D / 32;                   // state columns per lane
@@ -179,11 +199,14 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
     constexpr int SHIFT = 5 - Log2<NV>::value;    // lane l holds total (l >> SHIFT)
     constexpr int SEG = D * 2 / 16;               // 16-byte chunks in one q, k or v segment
     constexpr int CHUNKS = 3 * SEG;               // 16-byte chunks in a staged row
+    constexpr bool TMA = rows_use_tma<D, MODE>();
     static_assert(NV >= 2 && NV <= 32, "unsupported head width");
     constexpr bool TREE = MODE == kTree || MODE == kTreeLog;
     constexpr bool LOG = MODE == kWindowLog || MODE == kTreeLog;
 
     __shared__ RowSmem<D> sm;
+    __shared__ __align__(8) uint64_t stage_bar;   // TMA staging completes here
+    __shared__ int stage_fail;                    // a staging wait gave up
     __shared__ float o_all[P > 1 ? D : 1];        // the whole o vector, gathered from the slices
     // logged trees: every row's write u (to rebuild a parent's state) and,
     // per node, the set of rows on its root-to-node path (bit m = row m)
@@ -230,19 +253,40 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
     float S[RPW][CPL];
     load_tile<D, RPW, CPL>(S, slot_tile + (size_t)row0 * D, warp, lane);
 
-    // Stage the committed tail and the window's rows (this head's q | k | v
-    // channels) and the z rows into shared memory, 16 bytes per copy.
+    // Stage the committed tail and the window's rows (this head's q, k and v
+    // channels) and the z rows into shared memory.  d >= 64: seven TMA box
+    // loads issued by one thread onto one mbarrier (per part a [3][D] box of
+    // the tail and a [box_rows][D] box of the rows, and a [box_rows][D] box
+    // of z; box rows past the window are other streams' rows or zeros, and
+    // are never read).  d = 32: 16-byte cp.async.
     const uint16_t *tail = p.tail + (size_t)sl * 3 * CH;
-    for (int i = tid; i < (n + 3) * CHUNKS; i += kRowThreads) {
-        const int row = i / CHUNKS, ch = i - row * CHUNKS;
-        const int part = ch / SEG, off = (ch - part * SEG) * 8;
-        const int c = channel_of<D>(part, off, p.Hk, kh, h);
-        const uint16_t *src = row < 3 ? tail + (size_t)row * CH + c : p.mixed + (size_t)(r0 + row - 3) * CH + c;
-        cp_async16(&sm.u.xin[row][part * D + off], src);
-    }
-    for (int i = tid; i < n * SEG; i += kRowThreads) {
-        const int t = i / SEG, ch = i - t * SEG;
-        cp_async16(&sm.z[t][ch * 8], p.z + ((size_t)(r0 + t) * p.Hv + h) * D + ch * 8);
+    if constexpr (TMA) {
+        if (tid == 0) {
+            stage_fail = 0;
+            tc::mbar_init(&stage_bar, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            tc::fence_async_smem();
+            tc::mbar_expect_tx(&stage_bar, (uint32_t)((3 * (3 + p.box_rows) + p.box_rows) * D * 2));
+#pragma unroll
+            for (int part = 0; part < 3; ++part) {
+                const int c = channel_of<D>(part, 0, p.Hk, kh, h);
+                tc::tma_load_2d(&sm.u.xin[part][0][0], &p.map_tail, c, sl * 3, &stage_bar);
+                tc::tma_load_2d(&sm.u.xin[part][3][0], &p.map_mixed, c, r0, &stage_bar);
+            }
+            tc::tma_load_3d(&sm.z[0][0], &p.map_z, 0, h, r0, &stage_bar);
+        }
+    } else {
+        for (int i = tid; i < (n + 3) * CHUNKS; i += kRowThreads) {
+            const int row = i / CHUNKS, ch = i - row * CHUNKS;
+            const int part = ch / SEG, off = (ch - part * SEG) * 8;
+            const int c = channel_of<D>(part, off, p.Hk, kh, h);
+            const uint16_t *src = row < 3 ? tail + (size_t)row * CH + c : p.mixed + (size_t)(r0 + row - 3) * CH + c;
+            cp_async16(&sm.u.xin[part][row][off], src);
+        }
+        for (int i = tid; i < n * SEG; i += kRowThreads) {
+            const int t = i / SEG, ch = i - t * SEG;
+            cp_async16(&sm.z[t][ch * 8], p.z + ((size_t)(r0 + t) * p.Hv + h) * D + ch * 8);
+        }
     }
     if (TREE && tid < n) sm.parent[tid] = __ldg(p.parent + r0 + tid);
     // ---- a4: gates
@@ -256,6 +300,18 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
     }
     cp_async_wait_all();
     __syncthreads();
+    if constexpr (TMA) {
+        // bounded: on a timeout the error word says so, the stream's outputs
+        // are skipped, and the CTA still waits (bounded) for its copies
+        // before it leaves
+        if (!tc::mbar_wait(&stage_bar, 0, kRowWaitLimit)) {
+            raise_error(p.err, GDN_DERR_TIMEOUT);
+            tc::mbar_wait(&stage_bar, 0, kRowWaitLimit);
+            stage_fail = 1;
+        }
+        __syncthreads();
+        if (stage_fail) return;   // uniform: read after the barrier
+    }
 
     // ---- each row's parent and conv ancestors along its branch -------------
     if (tid == 0) {
@@ -325,10 +381,10 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
         const uint4 wa = wp[0], wb = wp[1];
         const uint32_t wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
         // taps, oldest first: 3, 2 and 1 steps back along the branch, then the row
-        const uint2 x0 = *reinterpret_cast<const uint2 *>(&sm.u.xin[3 + sm.anc[t][2]][cc]);
-        const uint2 x1 = *reinterpret_cast<const uint2 *>(&sm.u.xin[3 + sm.anc[t][1]][cc]);
-        const uint2 x2 = *reinterpret_cast<const uint2 *>(&sm.u.xin[3 + sm.anc[t][0]][cc]);
-        const uint2 x3 = *reinterpret_cast<const uint2 *>(&sm.u.xin[3 + t][cc]);
+        const uint2 x0 = *reinterpret_cast<const uint2 *>(&sm.u.xin[part][3 + sm.anc[t][2]][e]);
+        const uint2 x1 = *reinterpret_cast<const uint2 *>(&sm.u.xin[part][3 + sm.anc[t][1]][e]);
+        const uint2 x2 = *reinterpret_cast<const uint2 *>(&sm.u.xin[part][3 + sm.anc[t][0]][e]);
+        const uint2 x3 = *reinterpret_cast<const uint2 *>(&sm.u.xin[part][3 + t][e]);
         float *dst = part == 0 ? &sm.q[t][e] : (part == 1 ? &sm.k[t][e] : &sm.v[t][e]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -355,7 +411,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
             const int part = ch / SEG, off = (ch - part * SEG) * 8;
             const int c = channel_of<D>(part, off, p.Hk, kh, h);
             *reinterpret_cast<uint4 *>(p.rec_tail + ((size_t)(r0 + t) * 3 + m) * CH + c) =
-                *reinterpret_cast<const uint4 *>(&sm.u.xin[src_row][part * D + off]);
+                *reinterpret_cast<const uint4 *>(&sm.u.xin[part][src_row][off]);
         }
     }
     __syncthreads();
@@ -372,7 +428,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const RowParam
             const int part = ch / SEG, off = (ch - part * SEG) * 8;
             const int c = channel_of<D>(part, off, p.Hk, kh, h);
             *reinterpret_cast<uint4 *>(p.tail + ((size_t)sl * 3 + m) * CH + c) =
-                *reinterpret_cast<const uint4 *>(&sm.u.xin[m + 1][part * D + off]);
+                *reinterpret_cast<const uint4 *>(&sm.u.xin[part][m + 1][off]);
         }
     };
     if (MODE == kStep && P == 1) {

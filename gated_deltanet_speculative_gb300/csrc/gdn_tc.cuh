@@ -1,7 +1,8 @@
 // gdn_tc.cuh -- the sm_100-family tensor-core (tcgen05) and bulk-copy pieces
 // the prefill scan uses, written from the PTX ISA: TMEM allocation, one-thread
 // MMA issue with shared-memory matrix descriptors, MMA completion on an
-// mbarrier, TMEM loads/stores, and 1-D bulk copies (no multicast).
+// mbarrier, TMEM loads/stores, 1-D bulk copies and tiled tensor-map (TMA)
+// loads (no multicast).
 //
 // Operand layout ("K-major, no swizzle"): a row-major R x K bf16 matrix is
 // stored as 8 x 8 core matrices of 128 contiguous bytes (8 rows of 16 bytes);
@@ -105,6 +106,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity, uint3
             : "memory");
     }
     return done != 0;
+}
+
+// Tiled TMA loads global -> shared through a tensor map (a __grid_constant__
+// kernel parameter), completing the box's bytes on `mbar`.  Coordinates are
+// in elements, innermost first; the innermost one times the element size
+// must be a multiple of 16 bytes, and the destination 128-byte aligned.
+// Elements outside the tensor are filled with zeros.
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *map, int x, int y, uint64_t *mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(mbar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *map, int x, int y, int z, uint64_t *mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(mbar))
+        : "memory");
 }
 
 // 1-D bulk copy global -> shared that completes `bytes` on `mbar` (sizes and
