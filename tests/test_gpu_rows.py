@@ -326,3 +326,15 @@ def test_bounded_wait_timeout_sets_the_error_word_and_the_context_stays_usable(p
     assert gdn.get_device_error() == 0
     c = Case(synth.Geometry(2, 4, 32, 32), [4, 2], seed=101)
     compare_with_oracle(c, run_window(c))
+
+
+@pytest.mark.parametrize("g", [synth.Geometry(2, 4, 64, 64), synth.Geometry(2, 6, 128, 128)])
+@pytest.mark.parametrize("lengths", [[1], [3], [2, 1], [15]])
+def test_calls_with_fewer_rows_than_a_staging_box(g, lengths):
+    """The window's inputs are staged in boxes of up to 16 rows; a call whose
+    packed buffer holds fewer rows (1 to 15) uses shorter boxes.  Chains and
+    trees against the oracle."""
+    c = Case(g, lengths, seed=103 + sum(lengths), n_slots=len(lengths) + 1)
+    compare_with_oracle(c, run_window(c))
+    t = Case(g, lengths, seed=107 + sum(lengths), n_slots=len(lengths) + 1, tree=True)
+    compare_with_oracle(t, run_window(t, tree=True))
