@@ -210,3 +210,50 @@ def test_tree_replay_commit_rejects_bad_parent_and_keep():
                            la, lu, lk, lt)   # row 5 belongs to stream 1
     assert gdn.get_device_error() & 8
     assert np.array_equal(cache["state"].cpu().numpy(), before)
+
+
+@pytest.mark.parametrize("round_id", range(8))
+def test_randomised_rounds_logged_equal_recorded_bitwise(round_id):
+    """Shared rounds of random shape (2 to 16 streams, windows of 0 to 16
+    rows, a stream of unrelated rows packed in front, chains or trees,
+    d = 64 or 128,
+    random kept rows, some streams keeping nothing): the logged window and
+    its replay commit equal the recorded window and its copy commit, bit for
+    bit, in y, tails and the committed slots."""
+    rng = np.random.default_rng(3000 + round_id)
+    S = int(rng.integers(2, 17))
+    lengths = rng.integers(0, 17, size=S).tolist()
+    tree = bool(round_id % 2)
+    g = synth.Geometry(4, 12, 128, 128) if round_id % 4 < 2 else synth.Geometry(2, 8, 64, 64)
+    pad = int(rng.integers(0, 5))
+    c = Case(g, [pad] + lengths, seed=4000 + round_id, tree=tree, n_slots=S + 4)
+    keep = np.full(c.S, -1, np.int32)
+    for s in range(1, c.S):
+        lo, hi = c.stream_rows(s)
+        if hi > lo and rng.random() < 0.8:
+            keep[s] = lo + int(rng.integers(0, hi - lo))
+    d, w = c.dims_gpu(), c.dev_weights()
+    slot, rp, kp = dev(c.slots), dev(c.row_ptr), dev(keep)
+    par = dev(c.parent) if tree else None
+
+    cache_r, rows_r = c.dev_cache(), c.dev_rows()
+    rs, rt = c.dev_records()
+    if tree:
+        gdn.tree(d, w, cache_r, slot, rp, par, rows_r, rs, rt)
+    else:
+        gdn.window(d, w, cache_r, slot, rp, rows_r, rs, rt)
+    gdn.commit(d, cache_r, slot, kp, rs, rt)
+    cache_l, rows_l = c.dev_cache(), c.dev_rows()
+    la, lu, lk, lt = _logs(c)
+    if tree:
+        gdn.tree_log(d, w, cache_l, slot, rp, par, rows_l, la, lu, lk, lt)
+        gdn.commit_replay_tree(d, cache_l, slot, rp, par, kp, la, lu, lk, lt)
+    else:
+        gdn.window_log(d, w, cache_l, slot, rp, rows_l, la, lu, lk, lt)
+        gdn.commit_replay(d, cache_l, slot, rp, kp, la, lu, lk, lt)
+    assert gdn.get_device_error() == 0
+
+    assert np.array_equal(host_bits(rows_l["y"])[:c.R], host_bits(rows_r["y"])[:c.R])
+    assert np.array_equal(host_bits(lt)[:c.R], host_bits(rt)[:c.R])
+    assert np.array_equal(cache_l["state"].cpu().numpy().view(np.uint32), cache_r["state"].cpu().numpy().view(np.uint32))
+    assert np.array_equal(host_bits(cache_l["tail"]), host_bits(cache_r["tail"]))
