@@ -35,10 +35,15 @@
  *
  * Conventions shared by every entry point
  *  - Every pointer argument named "device" is a CUDA device pointer owned by
- *    the caller; the library allocates nothing, frees nothing and keeps no
- *    state between calls except, per device, the address of its device error
- *    word.  All work is enqueued on `stream` (a cudaStream_t; NULL = the
- *    legacy default stream) and the call returns without synchronising.
+ *    the caller; the library allocates no device memory, frees nothing and
+ *    keeps no state between calls except, per device, the address of its
+ *    device error word and the SM count, the driver's tensor-map encoder
+ *    (looked up once, for the TMA staging of windows and trees), and the
+ *    d = 128 prefill's two side streams and four events (see gdn_prefill).
+ *    All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and the call returns without synchronising.  Windows
+ *    and trees of d >= 64 encode three tensor maps on the host per call
+ *    (host work only, nothing is enqueued for it).
  *  - bf16 is IEEE bfloat16 (raw 16-bit storage); fp32 is IEEE binary32.
  *    Internally everything is fp32; y is rounded to bf16 (nearest even) once.
  *  - Geometry: Hk key heads, Hv value heads (Hv % Hk == 0, G = Hv/Hk <= 8),
