@@ -145,3 +145,49 @@ def test_prefill_resumed_at_a_grid_point_is_bit_identical(cut):
     assert np.array_equal(s1.view(np.uint32), s2.view(np.uint32))
     assert np.array_equal(t1, t2)
     assert np.array_equal(y1, y2)
+
+
+def test_kept_state_saved_to_host_and_restored_resumes_bit_identical():
+    """A stream's kept state in host memory (TensorFold #888: a kept state is
+    the stream's full recurrent state with its conv history, held in host
+    memory and restored later).  Round 1 is verified and committed; the
+    slot's state and tail are copied to pinned host memory, the device slot
+    is overwritten with garbage, then restored with plain async copies; round
+    2 from the restored slot equals round 2 of an uninterrupted run, bit for
+    bit (the library keeps nothing else between calls)."""
+    g = synth.LIKE_27B
+    S, W = 4, 16
+    c1 = Case(g, [W] * S, seed=131, n_slots=6)
+    c2 = Case(g, [W] * S, seed=137, n_slots=6)   # round 2's rows (same weights and slots as round 1)
+    d, w = c1.dims_gpu(), c1.dev_weights()
+    slot, rp = dev(c1.slots), dev(c1.row_ptr)
+    keep = dev(np.array([c1.row_ptr[s] + (5 * s + 3) % W for s in range(S)], np.int32))
+
+    def round_(cache, c):
+        rows = c.dev_rows()
+        rs, rt = c.dev_records()
+        gdn.window(d, w, cache, slot, rp, rows, rs, rt)
+        gdn.commit(d, cache, slot, keep, rs, rt)
+        return rows
+
+    # uninterrupted: round 1, round 2
+    cache_a = c1.dev_cache()
+    round_(cache_a, c1)
+    rows_a = round_(cache_a, c2)
+    # interrupted: round 1, save to pinned host memory, poison, restore, round 2
+    cache_b = c1.dev_cache()
+    round_(cache_b, c1)
+    host_state = torch.empty(cache_b["state"].shape, dtype=torch.float32).pin_memory()
+    host_tail = torch.empty(cache_b["tail"].shape, dtype=torch.bfloat16).pin_memory()
+    host_state.copy_(cache_b["state"], non_blocking=True)
+    host_tail.copy_(cache_b["tail"], non_blocking=True)
+    torch.cuda.synchronize()
+    cache_b["state"].fill_(float("nan"))
+    cache_b["tail"].fill_(float("nan"))
+    cache_b["state"].copy_(host_state, non_blocking=True)
+    cache_b["tail"].copy_(host_tail, non_blocking=True)
+    rows_b = round_(cache_b, c2)
+    assert gdn.get_device_error() == 0
+    assert np.array_equal(host_bits(rows_b["y"]), host_bits(rows_a["y"]))
+    assert np.array_equal(cache_b["state"].cpu().numpy().view(np.uint32), cache_a["state"].cpu().numpy().view(np.uint32))
+    assert np.array_equal(host_bits(cache_b["tail"]), host_bits(cache_a["tail"]))
