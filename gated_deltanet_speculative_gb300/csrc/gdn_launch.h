@@ -25,13 +25,19 @@ cudaError_t launch_step(const RowParams &p, int n_streams, cudaStream_t st) {
     cfg.blockDim = dim3(kRowThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = p.G * P;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // The step may be scheduled before the previous kernel ends (it waits for
+    // it, griddepcontrol.wait, before touching memory), which hides the launch
+    // gap between back-to-back steps; a previous kernel that does not signal
+    // its dependents simply runs to its end first.
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gdn_rows_kernel<D, kStep, P>, p);
 }
 

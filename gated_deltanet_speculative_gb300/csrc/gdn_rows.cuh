@@ -216,6 +216,16 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
     const int sli = blockIdx.x % P;               // row slice: state rows [row0, row0 + D/P)
     const int row0 = sli * (D / P);
     if constexpr (P > 1) cluster_arrive_relaxed();   // "started"; waited on before the first remote store
+    // Steps are launched as programmatic dependents of the kernel before them
+    // (decode runs them back to back, layer after layer): the CTAs may be
+    // scheduled while that kernel finishes, and wait here, before their first
+    // global access, until it has completed and its writes are visible, so
+    // ordering is that of a plain launch; then they let the next step be
+    // scheduled in turn.
+    if constexpr (MODE == kStep) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kh = h / p.G;
     const size_t CH = (size_t)p.CH;

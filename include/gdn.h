@@ -130,7 +130,13 @@ typedef struct {
  * committed state and tail of slot[s]; y[s] is written.
  *   slot      device int32 [n_streams], distinct values in [0, n_slots)
  *   n_streams >= 1 (<= 65535)
- * Launch: one CTA per (value head, stream), clusters of G CTAs.
+ * Launch: one CTA per (value head, stream), each head's state rows split
+ * over up to 8 CTAs when few streams would leave SMs idle, clusters of the
+ * key head's value heads.  The launch is a programmatic dependent of the
+ * kernel before it on `stream`: its CTAs may be scheduled while that kernel
+ * finishes, but touch no memory until it has completed, so ordering is that
+ * of a plain launch (back-to-back steps, e.g. layer after layer in a graph,
+ * overlap only their launch gaps).
  */
 int gdn_step(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
              const int32_t *slot, int32_t n_streams, const gdn_rows *rows,

@@ -9,7 +9,7 @@ import torch
 import gated_deltanet_speculative_gb300 as gdn
 from gated_deltanet_speculative_gb300 import synth
 
-from harness import Case, check_state, check_y, dev, host_bits
+from harness import Case, check_state, check_y, dev, dev_bf16, host_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -34,3 +34,57 @@ def test_decode_24_layers(n_streams):
             check_y(y[s:s + 1], ref["y"], what=f"decode y stream {s}")
             check_state(st[sl], ref["rec_state"][0], what=f"decode state stream {s}")
             assert np.array_equal(tl[sl], ref["rec_tail"][0])
+
+
+@pytest.mark.parametrize("n_streams", [1, 4])
+def test_dependent_steps_captured_in_a_graph_equal_eager_bitwise(n_streams):
+    """Steps are launched as programmatic dependents of the kernel before
+    them and wait for it before touching memory.  Eight consecutive steps on
+    the same slots (each reads the state and tail the one before wrote),
+    captured in a graph and replayed, equal eight eager steps bit for bit
+    (2B-like heads: sliced, clustered steps)."""
+    g = synth.LIKE_2B
+    T = 8
+    c = Case(g, [1] * (n_streams * T), seed=151 + n_streams, n_slots=n_streams + 1,
+             slots=np.arange(n_streams * T, dtype=np.int32) % n_streams)
+    d, w = c.dims_gpu(), c.dev_weights()
+    slot = dev(np.arange(n_streams, dtype=np.int32))
+    rows_t = []
+    for t in range(T):
+        sel = slice(t * n_streams, (t + 1) * n_streams)
+        r = {k: dev_bf16(c.rows[k][sel]) for k in ("mixed", "z", "a", "b")}
+        r["y"] = torch.zeros((n_streams, g.n_v_heads, g.d_v), dtype=torch.bfloat16, device="cuda")
+        rows_t.append(r)
+    base_state, base_tail = dev(c.cache["state"]), dev_bf16(c.cache["tail"])
+
+    cache = {"state": base_state.clone(), "tail": base_tail.clone()}
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        gdn.step(d, w, {"state": base_state.clone(), "tail": base_tail.clone()}, slot,
+                 dict(rows_t[0], y=torch.zeros_like(rows_t[0]["y"])), side)   # warm, outside the capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            for t in range(T):
+                gdn.step(d, w, cache, slot, rows_t[t], side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    cache["state"].copy_(base_state)
+    cache["tail"].copy_(base_tail)
+    for r in rows_t:
+        r["y"].zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert gdn.get_device_error() == 0
+    got_y = [host_bits(r["y"]) for r in rows_t]
+    got_s, got_t = cache["state"].cpu().numpy().view(np.uint32), host_bits(cache["tail"])
+
+    e_cache = {"state": base_state.clone(), "tail": base_tail.clone()}
+    for t in range(T):
+        e_rows = dict(rows_t[t], y=torch.zeros_like(rows_t[t]["y"]))
+        gdn.step(d, w, e_cache, slot, e_rows)
+        assert np.array_equal(host_bits(e_rows["y"]), got_y[t]), f"y of step {t}"
+    torch.cuda.synchronize()
+    assert np.array_equal(e_cache["state"].cpu().numpy().view(np.uint32), got_s)
+    assert np.array_equal(host_bits(e_cache["tail"]), got_t)
