@@ -338,3 +338,30 @@ def test_calls_with_fewer_rows_than_a_staging_box(g, lengths):
     compare_with_oracle(c, run_window(c))
     t = Case(g, lengths, seed=107 + sum(lengths), n_slots=len(lengths) + 1, tree=True)
     compare_with_oracle(t, run_window(t, tree=True))
+
+
+@pytest.mark.parametrize("tree", [False, True])
+def test_many_streams_in_one_call(tree):
+    """200 streams in one call (the ABI allows up to 65535; the bench's round
+    has 16), windows of 0 to 16 rows: sampled streams against the oracle and,
+    bit for bit, against the same stream run alone."""
+    g = synth.Geometry(2, 4, 64, 64)
+    rng = np.random.default_rng(211 + tree)
+    lengths = rng.integers(0, 17, size=200).tolist()
+    c = Case(g, lengths, seed=213 + tree, tree=tree, n_slots=203)
+    out = run_window(c, tree=tree)
+    sample = [s for s in (0, 1, 57, 123, 198, 199) if lengths[s] > 0]
+    compare_with_oracle(c, out, streams=sample)
+    for s in sample:
+        lo, hi = c.stream_rows(s)
+        solo = Case(g, [hi - lo], seed=213 + tree, slots=[0], tree=tree)
+        solo.w = c.w
+        sl = c.slots[s]
+        solo.cache = {"state": c.cache["state"][sl:sl + 1], "tail": c.cache["tail"][sl:sl + 1]}
+        solo.rows = {k: v[lo:hi] for k, v in c.rows.items()}
+        if tree:
+            solo.parent = c.parent[lo:hi].copy()
+        alone = run_window(solo, tree=tree)
+        assert np.array_equal(alone["y"], out["y"][lo:hi]), f"y stream {s}"
+        assert np.array_equal(alone["rec_state"].view(np.uint32), out["rec_state"][lo:hi].view(np.uint32))
+        assert np.array_equal(alone["rec_tail"], out["rec_tail"][lo:hi])
