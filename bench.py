@@ -447,6 +447,7 @@ def run_extra(dev, stream, flush, reps=20, only=None):
 
     if only in (None, "tree"):
         out["tree_round_16x16"] = _extra_tree(dev, stream, flush, reps, hbm)
+        out["few_stream_windows_27b_like"] = _extra_few_streams(dev, stream, flush, reps, hbm)
     if only in (None, "replay"):
         out["logged_round_replay_commit_16x16"] = _extra_logged_round(dev, stream, flush, reps, hbm)
         out["logged_tree_replay_commit_16x16"] = _extra_logged_tree(dev, stream, flush, reps, hbm)
@@ -568,6 +569,35 @@ def _extra_logged_tree(dev, stream, flush, reps, hbm):
             "recorded_tree_and_commit_ms": ms_rec, "recorded_rows_per_s": R / (ms_rec * 1e-3),
             "note": "parent states rebuilt from the slot (an L2 re-read plus a replay of the logged path) "
                     "are not counted"}
+
+
+def _extra_few_streams(dev, stream, flush, reps, hbm):
+    """Verify windows of 1, 2 and 4 streams x 16 rows (27B-like heads, all
+    rows recorded): latency-bound, the case a lone stream's round meets."""
+    import torch
+    import gated_deltanet_speculative_gb300 as gdn
+    g = GEOM
+    out = {}
+    for S in (1, 2, 4):
+        R = S * WINDOW
+        w = synth.layer_weights(g, 5)
+        cache = synth.slot_cache(g, S, 5)
+        rows = synth.row_inputs(g, R, 5)
+        d = gdn.Dims(g.n_k_heads, g.n_v_heads, g.d_k, g.d_v)
+        dw = {"conv_w": _bf(w["conv_w"]).to(dev), "A_log": torch.from_numpy(w["A_log"]).to(dev),
+              "dt_bias": torch.from_numpy(w["dt_bias"]).to(dev), "norm_w": _bf(w["norm_w"]).to(dev)}
+        dc = {"state": torch.from_numpy(cache["state"]).to(dev), "tail": _bf(cache["tail"]).to(dev)}
+        dr = {k: _bf(rows[k]).to(dev) for k in ("mixed", "z", "a", "b")}
+        dr["y"] = torch.empty((R, g.n_v_heads, g.d_v), dtype=torch.bfloat16, device=dev)
+        rs = torch.empty((R, g.n_v_heads, g.d_v, g.d_k), dtype=torch.float32, device=dev)
+        rt = torch.empty((R, 3, g.channels), dtype=torch.bfloat16, device=dev)
+        slot_t = torch.arange(S, dtype=torch.int32, device=dev)
+        rp_t = torch.from_numpy(synth.row_ptr([WINDOW] * S)).to(dev)
+        ms = _timed(lambda: gdn.window(d, dw, dc, slot_t, rp_t, dr, rs, rt, stream), max(reps, 20), stream, flush)
+        wb = window_bytes(g, S, R)
+        out[str(S)] = {"us_per_window": ms * 1e3, "rows_per_s": R / (ms * 1e-3),
+                       "frac_hbm": wb / (ms * 1e-3) / 1e9 / hbm}
+    return out
 
 
 def _extra_tree(dev, stream, flush, reps, hbm):

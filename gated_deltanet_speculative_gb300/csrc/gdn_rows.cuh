@@ -7,12 +7,14 @@
 //   registers for the whole window, so it crosses HBM once on the way in and
 //   once per recorded row on the way out.
 //
-// Steps may also split the tile's rows over P CTAs of a cluster (P slices of
-// D/P rows; every state row evolves from its own row, k, q and the gates
-// alone).  Each row's sums stay inside one warp with the same lane layout,
-// so a sliced step equals an unsliced one bit for bit; the RMSNorm, the only
-// step that mixes rows, gathers the whole o vector into every slice through
-// distributed shared memory and reduces it in the unsliced order.
+// Steps and chain windows may also split the tile's rows over P CTAs of a
+// cluster (P slices of D/P rows; every state row evolves from its own row,
+// k, q and the gates alone), when the (stream, head) units alone would
+// leave SMs idle.  Each row's sums stay inside one warp with the same lane
+// layout, so a sliced step or window equals an unsliced one bit for bit; the
+// RMSNorm, the only step that mixes rows, gathers the whole o vector into
+// every slice through distributed shared memory and reduces it in the
+// unsliced order.
 //
 // Per row (TensorFold #932, Qwen3.5 CUDA engine note: gated delta rule and
 // causal convolution; tree note: taps and recurrence follow each row's
@@ -82,13 +84,13 @@ constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kMaxRows = GDN_MAX_WINDOW;
 constexpr uint32_t kRowWaitLimit = 1u << 22;   // polls of the staging mbarrier before giving up
 
-// Windows and trees of d >= 64 stage their inputs with TMA.  d = 32 (a
-// parity geometry, whose 3-row tail block is not a multiple of 128 bytes)
-// and steps use 16-byte cp.async: a step has one row to stage, and its CTAs
-// run in clusters, where a CTA leaving early on a staging timeout would
-// strand its partners at the cluster barriers.
-template <int D, int MODE>
-__host__ __device__ constexpr bool rows_use_tma() { return D >= 64 && MODE != kStep; }
+// Unclustered windows and trees of d >= 64 stage their inputs with TMA.
+// d = 32 (a parity geometry, whose 3-row tail block is not a multiple of 128
+// bytes), steps and row-sliced windows use 16-byte cp.async: a step has one
+// row to stage, and clustered CTAs must not leave early on a staging timeout,
+// which would strand their partners at the cluster barriers.
+template <int D, int MODE, int P>
+__host__ __device__ constexpr bool rows_use_tma() { return D >= 64 && MODE != kStep && P == 1; }
 
 template <int D>
 struct __align__(128) RowSmem {
@@ -192,14 +194,14 @@ __device__ __forceinline__ void st_cluster_f32(const float *local, uint32_t rank
 
 template <int D, int MODE, int P = 1>
 __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_constant__ RowParams p) {
-    static_assert(P == 1 || MODE == kStep, "only steps split the state rows");
+    static_assert(P == 1 || MODE == kStep || MODE == kWindow, "only steps and chain windows split the state rows");
     constexpr int RPW = D / (kRowWarps * P);      // state rows per warp
     constexpr int CPL = D / 32;                   // state columns per lane
     constexpr int NV = 2 * RPW;                   // partial sums per lane: S k and S q
     constexpr int SHIFT = 5 - Log2<NV>::value;    // lane l holds total (l >> SHIFT)
     constexpr int SEG = D * 2 / 16;               // 16-byte chunks in one q, k or v segment
     constexpr int CHUNKS = 3 * SEG;               // 16-byte chunks in a staged row
-    constexpr bool TMA = rows_use_tma<D, MODE>();
+    constexpr bool TMA = rows_use_tma<D, MODE, P>();
     static_assert(NV >= 2 && NV <= 32, "unsupported head width");
     constexpr bool TREE = MODE == kTree || MODE == kTreeLog;
     constexpr bool LOG = MODE == kWindowLog || MODE == kTreeLog;
@@ -207,7 +209,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
     __shared__ RowSmem<D> sm;
     __shared__ __align__(8) uint64_t stage_bar;   // TMA staging completes here
     __shared__ int stage_fail;                    // a staging wait gave up
-    __shared__ float o_all[P > 1 ? D : 1];        // the whole o vector, gathered from the slices
+    // the whole o vector of each row, gathered from the slices
+    __shared__ float o_all[P > 1 && MODE != kStep ? kMaxRows : 1][P > 1 ? D : 1];
     // logged trees: every row's write u (to rebuild a parent's state) and,
     // per node, the set of rows on its root-to-node path (bit m = row m)
     __shared__ float u_rows[MODE == kTreeLog ? kMaxRows : 1][MODE == kTreeLog ? D : 1];
@@ -215,6 +218,9 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
     const int h = blockIdx.x / P, s = blockIdx.y;
     const int sli = blockIdx.x % P;               // row slice: state rows [row0, row0 + D/P)
     const int row0 = sli * (D / P);
+    // cluster rank of slice 0 of this head: a step's cluster holds the G value
+    // heads of its key head (G * P CTAs), a window's only the P slices of one head
+    const int crank0 = MODE == kStep ? (h % p.G) * P : 0;
     if constexpr (P > 1) cluster_arrive_relaxed();   // "started"; waited on before the first remote store
     // Steps are launched as programmatic dependents of the kernel before them
     // (decode runs them back to back, layer after layer): the CTAs may be
@@ -411,7 +417,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
     // ---- a6 (tail): the three newest inputs after each row, oldest first ----
     const int own_lo = lead ? 0 : 2 * SEG;   // chunks this CTA owns: v always, q/k if lead
     const int per_row = CHUNKS - own_lo;
-    if (MODE != kStep) {
+    if (MODE != kStep && sli == 0) {   // slice 0 of a sliced window writes them
         for (int i = tid; i < n * 3 * per_row; i += kRowThreads) {
             const int t = i / (3 * per_row);
             const int rem = i - t * 3 * per_row;
@@ -544,7 +550,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
             const float ov = __fmaf_rn(u_pair, sm.kq[t], __fmul_rn(dec, tot));
             if constexpr (P > 1) {   // into every slice of this head (cluster ranks (h % G) * P + j)
 #pragma unroll
-                for (int j = 0; j < P; ++j) st_cluster_f32(&o_all[row], (uint32_t)((h % p.G) * P + j), ov);
+                for (int j = 0; j < P; ++j)
+                    st_cluster_f32(&o_all[MODE == kStep ? 0 : t][row], (uint32_t)(crank0 + j), ov);
             } else {
                 sm.u.o[t][row] = ov;
             }
@@ -557,7 +564,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
         }
         if (MODE == kWindow || MODE == kTree) {
             const bool streaming = !(MODE == kTree && sm.reused[t]);
-            store_tile<D, RPW, CPL>(p.rec_state + ((size_t)(r0 + t) * p.Hv + h) * tile, S, warp, lane, streaming);
+            store_tile<D, RPW, CPL>(p.rec_state + ((size_t)(r0 + t) * p.Hv + h) * tile + (size_t)row0 * D, S, warp,
+                                    lane, streaming);
         }
         if (LOG && lane < 16 && (lane & ((1 << SHIFT) - 1)) == 0) {
             p.log_u[((size_t)(r0 + t) * p.Hv + h) * D + warp * RPW + vi] = u;
@@ -567,7 +575,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
     if (MODE == kStep) store_tile<D, RPW, CPL>(slot_tile + (size_t)row0 * D, S, warp, lane, false);
     if constexpr (P > 1) {
         cluster_sync_all();   // every slice's o rows have landed in every slice
-        shift_tail();         // and every slice has staged the old tail long ago
+        if (MODE == kStep) shift_tail();   // and every slice has staged the old tail long ago
     } else {
         __syncthreads();
     }
@@ -576,7 +584,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
     for (int t = warp; t < n; t += kRowWarps) {
         float ov[CPL];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) ov[c] = P > 1 ? o_all[lane * CPL + c] : sm.u.o[t][lane * CPL + c];
+        for (int c = 0; c < CPL; ++c)
+            ov[c] = P > 1 ? o_all[MODE == kStep ? 0 : t][lane * CPL + c] : sm.u.o[t][lane * CPL + c];
         float ss = __fmul_rn(ov[0], ov[0]);
 #pragma unroll
         for (int c = 1; c < CPL; ++c) ss = __fmaf_rn(ov[c], ov[c], ss);

@@ -365,3 +365,25 @@ def test_many_streams_in_one_call(tree):
         assert np.array_equal(alone["y"], out["y"][lo:hi]), f"y stream {s}"
         assert np.array_equal(alone["rec_state"].view(np.uint32), out["rec_state"][lo:hi].view(np.uint32))
         assert np.array_equal(alone["rec_tail"], out["rec_tail"][lo:hi])
+
+
+@pytest.mark.parametrize("g,n_round", [(synth.LIKE_2B, 5), (synth.Geometry(2, 6, 128, 128), 13),
+                                       (synth.Geometry(2, 4, 64, 64), 20), (synth.LIKE_27B, 2)])
+def test_sliced_windows_equal_unsliced_bitwise(g, n_round):
+    """A window of few streams splits each head's state rows over a cluster of
+    2 to 8 CTAs (a lone 2B-like stream: 8; a lone 27B-like stream: 2); a round
+    of n_round streams has enough (stream, head) units to run unsliced.  Each
+    stream alone equals the same stream in the round, bit for bit."""
+    c = Case(g, [16, 9, 1] + [16] * (n_round - 3), seed=223, n_slots=n_round + 1)
+    full = run_window(c)
+    for s in range(3):
+        lo, hi = c.stream_rows(s)
+        solo = Case(g, [hi - lo], seed=223, slots=[0])
+        solo.w = c.w
+        sl = c.slots[s]
+        solo.cache = {"state": c.cache["state"][sl:sl + 1], "tail": c.cache["tail"][sl:sl + 1]}
+        solo.rows = {k: v[lo:hi] for k, v in c.rows.items()}
+        out = run_window(solo)
+        assert np.array_equal(out["y"], full["y"][lo:hi]), f"y stream {s}"
+        assert np.array_equal(out["rec_state"].view(np.uint32), full["rec_state"][lo:hi].view(np.uint32))
+        assert np.array_equal(out["rec_tail"], full["rec_tail"][lo:hi])
