@@ -572,8 +572,9 @@ def _extra_logged_tree(dev, stream, flush, reps, hbm):
 
 
 def _extra_few_streams(dev, stream, flush, reps, hbm):
-    """Verify windows of 1, 2 and 4 streams x 16 rows (27B-like heads, all
-    rows recorded): latency-bound, the case a lone stream's round meets."""
+    """Verify windows of 1, 2 and 4 streams x 16 rows, and a lone stream's
+    16-node tree (27B-like heads, all rows recorded): latency-bound, the case
+    a lone stream's round meets."""
     import torch
     import gated_deltanet_speculative_gb300 as gdn
     g = GEOM
@@ -597,6 +598,11 @@ def _extra_few_streams(dev, stream, flush, reps, hbm):
         wb = window_bytes(g, S, R)
         out[str(S)] = {"us_per_window": ms * 1e3, "rows_per_s": R / (ms * 1e-3),
                        "frac_hbm": wb / (ms * 1e-3) / 1e9 / hbm}
+        if S == 1:   # a lone stream's 16-node random tree, all nodes recorded
+            par_t = torch.from_numpy(synth.random_tree(WINDOW, np.random.default_rng([5, 1]))).to(dev)
+            ms_t = _timed(lambda: gdn.tree(d, dw, dc, slot_t, rp_t, par_t, dr, rs, rt, stream), max(reps, 20), stream,
+                          flush)
+            out["1"]["us_per_tree"] = ms_t * 1e3
     return out
 
 

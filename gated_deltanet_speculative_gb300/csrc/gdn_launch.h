@@ -65,8 +65,8 @@ inline int step_slices(int D, int G, int Hv, int n_streams) {
     return P;
 }
 
-// Chain windows of few streams split each head's state rows over P CTAs of a
-// cluster of P (a window shifts no tail in place, so its cluster is one
+// Windows and trees of few streams split each head's state rows over P CTAs
+// of a cluster of P (they shift no tail in place, so a cluster is one
 // head's slices): double P while the cluster stays within 8 CTAs, every warp
 // keeps at least one state row, and every CTA still has an SM of its own.
 // A window CTA runs its rows one after another, so a slice that shares an
@@ -81,7 +81,7 @@ inline int window_slices(int D, int Hv, int n_streams) {
     return P;
 }
 
-template <int D, int P>
+template <int D, int MODE, int P>
 cudaError_t launch_window_sliced(const RowParams &p, int n_streams, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.Hv * P, n_streams);
@@ -95,12 +95,22 @@ cudaError_t launch_window_sliced(const RowParams &p, int n_streams, cudaStream_t
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gdn_rows_kernel<D, kWindow, P>, p);
+    return cudaLaunchKernelEx(&cfg, gdn_rows_kernel<D, MODE, P>, p);
+}
+
+template <int D, int MODE>
+cudaError_t launch_window_mode(const RowParams &p, int n_streams, cudaStream_t st) {
+    const int P = window_slices(D, p.Hv, n_streams);
+    if constexpr (D >= 64)
+        if (P == 8) return launch_window_sliced<D, MODE, 8>(p, n_streams, st);
+    if (P == 4) return launch_window_sliced<D, MODE, 4>(p, n_streams, st);
+    if (P == 2) return launch_window_sliced<D, MODE, 2>(p, n_streams, st);
+    gdn_rows_kernel<D, MODE><<<dim3(p.Hv, n_streams), kRowThreads, 0, st>>>(p);
+    return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_rows(int mode, const RowParams &p, int n_streams, cudaStream_t st) {
-    const dim3 grid(p.Hv, n_streams), block(kRowThreads);
     if (mode == kStep) {
         const int P = step_slices(D, p.G, p.Hv, n_streams);
         if constexpr (D >= 64)
@@ -109,17 +119,10 @@ cudaError_t launch_rows(int mode, const RowParams &p, int n_streams, cudaStream_
         if (P == 2) return launch_step<D, 2>(p, n_streams, st);
         return launch_step<D, 1>(p, n_streams, st);
     }
-    if (mode == kWindow) {
-        const int P = window_slices(D, p.Hv, n_streams);
-        if constexpr (D >= 64)
-            if (P == 8) return launch_window_sliced<D, 8>(p, n_streams, st);
-        if (P == 4) return launch_window_sliced<D, 4>(p, n_streams, st);
-        if (P == 2) return launch_window_sliced<D, 2>(p, n_streams, st);
-        gdn_rows_kernel<D, kWindow><<<grid, block, 0, st>>>(p);
-    } else if (mode == kWindowLog) gdn_rows_kernel<D, kWindowLog><<<grid, block, 0, st>>>(p);
-    else if (mode == kTreeLog) gdn_rows_kernel<D, kTreeLog><<<grid, block, 0, st>>>(p);
-    else gdn_rows_kernel<D, kTree><<<grid, block, 0, st>>>(p);
-    return cudaGetLastError();
+    if (mode == kWindow) return launch_window_mode<D, kWindow>(p, n_streams, st);
+    if (mode == kWindowLog) return launch_window_mode<D, kWindowLog>(p, n_streams, st);
+    if (mode == kTreeLog) return launch_window_mode<D, kTreeLog>(p, n_streams, st);
+    return launch_window_mode<D, kTree>(p, n_streams, st);
 }
 
 }  // namespace gdn

@@ -7,7 +7,7 @@
 //   registers for the whole window, so it crosses HBM once on the way in and
 //   once per recorded row on the way out.
 //
-// Steps and chain windows may also split the tile's rows over P CTAs of a
+// Steps, windows and trees may also split the tile's rows over P CTAs of a
 // cluster (P slices of D/P rows; every state row evolves from its own row,
 // k, q and the gates alone), when the (stream, head) units alone would
 // leave SMs idle.  Each row's sums stay inside one warp with the same lane
@@ -86,9 +86,10 @@ constexpr uint32_t kRowWaitLimit = 1u << 22;   // polls of the staging mbarrier 
 
 // Unclustered windows and trees of d >= 64 stage their inputs with TMA.
 // d = 32 (a parity geometry, whose 3-row tail block is not a multiple of 128
-// bytes), steps and row-sliced windows use 16-byte cp.async: a step has one
-// row to stage, and clustered CTAs must not leave early on a staging timeout,
-// which would strand their partners at the cluster barriers.
+// bytes), steps and row-sliced windows and trees use 16-byte cp.async: a
+// step has one row to stage, and clustered CTAs must not leave early on a
+// staging timeout, which would strand their partners at the cluster
+// barriers.
 template <int D, int MODE, int P>
 __host__ __device__ constexpr bool rows_use_tma() { return D >= 64 && MODE != kStep && P == 1; }
 
@@ -194,7 +195,7 @@ __device__ __forceinline__ void st_cluster_f32(const float *local, uint32_t rank
 
 template <int D, int MODE, int P = 1>
 __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_constant__ RowParams p) {
-    static_assert(P == 1 || MODE == kStep || MODE == kWindow, "only steps and chain windows split the state rows");
+    static_assert(P == 1 || D / (kRowWarps * P) >= 1, "every warp keeps at least one state row");
     constexpr int RPW = D / (kRowWarps * P);      // state rows per warp
     constexpr int CPL = D / 32;                   // state columns per lane
     constexpr int NV = 2 * RPW;                   // partial sums per lane: S k and S q
@@ -477,8 +478,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
         if (lane == 0) sm.kq[t] = acc;
     }
     if (LOG) {   // the rows' decay (every head) and normalised key (lead head of the group)
-        if (tid < n) p.log_a[(size_t)(r0 + tid) * p.Hv + h] = sm.decay[tid];
-        if (lead)
+        if (tid < n && sli == 0) p.log_a[(size_t)(r0 + tid) * p.Hv + h] = sm.decay[tid];
+        if (lead && sli == 0)
             for (int i = tid; i < n * D; i += kRowThreads)
                 p.log_k[((size_t)(r0 + i / D) * p.Hk + kh) * D + i % D] = sm.k[i / D][i % D];
     }
@@ -493,14 +494,15 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
             const int par = sm.parent[t];
             if (par != sm.order[j - 1]) {
                 if constexpr (MODE == kTree) {
-                    load_tile<D, RPW, CPL>(S, par < 0 ? slot_tile : p.rec_state + ((size_t)(r0 + par) * p.Hv + h) * tile,
+                    load_tile<D, RPW, CPL>(S, (par < 0 ? slot_tile : p.rec_state + ((size_t)(r0 + par) * p.Hv + h) * tile) +
+                                                  (size_t)row0 * D,
                                            warp, lane);
                 } else {
                     // the committed state, then the logged rows from the root
                     // down to the parent (ancestors have smaller indices, so
                     // ascending order is root first), each as in the forward
                     // pass:  S <- fma(u, k, a S)
-                    load_tile<D, RPW, CPL>(S, slot_tile, warp, lane);
+                    load_tile<D, RPW, CPL>(S, slot_tile + (size_t)row0 * D, warp, lane);
                     if (par >= 0) {
                         __syncwarp();   // this warp's rows of u_rows, written in earlier iterations
                         const int mask = path_mask[par];
@@ -568,7 +570,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
                                     lane, streaming);
         }
         if (LOG && lane < 16 && (lane & ((1 << SHIFT) - 1)) == 0) {
-            p.log_u[((size_t)(r0 + t) * p.Hv + h) * D + warp * RPW + vi] = u;
+            p.log_u[((size_t)(r0 + t) * p.Hv + h) * D + row0 + warp * RPW + vi] = u;
             if constexpr (MODE == kTreeLog) u_rows[t][warp * RPW + vi] = u;
         }
     }

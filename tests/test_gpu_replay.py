@@ -257,3 +257,47 @@ def test_randomised_rounds_logged_equal_recorded_bitwise(round_id):
     assert np.array_equal(host_bits(lt)[:c.R], host_bits(rt)[:c.R])
     assert np.array_equal(cache_l["state"].cpu().numpy().view(np.uint32), cache_r["state"].cpu().numpy().view(np.uint32))
     assert np.array_equal(host_bits(cache_l["tail"]), host_bits(cache_r["tail"]))
+
+
+@pytest.mark.parametrize("g,n_round", [(synth.LIKE_2B, 5), (synth.LIKE_27B, 2)])
+@pytest.mark.parametrize("mode", ["tree", "window_log", "tree_log"])
+def test_sliced_trees_and_logged_windows_equal_unsliced_bitwise(mode, g, n_round):
+    """Trees and logged windows of few streams split each head's state rows
+    over a cluster (a lone 2B-like stream: 8 slices; a lone 27B-like one: 2),
+    as recording windows do.  A stream alone equals the same stream in an
+    unsliced round, bit for bit: y, tails, and the recorded states or the
+    logs."""
+    tree = mode != "window_log"
+    c = Case(g, [16, 11] + [16] * (n_round - 2), seed=227, n_slots=n_round + 1, tree=tree)
+
+    def run(case):
+        d, w = case.dims_gpu(), case.dev_weights()
+        cache, rows = case.dev_cache(), case.dev_rows()
+        slot, rp = dev(case.slots), dev(case.row_ptr)
+        if mode == "tree":
+            rs, rt = case.dev_records()
+            gdn.tree(d, w, cache, slot, rp, dev(case.parent), rows, rs, rt)
+            extra = [rs.cpu().numpy().view(np.uint32)]
+        else:
+            la, lu, lk, rt = _logs(case)
+            if mode == "tree_log":
+                gdn.tree_log(d, w, cache, slot, rp, dev(case.parent), rows, la, lu, lk, rt)
+            else:
+                gdn.window_log(d, w, cache, slot, rp, rows, la, lu, lk, rt)
+            extra = [x.cpu().numpy().view(np.uint32) for x in (la, lu, lk)]
+        assert gdn.get_device_error() == 0
+        return [host_bits(rows["y"]), host_bits(rt)] + extra
+
+    full = run(c)
+    for s in range(2):
+        lo, hi = c.stream_rows(s)
+        solo = Case(g, [hi - lo], seed=227, slots=[0], tree=tree)
+        solo.w = c.w
+        sl = c.slots[s]
+        solo.cache = {"state": c.cache["state"][sl:sl + 1], "tail": c.cache["tail"][sl:sl + 1]}
+        solo.rows = {k: v[lo:hi] for k, v in c.rows.items()}
+        if tree:
+            solo.parent = c.parent[lo:hi].copy()
+        alone = run(solo)
+        for i, (a, b) in enumerate(zip(alone, full)):
+            assert np.array_equal(a[:hi - lo], b[lo:hi]), f"stream {s}: output {i} differs"
