@@ -158,6 +158,10 @@ int gdn_step(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
  *              newest conv inputs along the row's branch, oldest first)
  * Row r of y, rec_state and rec_tail equals, bit for bit, what gdn_step
  * would produce for that row from the state and tail it follows.
+ * Launch: one CTA per (value head, stream); when those would leave SMs
+ * idle (few streams), each head's state rows are split over a cluster of
+ * 2 to 8 CTAs, with the same bits.  d >= 64 without that split stages the
+ * inputs with TMA (three tensor maps encoded on the host per call).
  */
 int gdn_window(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
                const int32_t *slot, const int32_t *row_ptr, int32_t n_streams,
