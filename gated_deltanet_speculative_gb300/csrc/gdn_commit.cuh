@@ -152,27 +152,45 @@ __global__ void __launch_bounds__(kReplayThreads) gdn_commit_replay_kernel(const
         cp_async16(&ks[t][c4], p.log_k + (r * p.Hk + kh) * D + c4);
     }
     if (tid < n) as[tid] = __ldg(p.log_a + (size_t)row_of(tid) * p.Hv + h);
-    float S[RPW][CPL];
+    // The tile streams through registers in blocks of RB rows a warp, the
+    // next block's loads in flight while the current one is replayed: each
+    // element's updates depend on that element alone, so the blocks can be
+    // taken in any order and the arithmetic is that of the whole tile.
+    constexpr int RB = RPW < 4 ? RPW : 4, NB = RPW / RB;
     float *tile = p.state + ((size_t)sl * p.Hv + h) * D * D;
+    float cur[RB][CPL], nxt[RB][CPL];
+    auto load_block = [&](float (&x)[RB][CPL], int b) {
 #pragma unroll
-    for (int r = 0; r < RPW; ++r)
+        for (int r = 0; r < RB; ++r)
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) S[r][c] = tile[(size_t)(warp * RPW + r) * D + lane * CPL + c];
+            for (int c = 0; c < CPL; ++c) x[r][c] = tile[(size_t)(warp * RPW + b * RB + r) * D + lane * CPL + c];
+    };
+    load_block(cur, 0);
     cp_async_wait_all();
     __syncthreads();
-    for (int t = 0; t < n; ++t) {
-        const float a = as[t];
 #pragma unroll
-        for (int r = 0; r < RPW; ++r) {
-            const float ur = us[t][warp * RPW + r];
+    for (int b = 0; b < NB; ++b) {
+        if (b + 1 < NB) load_block(nxt, b + 1);
+        for (int t = 0; t < n; ++t) {
+            const float a = as[t];
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) S[r][c] = __fmaf_rn(ur, ks[t][lane * CPL + c], __fmul_rn(a, S[r][c]));
+            for (int r = 0; r < RB; ++r) {
+                const float ur = us[t][warp * RPW + b * RB + r];
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) cur[r][c] = __fmaf_rn(ur, ks[t][lane * CPL + c], __fmul_rn(a, cur[r][c]));
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) tile[(size_t)(warp * RPW + b * RB + r) * D + lane * CPL + c] = cur[r][c];
+        if (b + 1 < NB) {
+#pragma unroll
+            for (int r = 0; r < RB; ++r)
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) cur[r][c] = nxt[r][c];
         }
     }
-#pragma unroll
-    for (int r = 0; r < RPW; ++r)
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) tile[(size_t)(warp * RPW + r) * D + lane * CPL + c] = S[r][c];
     // this CTA's share of the kept row's tail, in 16-byte units
     const size_t units = (size_t)3 * p.CH / 8;
     const size_t lo = units * h / p.Hv, hi = units * (h + 1) / p.Hv;
