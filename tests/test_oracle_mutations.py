@@ -32,6 +32,9 @@ MUTATIONS = [
     ("record: tail shifted by one", "memcpy(rec_tail + ((size_t)t * 3 + m) * CH, hist[m + 1], sizeof(uint16_t) * CH);",
      "memcpy(rec_tail + ((size_t)t * 3 + m) * CH, hist[m], sizeof(uint16_t) * CH);"),
     ("tree: parents ignored", "if (node >= 0) node = parent ? parent[node] : node - 1;", "if (node >= 0) node = node - 1;"),
+    ("rmsnorm: z read at the key head", "zz[i] = bf16_value(z[((size_t)t * Hv + h) * dv + i]);",
+     "zz[i] = bf16_value(z[((size_t)t * Hv + kh) * dv + i]);"),
+    ("rmsnorm: w_norm reversed", "wn[i] = bf16_value(norm_w[i]);", "wn[i] = bf16_value(norm_w[dv - 1 - i]);"),
     ("chunked: Gamma exponent sign", "double m = bc[t] * exp(Gc[t] - Gc[s]) * A[t * C + s];",
      "double m = bc[t] * exp(Gc[s] - Gc[t]) * A[t * C + s];"),
     ("chunked: state term of U dropped", "U[(size_t)t * dv + i] -= acc;", "U[(size_t)t * dv + i] -= 0.0 * acc;"),
@@ -52,6 +55,7 @@ PINS = [
     lambda: pins.test_conv_past_taps_follow_the_tail(0),
     lambda: pins.test_conv_past_taps_follow_the_tail(2),
     pins.test_grouped_head_mapping,
+    pins.test_layer_output_is_gated_rmsnorm_of_its_own_head,
     pins.test_layer_recurrence_matches_explicit_matrix_chain,
     pins.test_tree_node_equals_chain_along_its_path,
     lambda: pins.test_chunked_form_equals_sequential_recurrence(37, 4),

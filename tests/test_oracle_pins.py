@@ -254,6 +254,29 @@ def test_layer_recurrence_matches_explicit_matrix_chain():
             np.testing.assert_allclose(out["rec_state"][t, h], S, atol=1e-12)
 
 
+def test_layer_output_is_gated_rmsnorm_of_its_own_head():
+    """y[t, h] is assembled from head h's own o_t = S_t q_t, z[t, h] and the
+    shared w_norm element by element: recomputed with numpy from the state
+    and q the oracle reports, y = o / sqrt(mean(o^2) + eps) * w_norm * SiLU(z)
+    with SiLU from scipy.special.expit.  Hk = 2, Hv = 6 puts value heads and
+    key heads at different indices, and a random w_norm is not symmetric, so
+    a z read at the key head's index or a reversed w_norm fails here."""
+    g = synth.Geometry(2, 6, 8, 8)
+    n = 6
+    w, s0, t0, r = _layer_inputs(g, n, 57)
+    dims = _dims(g)
+    out = oracle.gdn_rows(dims, w, s0, t0, r["mixed"], r["z"], r["a"], r["b"], extras=True)
+    z = oracle.bf16_to_f64(r["z"])
+    wn = oracle.bf16_to_f64(w["norm_w"])
+    assert not np.allclose(wn, wn[::-1])
+    for t in range(n):
+        for h in range(g.n_v_heads):
+            o = out["rec_state"][t, h] @ out["q"][t, h]
+            zz = z[t, h]
+            y = o / np.sqrt(np.mean(o * o) + dims.eps_rms) * wn * (zz * expit(zz))
+            np.testing.assert_allclose(out["y"][t, h], y, rtol=0, atol=1e-12 * max(1.0, np.abs(y).max()))
+
+
 # ---- structural invariants of the verify path ---------------------------
 
 def test_window_rows_equal_one_row_steps():
