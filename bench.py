@@ -230,7 +230,7 @@ def run_ours(args, rank, world, local_rank):
 
     def step():
         gdn.window(d, dw, dc, slot_t, rp_t, dr, rec_state, rec_tail, stream)
-        gdn.commit(d, dc, slot_t, keep_t, rec_state, rec_tail, stream)
+        gdn.commit(d, dc, slot_t, rp_t, keep_t, rec_state, rec_tail, stream)
 
     def barrier():
         if world > 1:
@@ -254,7 +254,7 @@ def run_ours(args, rank, world, local_rank):
         ev[i][0].record(stream)
         gdn.window(d, dw, dc, slot_t, rp_t, dr, rec_state, rec_tail, stream)
         ev[i][1].record(stream)
-        gdn.commit(d, dc, slot_t, keep_t, rec_state, rec_tail, stream)
+        gdn.commit(d, dc, slot_t, rp_t, keep_t, rec_state, rec_tail, stream)
         ev[i][2].record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -314,7 +314,7 @@ def run_ours(args, rank, world, local_rank):
         stream.wait_event(ev_in[b])
         gdn.window(d, dw, dc, slot_t, rp_t, bufs[b], rec_state, rec_tail, stream)
         ev_win[b].record(stream)
-        gdn.commit(d, dc, slot_t, keeps[b], rec_state, rec_tail, stream)
+        gdn.commit(d, dc, slot_t, rp_t, keeps[b], rec_state, rec_tail, stream)
         ev_done[b].record(stream)
         d2h_s.wait_event(ev_win[b])
         with torch.cuda.stream(d2h_s):
@@ -374,7 +374,10 @@ def run_ours(args, rank, world, local_rank):
                      "peak_source": f"{peak_src} (hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": wbytes,
                      "window_ms_per_launch": win_avg,
-                     "traffic": ncu_traffic("gdn_window_verify_16x16.md")},
+                     "traffic": ncu_traffic("gdn_window_verify_16x16.md"),
+                     "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum of one launch, read from the "
+                                       "committed ncu summary profiles/gdn_window_verify_16x16.md (not measured "
+                                       "in this run); null when the kernel's sources changed since that capture"},
         "commit": {"ms_per_launch": statistics.mean(com_ms), "bytes_per_launch": commit_bytes(g, n_committed),
                    "gbs": commit_bytes(g, n_committed) / (statistics.mean(com_ms) * 1e-3) / 1e9},
         "e2e": {"value": world * R / (e2e_ms * 1e-3), "unit": "rows/s", "ms_per_step": e2e_ms,
@@ -443,7 +446,7 @@ def run_extra(dev, stream, flush, reps=20, only=None):
         pass
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     bf16 = float(peaks.get("bf16_tflops", 1950.0))
-    fp32_alu = 152 * 128 * 2 * 2.07e9 / 1e12   # FFMA peak at the max SM clock, TFLOP/s
+    bf16_src = "measured bf16_tflops (burst)" if "bf16_tflops" in peaks else "fallback 1.95 PFLOP/s"
 
     if only in (None, "tree"):
         out["tree_round_16x16"] = _extra_tree(dev, stream, flush, reps, hbm)
@@ -454,7 +457,7 @@ def run_extra(dev, stream, flush, reps=20, only=None):
     if only in (None, "decode"):
         out["decode_24_layers_2b_like"] = _extra_decode(dev, stream, flush, reps, hbm)
     if only in (None, "prefill"):
-        out["prefill_27b_like"] = _extra_prefill(dev, stream, flush, reps, hbm, bf16, fp32_alu)
+        out["prefill_27b_like"] = _extra_prefill(dev, stream, flush, reps, hbm, bf16, bf16_src)
     return out
 
 
@@ -555,7 +558,7 @@ def _extra_logged_tree(dev, stream, flush, reps, hbm):
 
     def recorded():
         gdn.tree(d, dw, dc, t["slot"], t["rp"], t["par"], dr, rs, rt, stream)
-        gdn.commit(d, dc, t["slot"], t["keep_t"], rs, rt, stream)
+        gdn.commit(d, dc, t["slot"], t["rp"], t["keep_t"], rs, rt, stream)
 
     ms = _timed(logged, reps, stream, flush)
     ms_w = _timed(lambda: gdn.tree_log(d, dw, dc, t["slot"], t["rp"], t["par"], dr, la, lu, lk, rt, stream), reps,
@@ -682,7 +685,7 @@ def _extra_decode(dev, stream, flush, reps, hbm):
     return dec
 
 
-def _extra_prefill(dev, stream, flush, reps, hbm, bf16, fp32_alu):
+def _extra_prefill(dev, stream, flush, reps, hbm, bf16, bf16_src):
     """Prefill: (i) one 4722-token prompt; (ii) 512/1024/2048/4096 in one pass."""
     import torch
     import gated_deltanet_speculative_gb300 as gdn
@@ -716,7 +719,8 @@ def _extra_prefill(dev, stream, flush, reps, hbm, bf16, fp32_alu):
         by = prefill_bytes(g, T, S)
         pre[name] = {"ms": ms, "tokens_per_s": T / (ms * 1e-3), "algorithmic_tflops": fl / (ms * 1e-3) / 1e12,
                      "frac_bf16_tensor_peak": fl / (ms * 1e-3) / 1e12 / bf16,
-                     "frac_fp32_alu_peak": fl / (ms * 1e-3) / 1e12 / fp32_alu,
+                     "bf16_peak_tflops": bf16,
+                     "bf16_peak_source": bf16_src + ": each call is a sub-millisecond burst",
                      "algorithmic_gbs": by / (ms * 1e-3) / 1e9, "frac_hbm": by / (ms * 1e-3) / 1e9 / hbm,
                      "algorithmic_flop": fl, "algorithmic_bytes": by,
                      "note": "d=128, C=64: contractions on tcgen05 bf16 tensor cores as 3-pass hi/lo splits (3x the algorithmic MMA work); time includes a state reset copy"}

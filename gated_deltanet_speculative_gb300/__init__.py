@@ -12,4 +12,5 @@ from . import synth  # noqa: F401
 from ._binding import (Dims, GdnError, MAX_WINDOW, PREFILL_CHUNK, PREFILL_NOALLOC_SCRATCH_BYTES,  # noqa: F401
                        commit, commit_replay, commit_replay_tree, debug_wait_timeout, get_device_error,
                        library_path, load, prefill,
-                       prefill_noalloc, prefill_workspace_size, step, tree, tree_log, window, window_log)
+                       prefill_noalloc, prefill_workspace, prefill_workspace_size, step, tree, tree_log, window,
+                       window_log)

@@ -59,10 +59,11 @@ _SIGS = {
                    ctypes.POINTER(c_rows), _P, _P, _P],
     "gdn_tree": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _P, _I, _I,
                  ctypes.POINTER(c_rows), _P, _P, _P],
-    "gdn_commit": [ctypes.POINTER(c_dims), ctypes.POINTER(c_cache), _P, _P, _I, _I, _P, _P, _P],
+    "gdn_commit": [ctypes.POINTER(c_dims), ctypes.POINTER(c_cache), _P, _P, _P, _I, _I, _P, _P, _P],
     "gdn_prefill": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _I, _I,
                     ctypes.POINTER(c_rows), _I, _P, ctypes.c_size_t, _P],
     "gdn_prefill_workspace_size": [ctypes.POINTER(c_dims), _I, _I, _I],
+    "gdn_prefill_workspace": [ctypes.POINTER(c_dims), _I, _I, _I],
     "gdn_prefill_noalloc": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _I,
                             _I, ctypes.POINTER(c_rows), _I, _P],
     "gdn_window_log": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _I, _I,
@@ -95,7 +96,8 @@ def load(build_if_missing: bool = True):
                 fn = getattr(lib, name)
                 fn.argtypes = argtypes
                 fn.restype = {"gdn_status_string": ctypes.c_char_p,
-                              "gdn_prefill_workspace_size": ctypes.c_size_t}.get(name, ctypes.c_int)
+                              "gdn_prefill_workspace_size": ctypes.c_size_t,
+                              "gdn_prefill_workspace": ctypes.c_size_t}.get(name, ctypes.c_int)
             _lib = lib
     return _lib
 
@@ -213,18 +215,20 @@ def tree(dims: Dims, weights: dict, cache: dict, slot, row_ptr, parent, rows: di
                                     _ptr(rec_tail), _stream_ptr(stream)))
 
 
-def commit(dims: Dims, cache: dict, slot, keep_row, rec_state, rec_tail, stream=None):
-    """Slot s takes recorded row keep_row[s] (-1: slot untouched)."""
+def commit(dims: Dims, cache: dict, slot, row_ptr, keep_row, rec_state, rec_tail, stream=None):
+    """Slot s takes recorded row keep_row[s], one of its own rows
+    [row_ptr[s], row_ptr[s+1]) (-1: slot untouched)."""
     lib = load()
     _need(slot, "slot", torch.int32)
     S = slot.numel()
+    _need(row_ptr, "row_ptr", torch.int32, (S + 1,))
     _need(keep_row, "keep_row", torch.int32, (S,))
     cc = _cache(dims, cache)
     R = rec_state.shape[0]
     _need(rec_state, "rec_state", torch.float32, (R, dims.n_v_heads, dims.d_v, dims.d_k))
     _need(rec_tail, "rec_tail", torch.bfloat16, (R, 3, dims.channels))
-    _check("gdn_commit", lib.gdn_commit(ctypes.byref(dims.c()), ctypes.byref(cc), _ptr(slot), _ptr(keep_row), S, R,
-                                        _ptr(rec_state), _ptr(rec_tail), _stream_ptr(stream)))
+    _check("gdn_commit", lib.gdn_commit(ctypes.byref(dims.c()), ctypes.byref(cc), _ptr(slot), _ptr(row_ptr),
+                                        _ptr(keep_row), S, R, _ptr(rec_state), _ptr(rec_tail), _stream_ptr(stream)))
 
 
 def window_log(dims: Dims, weights: dict, cache: dict, slot, row_ptr, rows: dict, log_a, log_u, log_k, rec_tail,
@@ -316,6 +320,11 @@ PREFILL_CHUNK = 64
 def prefill_workspace_size(dims: Dims, n_seqs: int, n_tokens: int, chunk: int = PREFILL_CHUNK) -> int:
     """Bytes of scratch gdn_prefill needs (0 for invalid sizes)."""
     return int(load().gdn_prefill_workspace_size(ctypes.byref(dims.c()), int(n_seqs), int(n_tokens), int(chunk)))
+
+
+def prefill_workspace(dims: Dims, n_seqs: int, n_tokens: int, chunk: int = PREFILL_CHUNK) -> int:
+    """The same size through the header's shorter name."""
+    return int(load().gdn_prefill_workspace(ctypes.byref(dims.c()), int(n_seqs), int(n_tokens), int(chunk)))
 
 
 def prefill(dims: Dims, weights: dict, cache: dict, slot, cu_seqlens, rows: dict, workspace, chunk: int = PREFILL_CHUNK,

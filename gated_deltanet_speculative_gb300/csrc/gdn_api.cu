@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "gdn_commit.cuh"
+#include "gdn_context.h"
 #include "gdn_launch.h"
 #include "gdn_prefill_launch.h"
 
@@ -19,19 +20,17 @@ __device__ int g_device_error;   // OR of GDN_DERR_* bits raised by the kernels
 
 constexpr int kMaxDevices = 64;
 
-// Per-device address of g_device_error, looked up once per device.
+// Per-device address of g_device_error, looked up on a device's first call
+// and again whenever the current context has changed since.
 int *error_word() {
-    static int *addr[kMaxDevices] = {};
+    static void *addr[kMaxDevices] = {};
+    static unsigned long long ctx[kMaxDevices] = {};
     static std::mutex mu;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *a = nullptr;
-        if (cudaGetSymbolAddress(&a, g_device_error) != cudaSuccess) return nullptr;
-        addr[dev] = static_cast<int *>(a);
-    }
-    return addr[dev];
+    void *a = nullptr;
+    if (gdn::symbol_address(g_device_error, &a, &addr[dev], &ctx[dev], mu) != cudaSuccess) return nullptr;
+    return static_cast<int *>(a);
 }
 
 bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
@@ -266,10 +265,10 @@ int replay_entry(const gdn_dims *dims, const gdn_cache *cache, const int32_t *sl
 }  // namespace
 
 namespace gdn {
-// gdn_prefill with a choice of launch plan (see launch_prefill).
-int prefill_entry(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
-                  const int32_t *cu_seqlens, int32_t n_seqs, int32_t n_tokens, const gdn_rows *rows, int32_t chunk,
-                  void *workspace, size_t workspace_bytes, void *stream, bool pipelined) {
+// gdn_prefill's host checks of everything but the workspace.
+int prefill_validate(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
+                     const int32_t *cu_seqlens, int32_t n_seqs, int32_t n_tokens, const gdn_rows *rows,
+                     int32_t chunk) {
     GDN_TRY(check_dims(dims));
     GDN_TRY(check_weights(w));
     GDN_TRY(check_cache(cache));
@@ -278,11 +277,19 @@ int prefill_entry(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *c
     if (n_seqs <= 0 || n_seqs > 65535 || n_tokens <= 0 || n_tokens > (1 << 22) || chunk != gdn::kPrefillChunk)
         return GDN_EINVAL;
     if (!aligned(slot, 4) || !aligned(cu_seqlens, 4)) return GDN_EALIGN;
+    if ((size_t)n_tokens / chunk + (size_t)n_seqs > 65535) return GDN_EINVAL;
+    return GDN_OK;
+}
+
+// gdn_prefill with a choice of launch plan (see launch_prefill).
+int prefill_entry(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
+                  const int32_t *cu_seqlens, int32_t n_seqs, int32_t n_tokens, const gdn_rows *rows, int32_t chunk,
+                  void *workspace, size_t workspace_bytes, void *stream, bool pipelined) {
+    GDN_TRY(prefill_validate(dims, w, cache, slot, cu_seqlens, n_seqs, n_tokens, rows, chunk));
     const size_t need = gdn_prefill_workspace_size(dims, n_seqs, n_tokens, chunk);
     if (!workspace || workspace_bytes < need) return GDN_EWORKSPACE;
     if (!aligned(workspace, 16)) return GDN_EALIGN;
     const size_t max_chunks = (size_t)n_tokens / chunk + (size_t)n_seqs;
-    if (max_chunks > 65535) return GDN_EINVAL;
     int *err = error_word();
     if (!err) return GDN_ECUDA;
     gdn::PrefillParams p = {};
@@ -341,13 +348,15 @@ int gdn_tree(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
                       rec_tail, stream);
 }
 
-int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot, const int32_t *keep_row,
-               int32_t n_streams, int32_t n_rows, const float *rec_state, const void *rec_tail, void *stream) {
+int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot, const int32_t *row_ptr,
+               const int32_t *keep_row, int32_t n_streams, int32_t n_rows, const float *rec_state,
+               const void *rec_tail, void *stream) {
     GDN_TRY(check_dims(dims));
     GDN_TRY(check_cache(cache));
-    if (!slot || !keep_row || !rec_state || !rec_tail) return GDN_ENULL;
+    if (!slot || !row_ptr || !keep_row || !rec_state || !rec_tail) return GDN_ENULL;
     if (n_streams <= 0 || n_streams > 65535 || n_rows <= 0) return GDN_EINVAL;
-    if (!aligned(slot, 4) || !aligned(keep_row, 4) || !aligned(rec_state, 16) || !aligned(rec_tail, 16))
+    if (!aligned(slot, 4) || !aligned(row_ptr, 4) || !aligned(keep_row, 4) || !aligned(rec_state, 16) ||
+        !aligned(rec_tail, 16))
         return GDN_EALIGN;
     int *err = error_word();
     if (!err) return GDN_ECUDA;
@@ -359,6 +368,7 @@ int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot
     p.tail = static_cast<uint16_t *>(cache->tail);
     p.n_slots = cache->n_slots;
     p.slot = slot;
+    p.row_ptr = row_ptr;
     p.keep_row = keep_row;
     p.n_rows = n_rows;
     p.rec_state = rec_state;
@@ -377,6 +387,10 @@ size_t gdn_prefill_workspace_size(const gdn_dims *dims, int32_t n_seqs, int32_t 
     const size_t floats = max_chunks * dims->n_v_heads * gdn::prefill_chunk_floats(dims->d_k) +
                           (size_t)n_tokens * dims->n_v_heads * dims->d_v;
     return floats * sizeof(float);
+}
+
+size_t gdn_prefill_workspace(const gdn_dims *dims, int32_t n_seqs, int32_t n_tokens, int32_t chunk) {
+    return gdn_prefill_workspace_size(dims, n_seqs, n_tokens, chunk);
 }
 
 int gdn_prefill(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,

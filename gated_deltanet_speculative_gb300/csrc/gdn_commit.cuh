@@ -19,6 +19,7 @@ struct CommitParams {
     uint16_t *tail;           // bf16 [n_slots, 3, CH]
     int n_slots;
     const int *slot;          // [S]
+    const int *row_ptr;       // [S + 1] each stream's packed rows
     const int *keep_row;      // [S]
     int n_rows;
     const float *rec_state;   // [R, Hv, D, D]
@@ -32,10 +33,13 @@ __global__ void __launch_bounds__(kCommitThreads) gdn_commit_kernel(const Commit
     const int h = blockIdx.x, s = blockIdx.y;
     const int kr = p.keep_row[s];
     if (kr == -1) return;   // nothing accepted: the slot keeps its bits
-    const int sl = p.slot[s];
-    if (kr < -1 || kr >= p.n_rows || sl < 0 || sl >= p.n_slots) {
-        if (h == 0 && threadIdx.x == 0)
-            raise_error(p.err, (sl < 0 || sl >= p.n_slots) ? GDN_DERR_SLOT : GDN_DERR_KEEP);
+    const int sl = p.slot[s], r0 = p.row_ptr[s], r1 = p.row_ptr[s + 1];
+    // the kept row must be one of the stream's own rows (a stream keeps only
+    // its own accepted path)
+    const bool bad_slot = sl < 0 || sl >= p.n_slots;
+    const bool bad_keep = r0 < 0 || r1 > p.n_rows || kr < r0 || kr >= r1;
+    if (bad_slot || bad_keep) {
+        if (h == 0 && threadIdx.x == 0) raise_error(p.err, bad_slot ? GDN_DERR_SLOT : GDN_DERR_KEEP);
         return;
     }
     const size_t tile4 = (size_t)p.D * p.D / 4;

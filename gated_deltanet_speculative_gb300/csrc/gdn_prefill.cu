@@ -150,8 +150,7 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
     PrefillParams p = p0;
     p.c_lo = 0;
     p.c_hi = p.max_chunks;
-    const size_t items = (size_t)p.n_tokens * p.Hv;
-    const unsigned norm_blocks = (unsigned)((items + kNormThreads / 32 - 1) / (kNormThreads / 32));
+    const dim3 norm_grid(p.Hv, p.max_chunks);   // every chunk of the pass
     cudaError_t e;
     if constexpr (TC) {
         e = cudaFuncSetAttribute(gdn_prefill_prep_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -170,7 +169,7 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
             const int items = (p.c_hi - p.c_lo) * p.Hk;
             gdn_prefill_prep_tc_kernel<C><<<items < n_sm ? items : n_sm, kPrepTcThreads, kPrepTcSmem, st>>>(p);
             gdn_prefill_scan_tc_kernel<C><<<dim3(p.Hv, p.n_seqs), kScanTcThreads, kScanTcSmem, st>>>(p);
-            gdn_prefill_norm_kernel<D><<<norm_blocks, kNormThreads, 0, st>>>(p);
+            gdn_prefill_norm_chunks_kernel<D, C><<<norm_grid, kNormThreads, 0, st>>>(p);
             return cudaGetLastError();
         }
         std::lock_guard<std::mutex> lock(g_side_mu);
@@ -230,7 +229,7 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
                                  (int)Scan::kBytes);
         if (e != cudaSuccess) return e;
         gdn_prefill_scan_kernel<D, C, DS, NT><<<dim3(D / DS, p.Hv, p.n_seqs), NT, Scan::kBytes, st>>>(p);
-        gdn_prefill_norm_kernel<D><<<norm_blocks, kNormThreads, 0, st>>>(p);
+        gdn_prefill_norm_chunks_kernel<D, C><<<norm_grid, kNormThreads, 0, st>>>(p);
         return cudaGetLastError();
     }
 }

@@ -1511,16 +1511,12 @@ __device__ __forceinline__ void norm_item(const PrefillParams &p, size_t item, i
     }
 }
 
-// Every (token, head) of the pass.
-template <int D>
-__global__ void __launch_bounds__(kNormThreads) gdn_prefill_norm_kernel(const PrefillParams p) {
-    const size_t item = (size_t)blockIdx.x * (kNormThreads / 32) + (threadIdx.x >> 5);
-    if (item >= (size_t)p.n_tokens * p.Hv) return;
-    norm_item<D>(p, item, threadIdx.x & 31);
-}
-
 // The tokens of global chunks [c_lo, c_hi): one CTA per (value head, chunk),
 // so a pipelined pass normalises each chunk group right after its scan.
+// Only tokens of a sequence that the scan ran are normalised: tokens outside
+// every sequence (before cu_seqlens[0] or after the last entry) and the
+// tokens of a sequence skipped for a bad slot or bad cu_seqlens have no O,
+// and their y is left as it was.
 template <int D, int C>
 __global__ void __launch_bounds__(kNormThreads) gdn_prefill_norm_chunks_kernel(const PrefillParams p) {
     __shared__ int info[2];
@@ -1528,7 +1524,8 @@ __global__ void __launch_bounds__(kNormThreads) gdn_prefill_norm_chunks_kernel(c
     if (threadIdx.x == 0) {
         int seq = -1, start = 0, n = 0, seq_start = 0, bad = 0;
         const bool ok = locate_chunk(p, C, gc, seq, start, n, seq_start, bad);
-        info[0] = (ok && !bad) ? n : 0;
+        const int sl = ok ? __ldg(p.slot + seq) : -1;
+        info[0] = (ok && !bad && sl >= 0 && sl < p.n_slots) ? n : 0;
         info[1] = start;
     }
     __syncthreads();

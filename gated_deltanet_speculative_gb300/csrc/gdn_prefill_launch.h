@@ -22,6 +22,12 @@ cudaError_t launch_prefill(int D, const PrefillParams &p, cudaStream_t st, bool 
 // GDN_DERR_TIMEOUT in *err and returns.  Nothing is in flight meanwhile.
 cudaError_t launch_wait_selftest(unsigned polls, int *err, cudaStream_t st);
 
+// gdn_prefill's host checks of every argument except the workspace (a
+// GDN_* status; nothing is enqueued and no CUDA call is made).
+int prefill_validate(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
+                     const int32_t *cu_seqlens, int32_t n_seqs, int32_t n_tokens, const gdn_rows *rows,
+                     int32_t chunk);
+
 // gdn_prefill's validation and launch with the plan chosen by the caller
 // (gdn_prefill: pipelined; gdn_prefill_noalloc: everything on `stream`).
 int prefill_entry(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,

@@ -17,17 +17,21 @@
 //  - every call uses the same array.  Two calls whose work overlaps on the
 //    GPU (different streams, or different host threads on one device) race
 //    on it; serialise them.  Nothing in it has to start at zero: each call's
-//    kernels write every scratch byte before they read it, so the previous
-//    call's leftovers are harmless.
+//    kernels write every scratch byte they later read (the norm reads O only
+//    for tokens of sequences the scan ran), so the previous call's leftovers
+//    are never read.
 //  - the array's name is only a host-side stand-in in host code; its device
-//    address is looked up once per device (with that device current) by the
-//    first call made on that device, so make that first call before any
-//    stream capture begins.
+//    address is looked up with that device current, after the arguments
+//    have passed the host checks, by the first call made on that device, and
+//    again by the first call after the device's context was destroyed and
+//    made anew (cudaDeviceReset).  That lookup may load the module, so make
+//    the first call on a device before any stream capture begins.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "../../include/gdn.h"
+#include "gdn_context.h"
 #include "gdn_prefill_launch.h"
 
 namespace {
@@ -36,20 +40,17 @@ static __device__ __align__(256) unsigned char g_prefill_scratch[GDN_PREFILL_NOA
 
 constexpr int kMaxDevices = 64;
 void *g_scratch_ptr[kMaxDevices];
+unsigned long long g_scratch_ctx[kMaxDevices];
 std::mutex g_scratch_mu;
 
 // Device address of g_prefill_scratch on the current device.
 int scratch_address(void **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ECUDA;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_prefill_scratch) != cudaSuccess || ptr == nullptr) return GDN_ECUDA;
-        g_scratch_ptr[dev] = ptr;
-    }
-    *out = g_scratch_ptr[dev];
-    return GDN_OK;
+    return gdn::symbol_address(g_prefill_scratch, out, &g_scratch_ptr[dev], &g_scratch_ctx[dev], g_scratch_mu) ==
+                   cudaSuccess
+               ? GDN_OK
+               : GDN_ECUDA;
 }
 
 }  // namespace
@@ -57,12 +58,14 @@ int scratch_address(void **out) {
 extern "C" int gdn_prefill_noalloc(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
                                    const int32_t *slot, const int32_t *cu_seqlens, int32_t n_seqs,
                                    int32_t n_tokens, const gdn_rows *rows, int32_t chunk, void *stream) {
-    if (!dims) return GDN_ENULL;
+    // every host check first: a refused call makes no CUDA call at all
+    int rc = gdn::prefill_validate(dims, w, cache, slot, cu_seqlens, n_seqs, n_tokens, rows, chunk);
+    if (rc != GDN_OK) return rc;
     const size_t need = gdn_prefill_workspace_size(dims, n_seqs, n_tokens, chunk);
     if (need == 0) return GDN_EINVAL;
     if (need > (size_t)GDN_PREFILL_NOALLOC_SCRATCH_BYTES) return GDN_EWORKSPACE;
     void *scratch = nullptr;
-    const int rc = scratch_address(&scratch);
+    rc = scratch_address(&scratch);
     if (rc != GDN_OK) return rc;
     // everything on the caller's stream: no side stream or event is made here
     return gdn::prefill_entry(dims, w, cache, slot, cu_seqlens, n_seqs, n_tokens, rows, chunk, scratch,

@@ -35,11 +35,16 @@
  *
  * Conventions shared by every entry point
  *  - Every pointer argument named "device" is a CUDA device pointer owned by
- *    the caller; the library allocates no device memory, frees nothing and
- *    keeps no state between calls except, per device, the address of its
- *    device error word and the SM count, the driver's tensor-map encoder
- *    (looked up once, for the TMA staging of windows and trees), and the
- *    d = 128 prefill's two side streams and four events (see gdn_prefill).
+ *    the caller; the library allocates no device memory at run time, frees
+ *    nothing and keeps no state between calls except, per device: the
+ *    address of its device error word and the SM count; the driver's
+ *    tensor-map encoder (looked up once, for the TMA staging of windows and
+ *    trees); the d = 128 prefill's two side streams and four events (see
+ *    gdn_prefill); and gdn_prefill_noalloc's fixed scratch array, a
+ *    module-scope device array reserved wherever the module is loaded, with
+ *    its cached device address (see gdn_prefill_noalloc).  Cached device
+ *    addresses are looked up again after the device's context is destroyed
+ *    and made anew (cudaDeviceReset).
  *    All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream) and the call returns without synchronising.  Windows
  *    and trees of d >= 64 encode three tensor maps on the host per call
@@ -86,7 +91,7 @@ extern "C" {
 #define GDN_DERR_SLOT      1   /* slot[s] outside [0, n_slots) */
 #define GDN_DERR_ROWS      2   /* row_ptr not monotone, > n_rows, or > 16 rows */
 #define GDN_DERR_PARENT    4   /* parent[i] outside [-1, i) (window-local) */
-#define GDN_DERR_KEEP      8   /* keep_row[s] outside [-1, n_rows) */
+#define GDN_DERR_KEEP      8   /* keep_row[s] not -1 and not one of stream s's rows */
 #define GDN_DERR_SEQLENS  16   /* cu_seqlens not monotone or > n_tokens */
 #define GDN_DERR_TIMEOUT  32   /* a bounded wait inside a kernel gave up */
 
@@ -194,12 +199,17 @@ int gdn_tree(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
  * slot[s]'s state and tail become rec_state[r] and rec_tail[r].
  * keep_row[s] = -1 (nothing accepted) leaves the slot bit-unchanged.
  *   slot       device int32 [n_streams], distinct
- *   keep_row   device int32 [n_streams], each in [-1, n_rows)
+ *   row_ptr    device int32 [n_streams + 1], the row_ptr the window or tree
+ *              call took: stream s may keep only one of its own rows
+ *   keep_row   device int32 [n_streams], each -1 or in
+ *              [row_ptr[s], row_ptr[s+1]); anything else (a row of another
+ *              stream's window, or past n_rows) sets GDN_DERR_KEEP and
+ *              leaves that stream's slot bit-unchanged
  *   rec_state, rec_tail  as written by gdn_window / gdn_tree
  */
 int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot,
-               const int32_t *keep_row, int32_t n_streams, int32_t n_rows,
-               const float *rec_state, const void *rec_tail, void *stream);
+               const int32_t *row_ptr, const int32_t *keep_row, int32_t n_streams,
+               int32_t n_rows, const float *rec_state, const void *rec_tail, void *stream);
 
 /*
  * gdn_prefill -- chunked prompt prefill ([P747] the engine's prompt kernel,
@@ -208,9 +218,11 @@ int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot
  * [cu_seqlens[s], cu_seqlens[s+1]) of `rows`; it starts from slot[s]'s
  * committed state and tail (zero them for a fresh prompt; a nonzero state
  * resumes a kept one) and leaves the state and tail after its last token
- * in the slot.  y is written for every token.  The result equals running
- * the tokens through gdn_step one by one, up to fp32 rounding (the chunked
- * form reorders the sums).
+ * in the slot.  y is written for every token of a sequence; rows of the
+ * packed buffers outside every sequence (before cu_seqlens[0] or from
+ * cu_seqlens[n_seqs] on) are neither read nor written.  The result equals
+ * running the tokens through gdn_step one by one, up to fp32 rounding (the
+ * chunked form reorders the sums).
  *   cu_seqlens  device int32 [n_seqs + 1], non-decreasing, last <= n_tokens;
  *               empty sequences leave their slot untouched
  *   n_tokens    rows in the packed buffers (>= 1, <= 2^22)
@@ -243,6 +255,8 @@ int gdn_prefill(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cac
 /* Bytes of workspace gdn_prefill needs for these sizes (0 if invalid). */
 size_t gdn_prefill_workspace_size(const gdn_dims *dims, int32_t n_seqs, int32_t n_tokens,
                                   int32_t chunk);
+/* The same size under its shorter name (identical result). */
+size_t gdn_prefill_workspace(const gdn_dims *dims, int32_t n_seqs, int32_t n_tokens, int32_t chunk);
 
 /*
  * gdn_prefill_noalloc -- gdn_prefill without a workspace argument, for
@@ -255,11 +269,14 @@ size_t gdn_prefill_workspace_size(const gdn_dims *dims, int32_t n_seqs, int32_t 
  *   the library's module is loaded until the process exits.  Sizes whose
  *   gdn_prefill_workspace_size() exceeds it return GDN_EWORKSPACE before
  *   anything is enqueued; other arguments are validated as in gdn_prefill.
- *   The first call on a device looks up the array's device address (make it
- *   before any stream capture).  All calls share the array: calls whose work
- *   overlaps on the GPU race and must be serialised by the caller.  Nothing
- *   in the array needs to start at zero.  No cudaMalloc or cudaFree is made,
- *   and no stream or event is created: every launch goes on `stream`.
+ *   The first call on a device (and the first after that device's context
+ *   was destroyed and made anew) looks up the array's device address once
+ *   its arguments have passed the host checks; the lookup may load the
+ *   module, so make that call before any stream capture.  All calls share
+ *   the array: calls whose work overlaps on the GPU race and must be
+ *   serialised by the caller.  Nothing in the array needs to start at zero:
+ *   a call reads only what it wrote itself.  No cudaMalloc or cudaFree is
+ *   made, and no stream or event is created: every launch goes on `stream`.
  */
 #define GDN_PREFILL_NOALLOC_SCRATCH_BYTES (64u << 20)
 int gdn_prefill_noalloc(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,

@@ -103,7 +103,8 @@ def test_null_pointers_are_enull():
     assert _window(d, w, c, r, rec_state=None) == -2
     assert lib.gdn_tree(ctypes.byref(d), ctypes.byref(w), ctypes.byref(c), A16, A16, None, 2, 4, ctypes.byref(r),
                         A16, A16, None) == -2
-    assert lib.gdn_commit(ctypes.byref(d), ctypes.byref(c), A16, None, 2, 4, A16, A16, None) == -2
+    assert lib.gdn_commit(ctypes.byref(d), ctypes.byref(c), A16, A16, None, 2, 4, A16, A16, None) == -2
+    assert lib.gdn_commit(ctypes.byref(d), ctypes.byref(c), A16, None, A16, 2, 4, A16, A16, None) == -2
     assert lib.gdn_step(ctypes.byref(d), ctypes.byref(w), ctypes.byref(c), None, 2, ctypes.byref(r), None) == -2
     assert lib.gdn_get_device_error(None, None) == -2
 
@@ -116,7 +117,8 @@ def test_misaligned_pointers_are_ealign():
     d, w, c, r = _args()
     assert _window(d, w, c, r, rec_state=MIS) == -3
     assert _window(d, w, c, r, slot=A16 + 2) == -3
-    assert lib.gdn_commit(ctypes.byref(d), ctypes.byref(c), A16, A16, 2, 4, MIS, A16, None) == -3
+    assert lib.gdn_commit(ctypes.byref(d), ctypes.byref(c), A16, A16, A16, 2, 4, MIS, A16, None) == -3
+    assert lib.gdn_commit(ctypes.byref(d), ctypes.byref(c), A16, A16 + 2, A16, 2, 4, A16, A16, None) == -3
 
 
 def test_binding_checks_shapes_before_calling():

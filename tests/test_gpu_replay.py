@@ -45,7 +45,7 @@ def test_logged_window_and_replay_commit_equal_recorded_path(g):
     cache_r, rows_r = c.dev_cache(), c.dev_rows()
     rs, rt = c.dev_records()
     gdn.window(d, w, cache_r, slot, rp, rows_r, rs, rt)
-    gdn.commit(d, cache_r, slot, dev(keep), rs, rt)
+    gdn.commit(d, cache_r, slot, rp, dev(keep), rs, rt)
     # logged path
     cache_l, rows_l = c.dev_cache(), c.dev_rows()
     la, lu, lk, lt = _logs(c)
@@ -140,7 +140,7 @@ def test_logged_tree_and_replay_commit_equal_recorded_tree(g):
     cache_r, rows_r = c.dev_cache(), c.dev_rows()
     rs, rt = c.dev_records()
     gdn.tree(d, w, cache_r, slot, rp, par, rows_r, rs, rt)
-    gdn.commit(d, cache_r, slot, dev(keep), rs, rt)
+    gdn.commit(d, cache_r, slot, rp, dev(keep), rs, rt)
     cache_l, rows_l = c.dev_cache(), c.dev_rows()
     la, lu, lk, lt = _logs(c)
     gdn.tree_log(d, w, cache_l, slot, rp, par, rows_l, la, lu, lk, lt)
@@ -242,7 +242,7 @@ def test_randomised_rounds_logged_equal_recorded_bitwise(round_id):
         gdn.tree(d, w, cache_r, slot, rp, par, rows_r, rs, rt)
     else:
         gdn.window(d, w, cache_r, slot, rp, rows_r, rs, rt)
-    gdn.commit(d, cache_r, slot, kp, rs, rt)
+    gdn.commit(d, cache_r, slot, rp, kp, rs, rt)
     cache_l, rows_l = c.dev_cache(), c.dev_rows()
     la, lu, lk, lt = _logs(c)
     if tree:

@@ -73,7 +73,7 @@ def test_one_graph_serves_every_round_shape():
 
     def round_():
         gdn.tree(d, w, cache, slot, rp, par, rows, rs, rt)
-        gdn.commit(d, cache, slot, keep, rs, rt)
+        gdn.commit(d, cache, slot, rp, keep, rs, rt)
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -111,7 +111,7 @@ def test_one_graph_serves_every_round_shape():
         e_rows = dict(rows, y=torch.zeros_like(rows["y"]))
         e_rs, e_rt = torch.zeros_like(rs), torch.zeros_like(rt)
         gdn.tree(d, w, e_cache, slot, dev(rp_h), dev(par_h), e_rows, e_rs, e_rt)
-        gdn.commit(d, e_cache, slot, dev(keep_h), e_rs, e_rt)
+        gdn.commit(d, e_cache, slot, dev(rp_h), dev(keep_h), e_rs, e_rt)
         torch.cuda.synchronize()
         n_live = int(rp_h[-1])
         assert np.array_equal(got_y[:n_live], host_bits(e_rows["y"])[:n_live])
@@ -167,7 +167,7 @@ def test_kept_state_saved_to_host_and_restored_resumes_bit_identical():
         rows = c.dev_rows()
         rs, rt = c.dev_records()
         gdn.window(d, w, cache, slot, rp, rows, rs, rt)
-        gdn.commit(d, cache, slot, keep, rs, rt)
+        gdn.commit(d, cache, slot, rp, keep, rs, rt)
         return rows
 
     # uninterrupted: round 1, round 2

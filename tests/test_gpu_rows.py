@@ -255,7 +255,7 @@ def test_commit_accepted_lengths_then_step():
     acc = synth.accepted_lengths(c.S, 16, rng)
     acc[0], acc[1] = 0, 16
     keep = np.where(acc > 0, c.row_ptr[:-1] + acc - 1, -1).astype(np.int32)
-    gdn.commit(d, cache, slot, dev(keep), rs, rt)
+    gdn.commit(d, cache, slot, rp, dev(keep), rs, rt)
     assert gdn.get_device_error() == 0
     st, tl = cache["state"].cpu().numpy(), host_bits(cache["tail"])
     rsn, rtn = rs.cpu().numpy(), host_bits(rt)
@@ -310,9 +310,33 @@ def test_device_index_errors_skip_the_stream():
     assert gdn.get_device_error() & 2
     assert torch.isnan(rs2).all()
     keep = np.array([5, -1], np.int32)   # row 5 does not exist (R = 5 rows -> max index 4)
-    gdn.commit(d, cache, dev(c.slots), dev(keep), rs, rt)
+    gdn.commit(d, cache, dev(c.slots), dev(c.row_ptr), dev(keep), rs, rt)
     assert gdn.get_device_error() & 8
     assert np.array_equal(cache["state"].cpu().numpy(), c.cache["state"])
+
+
+def test_commit_refuses_a_row_of_another_streams_window():
+    """Each stream keeps only its own accepted rows: stream 0 naming row 3
+    (stream 1's first row) and stream 1 naming row 0 (stream 0's) set the
+    keep bit and leave both slots bit-unchanged, while a third stream's
+    valid kept row is committed in the same call."""
+    c = Case(synth.Geometry(2, 4, 64, 64), [3, 2, 4], seed=47, n_slots=5)
+    d = c.dims_gpu()
+    w, cache, rows = c.dev_weights(), c.dev_cache(), c.dev_rows()
+    rs, rt = c.dev_records()
+    gdn.window(d, w, cache, dev(c.slots), dev(c.row_ptr), rows, rs, rt)
+    assert gdn.get_device_error() == 0
+    keep = np.array([3, 0, 7], np.int32)
+    gdn.commit(d, cache, dev(c.slots), dev(c.row_ptr), dev(keep), rs, rt)
+    assert gdn.get_device_error() & 8
+    st, tl = cache["state"].cpu().numpy(), host_bits(cache["tail"])
+    for s in (0, 1):
+        sl = int(c.slots[s])
+        assert np.array_equal(st[sl].view(np.uint32), c.cache["state"][sl].view(np.uint32)), f"slot of stream {s}"
+        assert np.array_equal(tl[sl], c.cache["tail"][sl])
+    sl = int(c.slots[2])
+    assert np.array_equal(st[sl].view(np.uint32), rs[7].cpu().numpy().view(np.uint32))
+    assert np.array_equal(tl[sl], host_bits(rt)[7])
 
 
 @pytest.mark.parametrize("polls", [0, 1000])
