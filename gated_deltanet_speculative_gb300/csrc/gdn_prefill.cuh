@@ -658,7 +658,8 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     constexpr int AU = C + 4;                            // U~^T stage row (16-byte aligned)
     static_assert(C == 64, "the tensor-core block layout is for C = 64");
     static_assert(kPrepTcThreads / 32 * 8 == 2 * C, "the norm step gives each warp eight of the 2C rows");
-    static_assert(3 * C * AS * 4 + 16384 <= 66304 && 128 * AU * 4 <= 66304, "region 2 holds M, P, T, T op / U~^T");
+    static_assert(3 * C * AS * 4 + 16384 <= 66304 && 128 * AU * 4 <= 66304, "region 2 holds M, scratch, T, T op / U~^T");
+    static_assert(2 * D * C * 2 <= 64 * kPrepTcLD * 4, "q's region holds the K^T operand");
     extern __shared__ __align__(1024) unsigned char psm[];
     float *q = reinterpret_cast<float *>(psm + kPtQ);
     float *k = reinterpret_cast<float *>(psm + kPtK);
@@ -666,10 +667,11 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     uint16_t *xqk = reinterpret_cast<uint16_t *>(R2);           // [C+3][2D] q | k inputs
     uint16_t *xv = reinterpret_cast<uint16_t *>(psm + kPtR3);   // [C+3][D] v inputs of the head in hand
     unsigned char *kq_hi = R2, *kq_lo = R2 + 32768;             // [K; Q] operand (after the conv)
+    unsigned char *kt_hi = psm + kPtQ, *kt_lo = kt_hi + 16384;  // K^T [D][C] in q's place, per item
     unsigned char *v_hi = R1, *v_lo = R1 + 16384;               // (b V)^T [D][C]
-    unsigned char *y_hi = R1 + 32768, *y_lo = y_hi + 16384;     // (b gamma K)^T [D][C]
+    unsigned char *tp_hi = R1 + 32768, *tp_lo = tp_hi + 8192;   // T' = T diag(b gamma) [C][C]
     float *A = reinterpret_cast<float *>(R2);                   // M [C][AS]
-    float *QK = A + C * AS;                                     // P [C][AS]
+    float *QK = A + C * AS;                                     // level-2 scratch [C][AS]
     float *T = QK + C * AS;                                     // T [C][AS]
     unsigned char *t_hi = R2 + 49920, *t_lo = t_hi + 8192;      // T operand [C][C]
     float *Wf = reinterpret_cast<float *>(R1);                  // W [C][LD] after MMA 2
@@ -872,8 +874,18 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
             reinterpret_cast<float4 *>(dst)[e] = reinterpret_cast<const float4 *>(src)[e];
         }
     }
+    // K^T (rows j, K = t) in q's place (q is not read again): the A operand
+    // of every head's W^T product.  W = T diag(b gamma) K, so W^T = K^T T'^T
+    // with T' = T diag(b gamma): only the 64 x 64 factor T' is per head.
+    for (int it = tid; it < D * (C / 8); it += kPrepTcThreads) {   // rows j, 8 t
+        const int j = it % D, t0 = (it / D) * 8;
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = k[(t0 + e) * LD + j];
+        store_split8(kt_hi, kt_lo, j, t0, C, x);
+    }
     // (MMA 1 is waited for before the first head's M, P: its v conv and
-    // operands, and the Q copy, overlap it)
+    // operands, the Q copy and K^T overlap it)
     const int quarter = warp & 3, part = warp >> 2;   // 16 warps: lane quarter x column part
 
 #pragma unroll 1
@@ -898,29 +910,17 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
                 store_split8(v_hi, v_lo, e, t0 + h8, C, vb);
             }
         }
-        __syncthreads();   // xv and cw_v consumed
-        if (gi + 1 < p.G) stage_v(h + 1);   // in flight while this head is worked on
-        // (diag(b gamma) K)^T operand and K~^T for the scan
-        for (int it = tid; it < D * (C / 8); it += kPrepTcThreads) {   // rows j, 8 t
-            const int j = it % D, t0 = (it / D) * 8;
-            float y[8], kt[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float kv = k[(t0 + e) * LD + j];
-                y[e] = __fmul_rn(__fmul_rn(beta[t0 + e], eG[t0 + e]), kv);
-                kt[e] = (t0 + e) < n ? __fmul_rn(eGC[t0 + e], kv) : 0.0f;
-            }
-            store_split8(y_hi, y_lo, j, t0, C, y);
-            store_split8(blk + TcBlock::kPK, blk + TcBlock::kPK + TcBlock::kPKLo, C + j, t0, C, kt);
-        }
-        if (gi == 0) {   // MMA 1 done: [A; QK] in TMEM, region 2 free for M, P, T
+        if (gi == 0) {   // MMA 1 done: [A; QK] in TMEM, region 2 free for M, T
             ok = tc::mbar_wait(&bar_mma, ph, kPrepWaitLimit) && ok;
             ph ^= 1;
             tc::fence_after_sync();
         }
+        __syncthreads();   // xv and cw_v consumed; the K^T operand is complete
+        if (gi + 1 < p.G) stage_v(h + 1);   // in flight while this head is worked on
         {   // lane r holds row r of [A; QK]; the four warps on a lane quarter take
-            // 16 columns each and form M = strict_lower(diag(b) Gamma o A) and
-            // P = lower(Gamma o QK) in registers with this head's gates
+            // 16 columns each and form M = strict_lower(diag(b) Gamma o A) (into
+            // shared memory) and P = lower(Gamma o QK) (split and written to the
+            // chunk block from registers) with this head's gates
             const int r = quarter * 32 + lane;
             uint32_t v[16];
             tc::tmem_ld16_nowait(tmem_base + ((uint32_t)(quarter * 32) << 16) + part * 16, v);
@@ -928,118 +928,164 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
             const bool isA = r < C;   // warp-uniform
             const int t = isA ? r : r - C;
             const float Gt = Gc[t], bt = isA ? beta[t] : 1.0f;
-            float *dst = (isA ? A : QK) + t * AS + part * 16;
+            float x[2][8];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const int sc = part * 16 + e;
                 const bool keep = t < n && sc < n && (isA ? sc < t : sc <= t);
                 const float gam = __expf(__fsub_rn(Gt, Gc[sc]));
-                dst[e] = keep ? __fmul_rn(__fmul_rn(bt, gam), __uint_as_float(v[e])) : 0.0f;
+                x[e >> 3][e & 7] = keep ? __fmul_rn(__fmul_rn(bt, gam), __uint_as_float(v[e])) : 0.0f;
+            }
+            if (isA) {
+                float *dst = A + t * AS + part * 16;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) dst[e] = x[e >> 3][e & 7];
+            } else {
+                store_split8(blk + TcBlock::kPK, blk + TcBlock::kPK + TcBlock::kPKLo, t, part * 16, C, x[0]);
+                store_split8(blk + TcBlock::kPK, blk + TcBlock::kPK + TcBlock::kPKLo, t, part * 16 + 8, C, x[1]);
             }
         }
         __syncthreads();
-        // T = (I + M)^-1 by 16 x 16 blocks.  Threads < C invert the four diagonal
-        // blocks by forward substitution (one column each) while the others
-        // write P to the workspace.
+        // T = (I + M)^-1 by 16 x 16 blocks.  Threads < C solve the four diagonal
+        // blocks (one column each), right-looking: once x_kk is final it is
+        // folded into every later row, so each step is one FMA deep (the sums
+        // run in the same order as a row-by-row substitution).  The other
+        // threads meanwhile write K~^T = (diag(gamma_C / gamma) K)^T for the scan.
         if (tid < C) {
             const int b0 = (tid / 16) * 16, c = tid % 16;
             float x[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float acc = r == c ? 1.0f : 0.0f;
+            for (int r = 0; r < 16; ++r) x[r] = r == c ? 1.0f : 0.0f;
 #pragma unroll
-                for (int kk = 0; kk < r; ++kk) acc = __fmaf_rn(-A[(b0 + r) * AS + b0 + kk], x[kk], acc);
-                x[r] = r < c ? 0.0f : acc;
-            }
+            for (int kk = 0; kk < 15; ++kk)
+#pragma unroll
+                for (int r = kk + 1; r < 16; ++r) x[r] = __fmaf_rn(-A[(b0 + r) * AS + b0 + kk], x[kk], x[r]);
 #pragma unroll
             for (int r = 0; r < 16; ++r) T[(b0 + r) * AS + b0 + c] = x[r];
         } else {
-            for (int it = tid - C; it < C * (C / 8); it += kPrepTcThreads - C) {   // P: rows t, 8 columns s
-                const int t = it % C, s0 = (it / C) * 8;
-                float x[8];
+            for (int it = tid - C; it < D * (C / 8); it += kPrepTcThreads - C) {   // K~^T rows j, 8 t
+                const int j = it % D, t0 = (it / D) * 8;
+                float kt[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = QK[t * AS + s0 + e];
-                store_split8(blk + TcBlock::kPK, blk + TcBlock::kPK + TcBlock::kPKLo, t, s0, C, x);
+                for (int e = 0; e < 8; ++e)
+                    kt[e] = (t0 + e) < n ? __fmul_rn(eGC[t0 + e], k[(t0 + e) * LD + j]) : 0.0f;
+                store_split8(blk + TcBlock::kPK, blk + TcBlock::kPK + TcBlock::kPKLo, C + j, t0, C, kt);
             }
-        }
-        for (int i = tid; i < C * C; i += kPrepTcThreads) {   // zero the strictly upper blocks
-            const int t = i / C, s2 = i - t * C;
-            if (s2 / 16 > t / 16) T[t * AS + s2] = 0.0f;
         }
         __syncthreads();
         // Off-diagonal blocks by doubling: for a block lower-triangular
         // L = [L11 0; L21 L22], L^-1 has lower-left block -L22^-1 L21 L11^-1.
         // Level 1 (16-blocks): T10 = -T11 (M10 T00), T32 = -T33 (M32 T22);
         // level 2 (32-blocks): T[32:, :32] = -T[32:, 32:] (M[32:, :32] T[:32, :32]).
-        // The zero upper halves of the diagonal blocks let every sum run full length.
-        float *X = QK;   // scratch once P is out
+        // The diagonal blocks' zero upper halves let the level-1 sums run full
+        // length.  Every sum runs on two or four independent partial sums.
+        // The strictly upper 16-blocks of T are never written; the operands
+        // below take them as zero.
+        float *X = QK;   // scratch (P went straight to the chunk block)
         {
             const int pr = tid >> 8, rr = (tid >> 4) & 15, cc = tid & 15;
             const int bi = 2 * pr + 1, bj = 2 * pr;
             const float *m = A + (bi * 16 + rr) * AS + bj * 16;
             const float *tb = T + (bj * 16) * AS + bj * 16 + cc;
-            float acc = 0.0f;
+            float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) acc = __fmaf_rn(m[kk], tb[kk * AS], acc);
-            X[(pr * 16 + rr) * AS + cc] = acc;
+            for (int kk = 0; kk < 16; kk += 2) {
+                a0 = __fmaf_rn(m[kk], tb[kk * AS], a0);
+                a1 = __fmaf_rn(m[kk + 1], tb[(kk + 1) * AS], a1);
+            }
+            X[(pr * 16 + rr) * AS + cc] = __fadd_rn(a0, a1);
             __syncthreads();
             const float *td = T + (bi * 16 + rr) * AS + bi * 16;
             const float *xc = X + (pr * 16) * AS + cc;
-            acc = 0.0f;
+            a0 = 0.0f;
+            a1 = 0.0f;
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) acc = __fmaf_rn(td[kk], xc[kk * AS], acc);
-            T[(bi * 16 + rr) * AS + bj * 16 + cc] = -acc;
+            for (int kk = 0; kk < 16; kk += 2) {
+                a0 = __fmaf_rn(td[kk], xc[kk * AS], a0);
+                a1 = __fmaf_rn(td[kk + 1], xc[(kk + 1) * AS], a1);
+            }
+            T[(bi * 16 + rr) * AS + bj * 16 + cc] = -__fadd_rn(a0, a1);
         }
         __syncthreads();
         constexpr int H = C / 2;
         constexpr int NU = H * H / kPrepTcThreads;
-        {   // level 2, X = M[32:, :32] T[:32, :32]: warp-uniform column c, lane row r;
-            // T[:32, :32] is lower triangular, so the sum starts at kk = c
-            // (columns c and 31 - c pair up to balance the threads)
-#pragma unroll
-            for (int u = 0; u < NU; ++u) {
-                const int c = u == 0 ? warp : H - 1 - warp, r = lane;
-                const float *m = A + (H + r) * AS;
-                float acc = 0.0f;
-                for (int kk = c; kk < H; ++kk) acc = __fmaf_rn(m[kk], T[kk * AS + c], acc);
-                X[r * AS + c] = acc;
+        {   // level 2, X = M[32:, :32] T[:32, :32]: lane row r, warp-uniform columns
+            // c1 = w and c2 = 31 - w (balancing the threads); T[:32, :32] is lower
+            // triangular, so column c's sum starts at kk = c, and from kk = c2 on
+            // the two sums share their load of M[32 + r][kk]
+            static_assert(NU == 2, "two level-2 outputs per thread");
+            const int c1 = warp, c2 = H - 1 - warp, r = lane;
+            const float *m = A + (H + r) * AS;
+            float a0 = 0.0f, a1 = 0.0f, b0 = 0.0f, b1 = 0.0f;
+            int kk = c1;
+            for (; kk + 1 < c2; kk += 2) {
+                a0 = __fmaf_rn(m[kk], T[kk * AS + c1], a0);
+                a1 = __fmaf_rn(m[kk + 1], T[(kk + 1) * AS + c1], a1);
             }
+            if (kk < c2) {
+                a0 = __fmaf_rn(m[kk], T[kk * AS + c1], a0);
+                ++kk;
+            }
+            for (; kk < H; ++kk) {
+                const float mv = m[kk];
+                a1 = __fmaf_rn(mv, T[kk * AS + c1], a1);
+                b0 = __fmaf_rn(mv, T[kk * AS + c2], b0);
+            }
+            X[r * AS + c1] = __fadd_rn(a0, a1);
+            X[r * AS + c2] = __fadd_rn(b0, b1);
         }
         __syncthreads();
-        {   // T[32:, :32] = -T[32:, 32:] X: warp-uniform row r, lane column c;
-            // T[32:, 32:] is lower triangular, so the sum stops at kk = r
-#pragma unroll
-            for (int u = 0; u < NU; ++u) {
-                const int r = u == 0 ? warp : H - 1 - warp, c = lane;
-                const float *td = T + (H + r) * AS + H;
-                float acc = 0.0f;
-                for (int kk = 0; kk <= r; ++kk) acc = __fmaf_rn(td[kk], X[kk * AS + c], acc);
-                T[(H + r) * AS + c] = -acc;
+        {   // T[32:, :32] = -T[32:, 32:] X: lane column c, warp-uniform rows r1 = w
+            // and r2 = 31 - w; T[32:, 32:] is lower triangular, so row r's sum
+            // stops at kk = r, and up to kk = r1 the two sums share their load
+            // of X[kk][c]
+            const int r1 = warp, r2 = H - 1 - warp, c = lane;
+            const float *t1 = T + (H + r1) * AS + H, *t2 = T + (H + r2) * AS + H;
+            float a0 = 0.0f, a1 = 0.0f, b0 = 0.0f, b1 = 0.0f;
+            int kk = 0;
+            for (; kk <= r1; ++kk) {
+                const float xv = X[kk * AS + c];
+                a0 = __fmaf_rn(t1[kk], xv, a0);
+                b0 = __fmaf_rn(t2[kk], xv, b0);
             }
+            for (; kk + 1 <= r2; kk += 2) {
+                b0 = __fmaf_rn(t2[kk], X[kk * AS + c], b0);
+                b1 = __fmaf_rn(t2[kk + 1], X[(kk + 1) * AS + c], b1);
+            }
+            if (kk <= r2) b0 = __fmaf_rn(t2[kk], X[kk * AS + c], b0);
+            T[(H + r1) * AS + c] = -__fadd_rn(a0, a1);
+            T[(H + r2) * AS + c] = -__fadd_rn(b0, b1);
         }
         __syncthreads();
-        // T operand (rows t, K = s)
+        // operands, rows t, K = s: T (for U~) and T' = T diag(b gamma) (for W),
+        // both from one read of T
         for (int it = tid; it < C * (C / 8); it += kPrepTcThreads) {
             const int t = it % C, s0 = (it / C) * 8;
-            float x[8];
+            float x[8], xp[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = T[t * AS + s0 + e];
+            for (int e = 0; e < 8; ++e) {
+                const int s2 = s0 + e;
+                x[e] = (s2 >> 4) > (t >> 4) ? 0.0f : T[t * AS + s2];
+                xp[e] = __fmul_rn(x[e], __fmul_rn(beta[s2], eG[s2]));
+            }
             store_split8(t_hi, t_lo, t, s0, C, x);
+            store_split8(tp_hi, tp_lo, t, s0, C, xp);
         }
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
 
-        // MMA 2: W^T = (b gamma K)^T T^T (columns 64..127), U~^T = (b V)^T T^T (128..191)
+        // MMA 2: W^T = K^T T'^T (columns 64..127), U~^T = (b V)^T T^T (128..191)
         if (tid == 0) {
             constexpr uint32_t idn = tc::idesc_bf16(128, C);
             const uint32_t th = tc::smem_u32(t_hi), tl = tc::smem_u32(t_lo);
-            const uint32_t yh = tc::smem_u32(y_hi), yl = tc::smem_u32(y_lo);
+            const uint32_t ph_ = tc::smem_u32(tp_hi), pl = tc::smem_u32(tp_lo);
+            const uint32_t kh_ = tc::smem_u32(kt_hi), kl = tc::smem_u32(kt_lo);
             const uint32_t vh = tc::smem_u32(v_hi), vl = tc::smem_u32(v_lo);
-            tc::mma_bf16<C>(tmem_base + 64, yh, th, idn, false);
-            tc::mma_bf16<C>(tmem_base + 64, yh, tl, idn, true);
-            tc::mma_bf16<C>(tmem_base + 64, yl, th, idn, true);
+            tc::mma_bf16<C>(tmem_base + 64, kh_, ph_, idn, false);
+            tc::mma_bf16<C>(tmem_base + 64, kh_, pl, idn, true);
+            tc::mma_bf16<C>(tmem_base + 64, kl, ph_, idn, true);
             tc::mma_bf16<C>(tmem_base + 128, vh, th, idn, false);
             tc::mma_bf16<C>(tmem_base + 128, vh, tl, idn, true);
             tc::mma_bf16<C>(tmem_base + 128, vl, th, idn, true);
@@ -1049,8 +1095,9 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         ph ^= 1;
         tc::fence_after_sync();
         {
-            // lane j of W^T: W[t][j] for every t (warps 0-7); lane i of U~^T: U~^T[i][t] (warps 8-15);
-            // two warps per lane quarter and matrix, 32 columns each, into fp32 stages
+            // lane j of W^T: W[t][j] for every t (warps 0-7); lane i of U~^T:
+            // U~^T[i][t] (warps 8-15); two warps per lane quarter and matrix,
+            // 32 columns each, into fp32 stages
             const int r = quarter * 32 + lane;
             const bool isU = part >= 2;
             const int c0 = (part & 1) * (C / 2);
@@ -1075,13 +1122,6 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
             }
         }
         __syncthreads();
-        for (int it = tid; it < C * (D / 8); it += kPrepTcThreads) {   // -W hi | lo, rows t, 8 columns j
-            const int t = it % C, j0 = (it / C) * 8;
-            const float4 a4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0);
-            const float4 b4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0 + 4);
-            const float x[8] = {-a4.x, -a4.y, -a4.z, -a4.w, -b4.x, -b4.y, -b4.z, -b4.w};
-            store_split8(blk + TcBlock::kWQ, blk + TcBlock::kWQ + TcBlock::kWQLo, t, j0, D, x);
-        }
         {   // U~^T [128][64] fp32, row-major, coalesced 16-byte stores
             float4 *dst = reinterpret_cast<float4 *>(blk + TcBlock::kUt);
             for (int it = tid; it < D * C / 4; it += kPrepTcThreads) {
@@ -1089,9 +1129,16 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
                 dst[it] = *reinterpret_cast<const float4 *>(Uf + i * AU + t4 * 4);
             }
         }
+        for (int it = tid; it < C * (D / 8); it += kPrepTcThreads) {   // -W hi | lo, rows t, 8 columns j
+            const int t = it % C, j0 = (it / C) * 8;
+            const float4 a4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0);
+            const float4 b4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0 + 4);
+            const float x[8] = {-a4.x, -a4.y, -a4.z, -a4.w, -b4.x, -b4.y, -b4.z, -b4.w};
+            store_split8(blk + TcBlock::kWQ, blk + TcBlock::kWQ + TcBlock::kWQLo, t, j0, D, x);
+        }
         if (tid == 0) *reinterpret_cast<float *>(blk + TcBlock::kMisc) = eG[n - 1];
         if (tid < C) reinterpret_cast<float *>(blk + TcBlock::kGam)[tid] = eG[tid];   // gamma_t for O
-        __syncthreads();   // the stages are read; the next head reuses regions 1 and 2
+        __syncthreads();   // the W stage is read; the next head reuses region 1
     }
     }   // items
     if (tid == 0) {
