@@ -100,6 +100,12 @@ __device__ __forceinline__ void prefetch_l2(const void *gmem) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(gmem));
 }
 
+// Ask L2 for `bytes` (a multiple of 16) at a 16-byte aligned global address:
+// one bulk prefetch, nothing waits for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *gmem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void raise_error(int *err, int bits) {
     if (err) atomicOr(err, bits);
 }

@@ -229,13 +229,42 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
     // global access, until it has completed and its writes are visible, so
     // ordering is that of a plain launch; then they let the next step be
     // scheduled in turn.
-    if constexpr (MODE == kStep) {
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    }
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kh = h / p.G;
     const size_t CH = (size_t)p.CH;
+    if constexpr (MODE == kStep) {
+        // While the kernel before this step finishes, ask L2 for what the step
+        // reads that no kernel of the layer loop writes: this slice of the
+        // committed state tile, the head's conv weights and tail, and the
+        // step's input row.  Prefetches only move lines into L2, which every
+        // write reaches, so they cannot change a result.  The slot word is
+        // read on the L2 path (no L1 line survives across the wait) and only
+        // chooses what to prefetch; the step reads it again after the wait.
+        if (warp == 0) {
+            const int sl0 = __ldcg(p.slot + s);
+            if (sl0 >= 0 && sl0 < p.n_slots) {
+                if (lane == 0)
+                    prefetch_l2_bulk(p.state + ((size_t)sl0 * p.Hv + h) * D * D + (size_t)row0 * D,
+                                     (uint32_t)(D / P * D * 4));
+                if (sli == 0 && lane >= 1 && lane <= 9) {   // tail rows x (q, k, v) segments
+                    const int m = (lane - 1) / 3, part = (lane - 1) % 3;
+                    prefetch_l2_bulk(p.tail + ((size_t)sl0 * 3 + m) * CH + channel_of<D>(part, 0, p.Hk, kh, h),
+                                     (uint32_t)(D * 2));
+                }
+            }
+            if (sli == 0 && lane >= 10 && lane <= 12) {   // the input row's q, k, v segments
+                const int part = lane - 10;
+                prefetch_l2_bulk(p.mixed + (size_t)s * CH + channel_of<D>(part, 0, p.Hk, kh, h), (uint32_t)(D * 2));
+            }
+            if (sli == 0 && lane == 13) prefetch_l2_bulk(p.z + ((size_t)s * p.Hv + h) * D, (uint32_t)(D * 2));
+            if (sli == 0 && lane >= 14 && lane <= 16) {   // conv weights of the three segments
+                const int part = lane - 14;
+                prefetch_l2_bulk(p.conv_w + (size_t)channel_of<D>(part, 0, p.Hk, kh, h) * 4, (uint32_t)(D * 8));
+            }
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
     const bool lead = (h % p.G) == 0;    // this CTA writes the q/k channels shared by its key-head group
 
     // ---- a1: the stream's slot and rows (the same few words in every thread)
