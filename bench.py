@@ -3,10 +3,13 @@
 
 Workload (one step): the shared verify round of one GDN layer with 27B-like
 heads (Hk=16 key heads, Hv=48 value heads, d_k=d_v=128): 16 streams x 16-row
-chain windows (256 rows), every row's fp32 state and conv tail recorded
-(gdn_window), then each stream's random accepted length 0..16 committed
-(gdn_commit).  Inputs are seeded synthetic tensors resident in HBM; L2 is
-flushed (a 256 MiB write) between timed steps, outside the timed events.
+chain windows (256 rows), every row's fp32 state and conv tail recorded into
+a pool of cache entries (gdn_window_pooled), then each stream's random
+accepted length 0..16 committed by index (gdn_commit_swap: the slot takes
+the kept row's entry).  The same round with a record buffer and the copy
+commit (gdn_window + gdn_commit) is reported beside it.  Inputs are seeded
+synthetic tensors resident in HBM; L2 is flushed (a 256 MiB write) between
+timed steps, outside the timed events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -41,8 +44,8 @@ SEED = 2
 FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 WORKLOAD = ("verify round, one GDN layer: 16 streams x 16-row chain windows (256 rows), 27B-like heads "
-            "(Hk=16, Hv=48, d_k=d_v=128), every row's fp32 state and conv tail recorded, then a random "
-            "accepted length 0..16 per stream committed")
+            "(Hk=16, Hv=48, d_k=d_v=128), every row's fp32 state and conv tail recorded (into a pool of "
+            "cache entries), then a random accepted length 0..16 per stream committed (by index)")
 
 
 # ---- algorithmic bytes (each byte the round must move at least once) ------
@@ -223,14 +226,45 @@ def run_ours(args, rank, world, local_rank):
     slot_t = torch.from_numpy(slots).to(dev)
     rp_t = torch.from_numpy(rp).to(dev)
     keep_t = host_keep.to(dev)
-    rec_state = torch.empty((R, g.n_v_heads, g.d_v, g.d_k), dtype=torch.float32, device=dev)
-    rec_tail = torch.empty((R, 3, g.channels), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
-        gdn.window(d, dw, dc, slot_t, rp_t, dr, rec_state, rec_tail, stream)
-        gdn.commit(d, dc, slot_t, rp_t, keep_t, rec_state, rec_tail, stream)
+    # The round records every row in a pool of cache entries (gdn_window_pooled)
+    # and commits by index (gdn_commit_swap).  The pool holds the 16 committed
+    # states, the 256 records of a round and 16 spare entries; the entries
+    # each round records into come from a first-in first-out free list that
+    # the host keeps (the rows a round does not keep and the slots it
+    # replaces are freed), computed ahead for every round the bench runs, in
+    # the order the rounds run.
+    n_pool = N_STREAMS + R + N_STREAMS
+    pool_state = torch.empty((n_pool, g.n_v_heads, g.d_v, g.d_k), dtype=torch.float32, device=dev)
+    pool_tail = torch.empty((n_pool, 3, g.channels), dtype=torch.bfloat16, device=dev)
+    pool_state[:N_STREAMS].copy_(dc["state"])
+    pool_tail[:N_STREAMS].copy_(dc["tail"])
+    pool = {"state": pool_state, "tail": pool_tail}
+    n_rounds = max(args.warmup, 3) + 3 * args.steps + 2
+    recs = np.empty((n_rounds, R), np.int32)
+    free, cur = list(range(N_STREAMS, n_pool)), list(range(N_STREAMS))
+    for i in range(n_rounds):
+        rec, free = free[:R], free[R:]
+        kept = set()
+        for s_ in range(N_STREAMS):
+            if keep[s_] >= 0:
+                free.append(cur[s_])
+                cur[s_] = rec[keep[s_]]
+                kept.add(cur[s_])
+        free += [x for x in rec if x not in kept]
+        recs[i] = rec
+    host_recs = torch.from_numpy(recs).pin_memory()
+    recs_t = host_recs.to(dev)
+    rec_t = torch.empty(R, dtype=torch.int32, device=dev)   # the round's entries, as a serving loop sends them
+    round_no = [0]
+
+    def step(rec_slot=None, rows_=None, keep_=None):
+        rs = recs_t[round_no[0]] if rec_slot is None else rec_slot
+        gdn.window_pooled(d, dw, pool, slot_t, rp_t, dr if rows_ is None else rows_, rs, stream)
+        gdn.commit_swap(d, pool, slot_t, rp_t, keep_t if keep_ is None else keep_, rs, None, stream)
+        round_no[0] += 1
 
     def barrier():
         if world > 1:
@@ -251,11 +285,13 @@ def run_ours(args, rank, world, local_rank):
     t0 = time.time()
     for i in range(K):
         flush.fill_(i & 0xff)
+        rs = recs_t[round_no[0]]
         ev[i][0].record(stream)
-        gdn.window(d, dw, dc, slot_t, rp_t, dr, rec_state, rec_tail, stream)
+        gdn.window_pooled(d, dw, pool, slot_t, rp_t, dr, rs, stream)
         ev[i][1].record(stream)
-        gdn.commit(d, dc, slot_t, rp_t, keep_t, rec_state, rec_tail, stream)
+        gdn.commit_swap(d, pool, slot_t, rp_t, keep_t, rs, None, stream)
         ev[i][2].record(stream)
+        round_no[0] += 1
     torch.cuda.synchronize()
     barrier()
     t1 = time.time()
@@ -273,7 +309,8 @@ def run_ours(args, rank, world, local_rank):
         for k in ("mixed", "z", "a", "b"):
             dr[k].copy_(host_in[k], non_blocking=True)
         keep_t.copy_(host_keep, non_blocking=True)
-        step()
+        rec_t.copy_(host_recs[round_no[0]], non_blocking=True)
+        step(rec_slot=rec_t)
         host_y.copy_(dr["y"], non_blocking=True)
         ev2[i][1].record(stream)
     torch.cuda.synchronize()
@@ -290,17 +327,20 @@ def run_ours(args, rank, world, local_rank):
     h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     bufs = [dict(dr), {k: torch.empty_like(v) for k, v in dr.items()}]
     keeps = [keep_t, torch.empty_like(keep_t)]
+    recbufs = [rec_t, torch.empty_like(rec_t)]
+    in_round = [0, 0]
     host_ys = [host_y, torch.empty_like(host_y).pin_memory()]
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_win = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
     ev_y = [torch.cuda.Event() for _ in range(2)]
 
-    def copy_in(b):
+    def copy_in(b, rnd):
         with torch.cuda.stream(h2d_s):
             for k in ("mixed", "z", "a", "b"):
                 bufs[b][k].copy_(host_in[k], non_blocking=True)
             keeps[b].copy_(host_keep, non_blocking=True)
+            recbufs[b].copy_(host_recs[rnd], non_blocking=True)
         ev_in[b].record(h2d_s)
 
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -308,14 +348,16 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     t_start.record(stream)
     h2d_s.wait_stream(stream)
-    copy_in(0)
+    first = round_no[0]
+    copy_in(0, first)
     for i in range(K):
         b = i & 1
         stream.wait_event(ev_in[b])
-        gdn.window(d, dw, dc, slot_t, rp_t, bufs[b], rec_state, rec_tail, stream)
+        gdn.window_pooled(d, dw, pool, slot_t, rp_t, bufs[b], recbufs[b], stream)
         ev_win[b].record(stream)
-        gdn.commit(d, dc, slot_t, rp_t, keeps[b], rec_state, rec_tail, stream)
+        gdn.commit_swap(d, pool, slot_t, rp_t, keeps[b], recbufs[b], None, stream)
         ev_done[b].record(stream)
+        round_no[0] += 1
         d2h_s.wait_event(ev_win[b])
         with torch.cuda.stream(d2h_s):
             host_ys[b].copy_(bufs[b]["y"], non_blocking=True)
@@ -324,7 +366,7 @@ def run_ours(args, rank, world, local_rank):
             nb = (i + 1) & 1   # last used by step i - 1: its calls and its y read-back must be done
             h2d_s.wait_event(ev_done[nb])
             h2d_s.wait_event(ev_y[nb])
-            copy_in(nb)
+            copy_in(nb, first + i + 1)
     stream.wait_event(ev_y[(K - 1) & 1])
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -333,9 +375,35 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = t_start.elapsed_time(t_end) / K
     if gdn.get_device_error() != 0:
         raise RuntimeError("device error word set during the timed steps")
+    # the same round with its records in a buffer of their own and the copy
+    # commit (gdn_window + gdn_commit), for comparison
+    copy_round = None
+    if rank == 0:
+        del pool, pool_state, pool_tail
+        rec_state = torch.empty((R, g.n_v_heads, g.d_v, g.d_k), dtype=torch.float32, device=dev)
+        rec_tail = torch.empty((R, 3, g.channels), dtype=torch.bfloat16, device=dev)
+        nk = min(K, 50)
+        slot_c = torch.from_numpy(slots).to(dev)   # the pooled rounds moved slot_t into the pool
+        evc = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nk + 3)]
+        for i in range(nk + 3):
+            flush.fill_(i & 0xff)
+            evc[i][0].record(stream)
+            gdn.window(d, dw, dc, slot_c, rp_t, dr, rec_state, rec_tail, stream)
+            evc[i][1].record(stream)
+            gdn.commit(d, dc, slot_c, rp_t, keep_t, rec_state, rec_tail, stream)
+            evc[i][2].record(stream)
+        torch.cuda.synchronize()
+        cw_ms = statistics.mean(evc[i][0].elapsed_time(evc[i][1]) for i in range(3, nk + 3))
+        cc_ms = statistics.mean(evc[i][1].elapsed_time(evc[i][2]) for i in range(3, nk + 3))
+        n_committed_ = int((keep >= 0).sum())
+        copy_round = {"ms_per_step": cw_ms + cc_ms, "rows_per_s": R / ((cw_ms + cc_ms) * 1e-3),
+                      "window_ms": cw_ms, "commit_ms": cc_ms, "commit_bytes": commit_bytes(g, n_committed_),
+                      "commit_gbs": commit_bytes(g, n_committed_) / (cc_ms * 1e-3) / 1e9,
+                      "method": "gdn_window into a record buffer, then gdn_commit copying each kept row's "
+                                "state and tail into its slot; CUDA events, L2 flushed between steps"}
+        del rec_state, rec_tail
     extra = None
     if not args.no_extra and rank == 0:
-        del rec_state, rec_tail
         extra = run_extra(dev, stream, flush)
         if gdn.get_device_error() != 0:
             raise RuntimeError("device error word set during the secondary measurements")
@@ -349,7 +417,7 @@ def run_ours(args, rank, world, local_rank):
     wbytes = window_bytes(g, N_STREAMS, R)
     peak, peak_src = hbm_peak()
     achieved = wbytes / (win_avg * 1e-3) / 1e9
-    h2d = sum(host_in[k].numel() * 2 for k in host_in) + host_keep.numel() * 4
+    h2d = sum(host_in[k].numel() * 2 for k in host_in) + host_keep.numel() * 4 + R * 4   # + the round's pool entries
     d2h = host_y.numel() * 2
     line = {
         "metric": METRIC,
@@ -378,8 +446,9 @@ def run_ours(args, rank, world, local_rank):
                      "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum of one launch, read from the "
                                        "committed ncu summary profiles/gdn_window_verify_16x16.md (not measured "
                                        "in this run); null when the kernel's sources changed since that capture"},
-        "commit": {"ms_per_launch": statistics.mean(com_ms), "bytes_per_launch": commit_bytes(g, n_committed),
-                   "gbs": commit_bytes(g, n_committed) / (statistics.mean(com_ms) * 1e-3) / 1e9},
+        "commit": {"kind": "index swap (gdn_commit_swap): slot[s] takes the kept row's pool entry",
+                   "ms_per_launch": statistics.mean(com_ms), "streams_committed": n_committed},
+        "copy_commit_round": copy_round,
         "e2e": {"value": world * R / (e2e_ms * 1e-3), "unit": "rows/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "method": "pinned host inputs copied in and y read back every step through the public API; "

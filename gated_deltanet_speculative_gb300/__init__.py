@@ -3,6 +3,7 @@
 The C ABI of include/gdn.h (libgdn.so, hand-written sm_103a kernels) behind a
 thin ctypes binding: ``step``, ``window``, ``tree``, ``commit``,
 ``window_log``, ``commit_replay``, ``tree_log``, ``commit_replay_tree``,
+``window_pooled``, ``tree_pooled``, ``commit_swap``,
 ``prefill``, ``prefill_noalloc`` and ``get_device_error`` take torch CUDA tensors and enqueue on the current
 stream.  ``synth`` draws the seeded synthetic inputs.  Importing the package
 does not load the CUDA library; the first call does (and raises if it is
@@ -10,7 +11,7 @@ missing).
 """
 from . import synth  # noqa: F401
 from ._binding import (Dims, GdnError, MAX_WINDOW, PREFILL_CHUNK, PREFILL_NOALLOC_SCRATCH_BYTES,  # noqa: F401
-                       commit, commit_replay, commit_replay_tree, debug_wait_timeout, get_device_error,
+                       commit, commit_replay, commit_replay_tree, commit_swap, debug_wait_timeout, get_device_error,
                        library_path, load, prefill,
-                       prefill_noalloc, prefill_workspace, prefill_workspace_size, step, tree, tree_log, window,
-                       window_log)
+                       prefill_noalloc, prefill_workspace, prefill_workspace_size, step, tree, tree_log, tree_pooled,
+                       window, window_log, window_pooled)

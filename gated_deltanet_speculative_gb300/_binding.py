@@ -60,6 +60,11 @@ _SIGS = {
     "gdn_tree": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _P, _I, _I,
                  ctypes.POINTER(c_rows), _P, _P, _P],
     "gdn_commit": [ctypes.POINTER(c_dims), ctypes.POINTER(c_cache), _P, _P, _P, _I, _I, _P, _P, _P],
+    "gdn_window_pooled": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _I, _I,
+                          ctypes.POINTER(c_rows), _P, _P],
+    "gdn_tree_pooled": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _P, _I,
+                        _I, ctypes.POINTER(c_rows), _P, _P],
+    "gdn_commit_swap": [ctypes.POINTER(c_dims), ctypes.POINTER(c_cache), _P, _P, _P, _P, _I, _I, _P, _P],
     "gdn_prefill": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _I, _I,
                     ctypes.POINTER(c_rows), _I, _P, ctypes.c_size_t, _P],
     "gdn_prefill_workspace_size": [ctypes.POINTER(c_dims), _I, _I, _I],
@@ -229,6 +234,52 @@ def commit(dims: Dims, cache: dict, slot, row_ptr, keep_row, rec_state, rec_tail
     _need(rec_tail, "rec_tail", torch.bfloat16, (R, 3, dims.channels))
     _check("gdn_commit", lib.gdn_commit(ctypes.byref(dims.c()), ctypes.byref(cc), _ptr(slot), _ptr(row_ptr),
                                         _ptr(keep_row), S, R, _ptr(rec_state), _ptr(rec_tail), _stream_ptr(stream)))
+
+
+def window_pooled(dims: Dims, weights: dict, cache: dict, slot, row_ptr, rows: dict, rec_slot, stream=None):
+    """Chain verify windows recording row r at cache entry rec_slot[r]."""
+    lib = load()
+    _need(slot, "slot", torch.int32)
+    S = slot.numel()
+    _need(row_ptr, "row_ptr", torch.int32, (S + 1,))
+    R = rows["mixed"].shape[0]
+    _need(rec_slot, "rec_slot", torch.int32, (R,))
+    cw, cc, cr = _weights(dims, weights), _cache(dims, cache), _rows(dims, rows, R)
+    _check("gdn_window_pooled", lib.gdn_window_pooled(ctypes.byref(dims.c()), ctypes.byref(cw), ctypes.byref(cc),
+                                                      _ptr(slot), _ptr(row_ptr), S, R, ctypes.byref(cr),
+                                                      _ptr(rec_slot), _stream_ptr(stream)))
+
+
+def tree_pooled(dims: Dims, weights: dict, cache: dict, slot, row_ptr, parent, rows: dict, rec_slot, stream=None):
+    """Tree verify windows recording node r at cache entry rec_slot[r]."""
+    lib = load()
+    _need(slot, "slot", torch.int32)
+    S = slot.numel()
+    R = rows["mixed"].shape[0]
+    _need(row_ptr, "row_ptr", torch.int32, (S + 1,))
+    _need(parent, "parent", torch.int32, (R,))
+    _need(rec_slot, "rec_slot", torch.int32, (R,))
+    cw, cc, cr = _weights(dims, weights), _cache(dims, cache), _rows(dims, rows, R)
+    _check("gdn_tree_pooled", lib.gdn_tree_pooled(ctypes.byref(dims.c()), ctypes.byref(cw), ctypes.byref(cc),
+                                                  _ptr(slot), _ptr(row_ptr), _ptr(parent), S, R, ctypes.byref(cr),
+                                                  _ptr(rec_slot), _stream_ptr(stream)))
+
+
+def commit_swap(dims: Dims, cache: dict, slot, row_ptr, keep_row, rec_slot, freed=None, stream=None):
+    """Slot s takes pool entry rec_slot[keep_row[s]] (-1: unchanged); its
+    previous entry goes to freed[s] (-1 when nothing was committed)."""
+    lib = load()
+    _need(slot, "slot", torch.int32)
+    S = slot.numel()
+    _need(row_ptr, "row_ptr", torch.int32, (S + 1,))
+    _need(keep_row, "keep_row", torch.int32, (S,))
+    _need(rec_slot, "rec_slot", torch.int32)
+    if freed is not None:
+        _need(freed, "freed", torch.int32, (S,))
+    cc = _cache(dims, cache)
+    _check("gdn_commit_swap", lib.gdn_commit_swap(ctypes.byref(dims.c()), ctypes.byref(cc), _ptr(slot), _ptr(row_ptr),
+                                                  _ptr(keep_row), _ptr(rec_slot), S, rec_slot.numel(), _ptr(freed),
+                                                  _stream_ptr(stream)))
 
 
 def window_log(dims: Dims, weights: dict, cache: dict, slot, row_ptr, rows: dict, log_a, log_u, log_k, rec_tail,

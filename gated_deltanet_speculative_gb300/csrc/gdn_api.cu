@@ -176,7 +176,8 @@ int encode_row_maps(gdn::RowParams &p, int D, int n_rows) {
 
 int rows_entry(int mode, const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
                const int32_t *row_ptr, const int32_t *parent, int32_t n_streams, int32_t n_rows,
-               const gdn_rows *rows, float *rec_state, void *rec_tail, void *stream, LogBuffers logs = {}) {
+               const gdn_rows *rows, float *rec_state, void *rec_tail, void *stream, LogBuffers logs = {},
+               const int32_t *rec_slot = nullptr) {
     GDN_TRY(check_dims(dims));
     GDN_TRY(check_weights(w));
     GDN_TRY(check_cache(cache));
@@ -205,6 +206,7 @@ int rows_entry(int mode, const gdn_dims *dims, const gdn_weights *w, const gdn_c
     p.n_rows = mode == gdn::kStep ? n_streams : n_rows;
     p.rec_state = rec_state;
     p.rec_tail = static_cast<uint16_t *>(rec_tail);
+    p.rec_slot = rec_slot;
     p.log_a = logs.a;
     p.log_u = logs.u;
     p.log_k = logs.k;
@@ -346,6 +348,62 @@ int gdn_tree(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
              const gdn_rows *rows, float *rec_state, void *rec_tail, void *stream) {
     return rows_entry(gdn::kTree, dims, w, cache, slot, row_ptr, parent, n_streams, n_rows, rows, rec_state,
                       rec_tail, stream);
+}
+
+int gdn_window_pooled(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
+                      const int32_t *row_ptr, int32_t n_streams, int32_t n_rows, const gdn_rows *rows,
+                      const int32_t *rec_slot, void *stream) {
+    if (!cache) return GDN_ENULL;
+    if (!rec_slot) return GDN_ENULL;
+    if (!aligned(rec_slot, 4)) return GDN_EALIGN;
+    return rows_entry(gdn::kWindow, dims, w, cache, slot, row_ptr, nullptr, n_streams, n_rows, rows, cache->state,
+                      cache->tail, stream, LogBuffers{}, rec_slot);
+}
+
+int gdn_tree_pooled(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
+                    const int32_t *row_ptr, const int32_t *parent, int32_t n_streams, int32_t n_rows,
+                    const gdn_rows *rows, const int32_t *rec_slot, void *stream) {
+    if (!cache) return GDN_ENULL;
+    if (!rec_slot) return GDN_ENULL;
+    if (!aligned(rec_slot, 4)) return GDN_EALIGN;
+    return rows_entry(gdn::kTree, dims, w, cache, slot, row_ptr, parent, n_streams, n_rows, rows, cache->state,
+                      cache->tail, stream, LogBuffers{}, rec_slot);
+}
+
+int gdn_commit_swap(const gdn_dims *dims, const gdn_cache *cache, int32_t *slot, const int32_t *row_ptr,
+                    const int32_t *keep_row, const int32_t *rec_slot, int32_t n_streams, int32_t n_rows,
+                    int32_t *freed, void *stream) {
+    GDN_TRY(check_dims(dims));
+    GDN_TRY(check_cache(cache));
+    if (!slot || !row_ptr || !keep_row || !rec_slot) return GDN_ENULL;
+    if (n_streams <= 0 || n_streams > 65535 || n_rows <= 0) return GDN_EINVAL;
+    if (!aligned(slot, 4) || !aligned(row_ptr, 4) || !aligned(keep_row, 4) || !aligned(rec_slot, 4) ||
+        (freed && !aligned(freed, 4)))
+        return GDN_EALIGN;
+    int *err = error_word();
+    if (!err) return GDN_ECUDA;
+    gdn::SwapParams p = {};
+    p.slot = slot;
+    p.row_ptr = row_ptr;
+    p.keep_row = keep_row;
+    p.rec_slot = rec_slot;
+    p.freed = freed;
+    p.n_streams = n_streams;
+    p.n_rows = n_rows;
+    p.n_slots = cache->n_slots;
+    p.err = err;
+    // a programmatic dependent of the kernel before it: scheduled early, it
+    // waits (griddepcontrol.wait) before reading anything that kernel writes
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((n_streams + gdn::kSwapThreads - 1) / gdn::kSwapThreads));
+    cfg.blockDim = dim3(gdn::kSwapThreads);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gdn::gdn_commit_swap_kernel, p) == cudaSuccess ? GDN_OK : GDN_ECUDA;
 }
 
 int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot, const int32_t *row_ptr,

@@ -69,6 +69,51 @@ __global__ void __launch_bounds__(kCommitThreads) gdn_commit_kernel(const Commit
     for (size_t i = lo + threadIdx.x; i < hi; i += kCommitThreads) tdst[i] = __ldcs(tsrc + i);
 }
 
+// Commit by index (pooled records): the kept row's state and tail were
+// recorded in pool entry rec_slot[r] of the cache itself, so stream s keeps
+// them by taking that entry as its slot; its previous entry is handed back
+// in freed[s] (-1 when nothing is committed).  One thread per stream.
+struct SwapParams {
+    int *slot;               // [S] in/out
+    const int *row_ptr;      // [S + 1]
+    const int *keep_row;     // [S]
+    const int *rec_slot;     // [R]
+    int *freed;              // [S] or nullptr
+    int n_streams, n_rows, n_slots;
+    int *err;
+};
+
+constexpr int kSwapThreads = 128;
+
+__global__ void __launch_bounds__(kSwapThreads) gdn_commit_swap_kernel(const SwapParams p) {
+    const int s = blockIdx.x * kSwapThreads + threadIdx.x;
+    // Launched as a programmatic dependent of the window before it: while
+    // that kernel finishes, ask L2 for the index words (only a hint; they
+    // are read after the wait, when the previous kernel's writes are visible).
+    if (s < p.n_streams) {
+        prefetch_l2(p.keep_row + s);
+        prefetch_l2(p.row_ptr + s);
+        prefetch_l2(p.slot + s);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (s >= p.n_streams) return;
+    const int kr = p.keep_row[s];
+    int out = -1;
+    if (kr != -1) {
+        const int r0 = p.row_ptr[s], r1 = p.row_ptr[s + 1], old = p.slot[s];
+        const bool bad_keep = r0 < 0 || r1 > p.n_rows || kr < r0 || kr >= r1;
+        const int ne = bad_keep ? -1 : p.rec_slot[kr];
+        const bool bad_slot = !bad_keep && (ne < 0 || ne >= p.n_slots || ne == old);
+        if (bad_keep || bad_slot) {
+            raise_error(p.err, bad_keep ? GDN_DERR_KEEP : GDN_DERR_SLOT);
+        } else {
+            p.slot[s] = ne;
+            out = old;
+        }
+    }
+    if (p.freed) p.freed[s] = out;
+}
+
 // Replay commit: slot[s] <- the committed state advanced along the kept path
 // of the stream's logged window, one rank-1 update per row,  S <- u k^T + a S
 // with the same rounding as the window (fma(u_i, k_j, a * S_ij)), so the

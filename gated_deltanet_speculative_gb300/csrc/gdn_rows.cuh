@@ -66,8 +66,9 @@ struct RowParams {
     const int *row_ptr;       // [S + 1] (windows, trees)
     const int *parent;        // [R] (trees)
     int n_rows;
-    float *rec_state;         // [R, Hv, D, D]
-    uint16_t *rec_tail;       // bf16 [R, 3, CH]
+    float *rec_state;         // [R, Hv, D, D], or the state pool (pooled records)
+    uint16_t *rec_tail;       // bf16 [R, 3, CH], or the tail pool (pooled records)
+    const int *rec_slot;      // [R] pooled records: row r is recorded at entry rec_slot[r]; else nullptr
     float *log_a;             // [R, Hv] decay (logged modes)
     float *log_u;             // [R, Hv, D] write u = b (v - a S k) (logged modes)
     float *log_k;             // [R, Hk, D] normalised key (logged modes)
@@ -118,6 +119,7 @@ struct __align__(128) RowSmem {
     // the ancestor's staged row is 3 + e
     int anc[kMaxRows][3];
     int parent[kMaxRows];
+    int recidx[kMaxRows];   // where each row's state and tail are recorded (row r0 + t, or its pool entry)
     int reused[kMaxRows];   // tree: re-read later by a child that does not follow it
     int order[kMaxRows];    // tree: depth-first preorder (children in row order); else 0, 1, ...
     int nsub[kMaxRows];     // tree: subtree sizes, then each node's next free preorder slot
@@ -337,6 +339,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
     if (TREE && tid < n) sm.parent[tid] = __ldg(p.parent + r0 + tid);
     // ---- a4: gates
     if (tid < n) {
+        sm.recidx[tid] = p.rec_slot ? __ldg(p.rec_slot + r0 + tid) : r0 + tid;
         const size_t gi = (size_t)(r0 + tid) * p.Hv + h;
         const float ain = bf_bits(p.a[gi]);
         const float bin = bf_bits(p.b[gi]);
@@ -367,6 +370,9 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
             if (par < -1 || par >= t) bad = GDN_DERR_PARENT;
             sm.parent[t] = par;
             sm.reused[t] = 0;
+            // a pooled record must be a pool entry other than the stream's slot
+            const int ri = sm.recidx[t];
+            if (p.rec_slot && (ri < 0 || ri >= p.n_slots || ri == sl)) bad |= GDN_DERR_SLOT;
         }
         for (int t = 0; t < n && !bad; ++t) {
             int node = t, tail_next = 2;
@@ -456,7 +462,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
             const int src_row = m == 2 ? 3 + t : 3 + sm.anc[t][1 - m];
             const int part = ch / SEG, off = (ch - part * SEG) * 8;
             const int c = channel_of<D>(part, off, p.Hk, kh, h);
-            *reinterpret_cast<uint4 *>(p.rec_tail + ((size_t)(r0 + t) * 3 + m) * CH + c) =
+            *reinterpret_cast<uint4 *>(p.rec_tail + ((size_t)sm.recidx[t] * 3 + m) * CH + c) =
                 *reinterpret_cast<const uint4 *>(&sm.u.xin[part][src_row][off]);
         }
     }
@@ -523,7 +529,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
             const int par = sm.parent[t];
             if (par != sm.order[j - 1]) {
                 if constexpr (MODE == kTree) {
-                    load_tile<D, RPW, CPL>(S, (par < 0 ? slot_tile : p.rec_state + ((size_t)(r0 + par) * p.Hv + h) * tile) +
+                    load_tile<D, RPW, CPL>(S, (par < 0 ? slot_tile : p.rec_state + ((size_t)sm.recidx[par] * p.Hv + h) * tile) +
                                                   (size_t)row0 * D,
                                            warp, lane);
                 } else {
@@ -595,7 +601,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
         }
         if (MODE == kWindow || MODE == kTree) {
             const bool streaming = !(MODE == kTree && sm.reused[t]);
-            store_tile<D, RPW, CPL>(p.rec_state + ((size_t)(r0 + t) * p.Hv + h) * tile + (size_t)row0 * D, S, warp,
+            store_tile<D, RPW, CPL>(p.rec_state + ((size_t)sm.recidx[t] * p.Hv + h) * tile + (size_t)row0 * D, S, warp,
                                     lane, streaming);
         }
         if (LOG && lane < 16 && (lane & ((1 << SHIFT) - 1)) == 0) {

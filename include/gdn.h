@@ -212,6 +212,53 @@ int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot
                int32_t n_rows, const float *rec_state, const void *rec_tail, void *stream);
 
 /*
+ * gdn_window_pooled, gdn_tree_pooled -- gdn_window / gdn_tree recording each
+ * row in the cache itself, so that committing a row is a change of index
+ * instead of a copy (the survey of the verify path's commit step: the kept
+ * row can become the slot by an index swap; [P747] first note: each stream
+ * keeps only its accepted rows).  The cache is then a pool of entries, some
+ * holding committed states (named by slot[]), the others free.  Row r's
+ * state and tail go to entry rec_slot[r] of cache->state and cache->tail,
+ * bit for bit what gdn_window / gdn_tree write to rec_state[r] and
+ * rec_tail[r]; y is the same too.
+ *   rec_slot  device int32 [n_rows]: pool entries in [0, n_slots), distinct
+ *             from each other and from every slot[s] of the call (the
+ *             library checks only that each is in range and is not its own
+ *             stream's slot: otherwise GDN_DERR_SLOT and the stream is
+ *             skipped).  Entries the caller no longer needs (the rows it does
+ *             not keep) are free again after the commit.
+ * Everything else as gdn_window / gdn_tree.
+ */
+int gdn_window_pooled(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
+                      const int32_t *slot, const int32_t *row_ptr, int32_t n_streams,
+                      int32_t n_rows, const gdn_rows *rows, const int32_t *rec_slot, void *stream);
+int gdn_tree_pooled(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
+                    const int32_t *slot, const int32_t *row_ptr, const int32_t *parent,
+                    int32_t n_streams, int32_t n_rows, const gdn_rows *rows,
+                    const int32_t *rec_slot, void *stream);
+
+/*
+ * gdn_commit_swap -- commit after gdn_window_pooled / gdn_tree_pooled: for
+ * stream s with keep_row[s] = r in [row_ptr[s], row_ptr[s+1]), slot[s]
+ * becomes rec_slot[r] (the entry that already holds row r's state and tail)
+ * and freed[s] receives the stream's previous entry; keep_row[s] = -1 leaves
+ * slot[s] as it is and sets freed[s] = -1.  One small kernel, no state or
+ * tail is moved; it is launched as a programmatic dependent of the kernel
+ * before it on `stream` (scheduled early, it reads nothing before that
+ * kernel has completed).
+ *   slot      device int32 [n_streams], read and written
+ *   row_ptr, keep_row  as gdn_commit
+ *   rec_slot  device int32 [n_rows], as given to the pooled window or tree
+ *   freed     device int32 [n_streams] or NULL
+ * A keep_row outside the stream's rows sets GDN_DERR_KEEP, a rec_slot[r]
+ * outside [0, n_slots) or equal to slot[s] sets GDN_DERR_SLOT; either
+ * leaves slot[s] as it is (freed[s] = -1).
+ */
+int gdn_commit_swap(const gdn_dims *dims, const gdn_cache *cache, int32_t *slot,
+                    const int32_t *row_ptr, const int32_t *keep_row, const int32_t *rec_slot,
+                    int32_t n_streams, int32_t n_rows, int32_t *freed, void *stream);
+
+/*
  * gdn_prefill -- chunked prompt prefill ([P747] the engine's prompt kernel,
  * several prompts prefilled in one pass; [P932] tree note: a prompt writes
  * its slot directly).  Sequence s owns packed tokens
