@@ -27,9 +27,12 @@ __device__ __forceinline__ float bf_bits(uint16_t u) {
     return __uint_as_float(static_cast<uint32_t>(u) << 16);
 }
 
-// SiLU(x) = x / (1 + e^-x)
+// SiLU(x) = x / (1 + e^-x), with the fast exponential and division (a few
+// ulp; one function for every instantiation, so steps, windows and trees
+// still agree bit for bit; beyond |x| ~ 88 the quotient's limit, x or 0, is
+// what comes out)
 __device__ __forceinline__ float silu(float x) {
-    return __fdiv_rn(x, __fadd_rn(1.0f, expf(-x)));
+    return __fdividef(x, __fadd_rn(1.0f, __expf(-x)));
 }
 
 // sigmoid(x) = 1 / (1 + e^-x)

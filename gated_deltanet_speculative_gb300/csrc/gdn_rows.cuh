@@ -338,6 +338,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
     }
     if (TREE && tid < n) sm.parent[tid] = __ldg(p.parent + r0 + tid);
     // ---- a4: gates
+    if (tid == 0) sm.bad = 0;
     if (tid < n) {
         sm.recidx[tid] = p.rec_slot ? __ldg(p.rec_slot + r0 + tid) : r0 + tid;
         const size_t gi = (size_t)(r0 + tid) * p.Hv + h;
@@ -363,36 +364,43 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
     }
 
     // ---- each row's parent and conv ancestors along its branch -------------
-    if (tid == 0) {
-        int bad = 0;
-        for (int t = 0; t < n; ++t) {
-            const int par = TREE ? sm.parent[t] : t - 1;
-            if (par < -1 || par >= t) bad = GDN_DERR_PARENT;
-            sm.parent[t] = par;
-            sm.reused[t] = 0;
-            // a pooled record must be a pool entry other than the stream's slot
-            const int ri = sm.recidx[t];
-            if (p.rec_slot && (ri < 0 || ri >= p.n_slots || ri == sl)) bad |= GDN_DERR_SLOT;
-        }
-        for (int t = 0; t < n && !bad; ++t) {
-            int node = t, tail_next = 2;
-            for (int m = 0; m < 3; ++m) {
-                if (node >= 0) node = sm.parent[node];
-                if (node >= 0) {
-                    sm.anc[t][m] = node;
-                } else {
-                    sm.anc[t][m] = tail_next - 3;
-                    --tail_next;
-                }
+    // Each row's thread checks its own parent and record entry ...
+    if (tid < n) {
+        const int par = TREE ? sm.parent[tid] : tid - 1;
+        int bad = (par < -1 || par >= tid) ? GDN_DERR_PARENT : 0;
+        // a pooled record must be a pool entry other than the stream's slot
+        const int ri = sm.recidx[tid];
+        if (p.rec_slot && (ri < 0 || ri >= p.n_slots || ri == sl)) bad |= GDN_DERR_SLOT;
+        if (bad) atomicOr(&sm.bad, bad);
+        sm.parent[tid] = par;
+        sm.reused[tid] = 0;
+        sm.order[tid] = tid;
+    }
+    __syncthreads();
+    if (sm.bad) {   // uniform over the CTA and over its cluster (same stream)
+        if (h == 0 && tid == 0) raise_error(p.err, sm.bad);
+        return;
+    }
+    // ... then walks up to three parents for its conv ancestors
+    if (tid < n) {
+        int node = tid, tail_next = 2;
+        for (int m = 0; m < 3; ++m) {
+            if (node >= 0) node = sm.parent[node];
+            if (node >= 0) {
+                sm.anc[tid][m] = node;
+            } else {
+                sm.anc[tid][m] = tail_next - 3;
+                --tail_next;
             }
         }
+    }
+    if (TREE && tid == 0) {
         // Visit order: a chain in row order; a tree depth first, so that a node
         // follows its parent wherever it can and the parent's state is still
         // in registers (only a node's later children reload it).  Preorder
         // without a stack: subtree sizes bottom-up (parents precede
         // children), then each node takes its parent's next free slot.
-        for (int t = 0; t < n; ++t) sm.order[t] = t;
-        if (TREE && !bad) {
+        {
             for (int t = 0; t < n; ++t) sm.nsub[t] = 1;
             for (int t = n - 1; t > 0; --t)
                 if (sm.parent[t] >= 0) sm.nsub[sm.parent[t]] += sm.nsub[t];
@@ -418,11 +426,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
                 for (int t = 0; t < n; ++t)
                     path_mask[t] = (1 << t) | (sm.parent[t] >= 0 ? path_mask[sm.parent[t]] : 0);
         }
-        if (bad && h == 0) raise_error(p.err, bad);
-        sm.bad = bad;
     }
     __syncthreads();
-    if (sm.bad) return;
 
     // ---- a2: conv over the branch's four taps, then SiLU (4 channels each) --
     for (int i = tid; i < n * (3 * D / 4); i += kRowThreads) {
