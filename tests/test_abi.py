@@ -160,3 +160,34 @@ def test_debug_wait_timeout_bounds_its_polls():
     (2^22) before launching anything."""
     lib = gdn.load()
     assert lib.gdn_debug_wait_timeout((1 << 22) + 1, None) == -1
+
+
+def test_pooled_entry_points_refuse_bad_arguments_on_the_host():
+    """gdn_window_pooled / gdn_tree_pooled / gdn_commit_swap: a missing
+    rec_slot, row_ptr or keep_row is GDN_ENULL, a misaligned index array
+    GDN_EALIGN, a non-positive size GDN_EINVAL, all before any CUDA call
+    (the addresses below are never dereferenced)."""
+    lib = gdn.load()
+    d, w, c, r = _args()
+    W, C, R = ctypes.byref(w), ctypes.byref(c), ctypes.byref(r)
+    D = ctypes.byref(d)
+    assert lib.gdn_window_pooled(D, W, C, A16, A16, 2, 4, R, None, None) == -2
+    assert lib.gdn_window_pooled(D, W, C, A16, A16, 2, 4, R, A16 + 2, None) == -3
+    assert lib.gdn_window_pooled(D, W, C, A16, A16, 0, 4, R, A16, None) == -1
+    assert lib.gdn_window_pooled(D, W, None, A16, A16, 2, 4, R, A16, None) == -2
+    assert lib.gdn_tree_pooled(D, W, C, A16, A16, None, 2, 4, R, A16, None) == -2
+    assert lib.gdn_tree_pooled(D, W, C, A16, A16, A16, 2, 4, R, None, None) == -2
+    assert lib.gdn_commit_swap(D, C, A16, A16, A16, None, 2, 4, None, None) == -2
+    assert lib.gdn_commit_swap(D, C, A16, None, A16, A16, 2, 4, None, None) == -2
+    assert lib.gdn_commit_swap(D, C, A16, A16, A16, A16, 2, 4, A16 + 1, None) == -3
+    assert lib.gdn_commit_swap(D, C, A16, A16, A16, A16, 2, 0, None, None) == -1
+    assert lib.gdn_commit_swap(D, C, A16, A16, A16, A16, 0, 4, None, None) == -1
+
+
+def test_commit_refuses_a_missing_or_misaligned_row_ptr():
+    lib = gdn.load()
+    d, w, c, r = _args()
+    assert lib.gdn_commit(ctypes.byref(d), ctypes.byref(c), A16, None, A16, 2, 4, A16, A16, None) == -2
+    assert lib.gdn_commit(ctypes.byref(d), ctypes.byref(c), A16, A16 + 2, A16, 2, 4, A16, A16, None) == -3
+    assert lib.gdn_prefill_workspace(ctypes.byref(d), 1, 4722, 64) == \
+        lib.gdn_prefill_workspace_size(ctypes.byref(d), 1, 4722, 64) > 0
