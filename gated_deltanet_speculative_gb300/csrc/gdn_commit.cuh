@@ -95,12 +95,14 @@ __global__ void __launch_bounds__(kSwapThreads) gdn_commit_swap_kernel(const Swa
         prefetch_l2(p.row_ptr + s);
         prefetch_l2(p.slot + s);
     }
+    for (int i = s * 32; i < p.n_rows; i += gridDim.x * kSwapThreads * 32) prefetch_l2(p.rec_slot + i);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (s >= p.n_streams) return;
+    // the four index words at once, then the kept row's entry
     const int kr = p.keep_row[s];
+    const int r0 = p.row_ptr[s], r1 = p.row_ptr[s + 1], old = p.slot[s];
     int out = -1;
     if (kr != -1) {
-        const int r0 = p.row_ptr[s], r1 = p.row_ptr[s + 1], old = p.slot[s];
         const bool bad_keep = r0 < 0 || r1 > p.n_rows || kr < r0 || kr >= r1;
         const int ne = bad_keep ? -1 : p.rec_slot[kr];
         const bool bad_slot = !bad_keep && (ne < 0 || ne >= p.n_slots || ne == old);

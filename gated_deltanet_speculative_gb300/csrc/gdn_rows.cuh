@@ -266,6 +266,12 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
         }
         asm volatile("griddepcontrol.wait;" ::: "memory");
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    } else {
+        // A window or tree lets a kernel launched after it as a programmatic
+        // dependent (the index commit) be scheduled as soon as every CTA of
+        // this grid has started: that kernel waits for this grid's end
+        // (griddepcontrol.wait) before it reads or writes anything.
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
     const bool lead = (h % p.G) == 0;    // this CTA writes the q/k channels shared by its key-head group
 

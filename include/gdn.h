@@ -166,7 +166,10 @@ int gdn_step(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
  * Launch: one CTA per (value head, stream); when those would leave SMs
  * idle (few streams), each head's state rows are split over a cluster of
  * 2 to 8 CTAs, with the same bits.  d >= 64 without that split stages the
- * inputs with TMA (three tensor maps encoded on the host per call).
+ * inputs with TMA (three tensor maps encoded on the host per call).  Every
+ * CTA signals programmatic dependents when it starts, so a kernel launched
+ * after it as one (gdn_commit_swap) is scheduled early and waits for the
+ * window's end; a plain launch after it is unaffected.
  */
 int gdn_window(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
                const int32_t *slot, const int32_t *row_ptr, int32_t n_streams,
