@@ -180,3 +180,55 @@ def test_pooled_index_checks_skip_the_stream():
     assert bits & 8 and bits & 1
     assert np.array_equal(slot_t.cpu().numpy(), c.slots)
     assert np.array_equal(freed.cpu().numpy(), [-1, -1])
+
+
+def test_pooled_full_round_16x16_then_swap_against_oracle():
+    """The round the benchmark times, at its size: 16 streams x 16 rows,
+    27B-like heads, a pool of 16 + 256 + 16 entries with the round's entries
+    taken in a shuffled order, every row recorded into its entry
+    (gdn_window_pooled), then random accepted lengths committed by index
+    (gdn_commit_swap).  y and every recorded state and tail against the
+    oracle; each committed slot's entry holds the oracle's state and tail
+    after the stream's last accepted row."""
+    from harness import check_state, check_y
+    g = synth.LIKE_27B
+    c = Case(g, [16] * 16, seed=181)
+    d = c.dims_gpu()
+    n_pool = c.S + c.R + c.S
+    rng = np.random.default_rng(181)
+    free = c.S + rng.permutation(c.R + c.S).astype(np.int32)
+    rec_slot = free[:c.R].copy()
+    slots = np.arange(c.S, dtype=np.int32)
+    ps = torch.full((n_pool, g.n_v_heads, g.d_v, g.d_k), float("nan"), dtype=torch.float32, device="cuda")
+    pt = torch.full((n_pool, 3, g.channels), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ps[:c.S].copy_(torch.from_numpy(c.cache["state"][c.slots]))
+    pt[:c.S].copy_(torch.from_numpy(c.cache["tail"][c.slots].view(np.int16)).view(torch.bfloat16))
+    pool = {"state": ps, "tail": pt}
+    rows = c.dev_rows()
+    slot_t = dev(slots)
+    gdn.window_pooled(d, c.dev_weights(), pool, slot_t, dev(c.row_ptr), rows, dev(rec_slot))
+    acc = synth.accepted_lengths(c.S, 16, rng)
+    keep = np.where(acc > 0, c.row_ptr[:-1] + acc - 1, -1).astype(np.int32)
+    freed = torch.empty(c.S, dtype=torch.int32, device="cuda")
+    gdn.commit_swap(d, pool, slot_t, dev(c.row_ptr), dev(keep), dev(rec_slot), freed)
+    assert gdn.get_device_error() == 0
+    y = host_bits(rows["y"])
+    new_slot = slot_t.cpu().numpy()
+    assert np.array_equal(new_slot, np.where(keep >= 0, rec_slot[np.maximum(keep, 0)], slots))
+    assert np.array_equal(freed.cpu().numpy(), np.where(keep >= 0, slots, -1))
+    for s in range(c.S):
+        lo, hi = c.stream_rows(s)
+        ref = c.oracle_stream(s)
+        ent = rec_slot[lo:hi]
+        check_y(y[lo:hi], ref["y"], what=f"y stream {s}")
+        check_state(ps[torch.from_numpy(ent).long().cuda()].cpu().numpy(), ref["rec_state"],
+                    what=f"recorded states stream {s}")
+        assert np.array_equal(host_bits(pt[torch.from_numpy(ent).long().cuda()]), ref["rec_tail"]), f"tails {s}"
+        e = int(new_slot[s])
+        if keep[s] >= 0:
+            k = int(keep[s]) - lo
+            check_state(ps[e].cpu().numpy()[None], ref["rec_state"][k][None], what=f"committed state {s}")
+            assert np.array_equal(host_bits(pt[e]), ref["rec_tail"][k]), f"committed tail {s}"
+        else:
+            assert np.array_equal(ps[e].cpu().numpy().view(np.uint32),
+                                  c.cache["state"][c.slots[s]].view(np.uint32)), f"untouched slot {s}"
