@@ -232,3 +232,45 @@ def test_pooled_full_round_16x16_then_swap_against_oracle():
         else:
             assert np.array_equal(ps[e].cpu().numpy().view(np.uint32),
                                   c.cache["state"][c.slots[s]].view(np.uint32)), f"untouched slot {s}"
+
+
+def test_pooled_round_swap_then_step_back_to_back_equals_copy_path():
+    """window_pooled, commit_swap and a one-row step of every stream, queued
+    back to back with no host synchronisation in between (the swap and the
+    step are programmatic dependents of the kernel before them and read the
+    slot words only after it ends), against gdn_window + gdn_commit +
+    gdn_step, bit for bit."""
+    g = synth.Geometry(2, 6, 128, 128)
+    c = Case(g, [16, 9, 4, 1], seed=191, n_slots=4, slots=[0, 1, 2, 3])
+    acc = np.array([16, 0, 2, 1], np.int32)
+    keep = np.where(acc > 0, c.row_ptr[:-1] + acc - 1, -1).astype(np.int32)
+    step_rows = synth.row_inputs(g, c.S, 193)
+    d = c.dims_gpu()
+
+    def dev_step_rows():
+        r = {k: dev_bf16(step_rows[k]) for k in ("mixed", "z", "a", "b")}
+        r["y"] = torch.full((c.S, g.n_v_heads, g.d_v), float("nan"), dtype=torch.bfloat16, device="cuda")
+        return r
+
+    # copy path
+    w, cache, rows, rs, rt = run_recorded(c, False)
+    gdn.commit(d, cache, dev(c.slots), dev(c.row_ptr), dev(keep), rs, rt)
+    sr = dev_step_rows()
+    gdn.step(d, w, cache, dev(c.slots), sr)
+    assert gdn.get_device_error() == 0
+    # pooled path, one stream, no synchronisation
+    pool, n_pool = pool_of(c, c.R)
+    rec_slot = (c.n_slots + np.arange(c.R)).astype(np.int32)
+    slot_t = dev(c.slots.copy())
+    prow, psr = c.dev_rows(), dev_step_rows()
+    gdn.window_pooled(d, c.dev_weights(), pool, slot_t, dev(c.row_ptr), prow, dev(rec_slot))
+    gdn.commit_swap(d, pool, slot_t, dev(c.row_ptr), dev(keep), dev(rec_slot))
+    gdn.step(d, c.dev_weights(), pool, slot_t, psr)
+    assert gdn.get_device_error() == 0
+    assert np.array_equal(host_bits(psr["y"]), host_bits(sr["y"]))
+    cur = slot_t.cpu().numpy()
+    st, pst = cache["state"].cpu().numpy(), pool["state"].cpu().numpy()
+    tl, ptl = host_bits(cache["tail"]), host_bits(pool["tail"])
+    for s in range(c.S):
+        assert np.array_equal(pst[cur[s]].view(np.uint32), st[c.slots[s]].view(np.uint32)), f"state {s}"
+        assert np.array_equal(ptl[cur[s]], tl[c.slots[s]]), f"tail {s}"
