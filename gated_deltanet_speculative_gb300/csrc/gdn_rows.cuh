@@ -122,7 +122,6 @@ struct __align__(128) RowSmem {
     int recidx[kMaxRows];   // where each row's state and tail are recorded (row r0 + t, or its pool entry)
     int reused[kMaxRows];   // tree: re-read later by a child that does not follow it
     int order[kMaxRows];    // tree: depth-first preorder (children in row order); else 0, 1, ...
-    int nsub[kMaxRows];     // tree: subtree sizes, then each node's next free preorder slot
     int bad;
 };
 
@@ -400,38 +399,44 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
             }
         }
     }
-    if (TREE && tid == 0) {
-        // Visit order: a chain in row order; a tree depth first, so that a node
-        // follows its parent wherever it can and the parent's state is still
-        // in registers (only a node's later children reload it).  Preorder
-        // without a stack: subtree sizes bottom-up (parents precede
-        // children), then each node takes its parent's next free slot.
-        {
-            for (int t = 0; t < n; ++t) sm.nsub[t] = 1;
-            for (int t = n - 1; t > 0; --t)
-                if (sm.parent[t] >= 0) sm.nsub[sm.parent[t]] += sm.nsub[t];
-            int root_next = 0;
-            for (int t = 0; t < n; ++t) {
-                const int par = sm.parent[t];
-                int pre;
-                if (par < 0) {
-                    pre = root_next;
-                    root_next += sm.nsub[t];
-                } else {
-                    pre = sm.nsub[par];   // the parent's next free slot (set below when it was placed)
-                    sm.nsub[par] = pre + sm.nsub[t];
-                }
-                sm.order[pre] = t;
-                sm.nsub[t] = pre + 1;     // from here on: this node's next free slot
-            }
-            for (int j = 1; j < n; ++j) {
-                const int par = sm.parent[sm.order[j]];
-                if (par >= 0 && par != sm.order[j - 1]) sm.reused[par] = 1;
-            }
-            if constexpr (MODE == kTreeLog)   // parents precede children
-                for (int t = 0; t < n; ++t)
-                    path_mask[t] = (1 << t) | (sm.parent[t] >= 0 ? path_mask[sm.parent[t]] : 0);
+    if (TREE && warp == 0) {
+        // Visit order: a tree depth first, children (and roots) in row order,
+        // so that a node follows its parent wherever it can and the parent's
+        // state is still in registers (only a node's later children reload
+        // it).  Lane t < n takes node t: its ancestor-or-self set by walking
+        // up, subtree sizes by ballot over those sets, and its preorder slot
+        // = its depth + the subtree sizes of the earlier siblings of every
+        // node on its root-to-node path.
+        const bool live = lane < n;
+        const int par = live ? sm.parent[lane] : -1;
+        uint32_t anc = live ? (1u << lane) : 0u;
+        for (int p_ = par, step = 0; step < kMaxRows; ++step) {
+            const bool up = p_ >= 0;
+            if (!__any_sync(kFull, up)) break;
+            if (up) anc |= 1u << p_;
+            const int pp = __shfl_sync(kFull, par, up ? p_ : 0);
+            p_ = up ? pp : -1;
         }
+        int nsub = 0;
+        for (int b = 0; b < n; ++b) {
+            const uint32_t m = __ballot_sync(kFull, live && ((anc >> b) & 1u));
+            if (lane == b) nsub = __popc(m);
+        }
+        int before = 0;   // subtree sizes of the earlier siblings
+        for (int q = 0; q < n; ++q) {
+            const int pq = __shfl_sync(kFull, par, q), nq = __shfl_sync(kFull, nsub, q);
+            if (live && q < lane && pq == par) before += nq;
+        }
+        int pre = __popc(anc) - 1;
+        for (int a = 0; a < n; ++a) {
+            const int ba = __shfl_sync(kFull, before, a);
+            if ((anc >> a) & 1u) pre += ba;
+        }
+        if (live) sm.order[pre] = lane;
+        __syncwarp();
+        if (live && pre > 0 && par >= 0 && par != sm.order[pre - 1]) sm.reused[par] = 1;
+        if constexpr (MODE == kTreeLog)
+            if (live) path_mask[lane] = (int)anc;
     }
     __syncthreads();
 
