@@ -217,13 +217,13 @@ int gdn_commit(const gdn_dims *dims, const gdn_cache *cache, const int32_t *slot
 /*
  * gdn_window_pooled, gdn_tree_pooled -- gdn_window / gdn_tree recording each
  * row in the cache itself, so that committing a row is a change of index
- * instead of a copy (the survey of the verify path's commit step: the kept
- * row can become the slot by an index swap; [P747] first note: each stream
- * keeps only its accepted rows).  The cache is then a pool of entries, some
- * holding committed states (named by slot[]), the others free.  Row r's
- * state and tail go to entry rec_slot[r] of cache->state and cache->tail,
- * bit for bit what gdn_window / gdn_tree write to rec_state[r] and
- * rec_tail[r]; y is the same too.
+ * instead of a copy ([P747] first note: each stream keeps only its accepted
+ * rows; [P932] MLX checkpoint note: only the accepted path is kept, so the
+ * kept row's record can simply become the slot).  The cache is then a pool
+ * of entries, some holding committed states (named by slot[]), the others
+ * free.  Row r's state and tail go to entry rec_slot[r] of cache->state and
+ * cache->tail, bit for bit what gdn_window / gdn_tree write to rec_state[r]
+ * and rec_tail[r]; y is the same too.
  *   rec_slot  device int32 [n_rows]: pool entries in [0, n_slots), distinct
  *             from each other and from every slot[s] of the call (the
  *             library checks only that each is in range and is not its own
