@@ -789,12 +789,31 @@ def _extra_decode(dev, stream, flush, reps, hbm):
         e1.record(stream)
         torch.cuda.synchronize()
         ms_nf = e0.elapsed_time(e1) / 50
+        # the same 24 steps with GDN_STEP_EARLY_STATE: each step's kernel before
+        # is the step of another layer, so its state, tail and weights may be
+        # read while that kernel finishes
+        graph_e = torch.cuda.CUDAGraph()
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            step24_early = lambda: [gdn.step_ex(d2, lw, lc, sl, lr, gdn.STEP_EARLY_STATE, side)
+                                    for lw, lc, lr in layers]
+            step24_early()
+            side.synchronize()
+            with torch.cuda.graph(graph_e, stream=side):
+                step24_early()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        ms_e = _timed(graph_e.replay, reps, stream, flush)
         b = 24 * decode_bytes(g2, S)
         dec[str(S)] = {"ms_per_24_layer_step": ms, "rows_per_s": S / (ms * 1e-3),
                        "algorithmic_gbs": b / (ms * 1e-3) / 1e9, "frac_hbm": b / (ms * 1e-3) / 1e9 / hbm,
                        "graph": {"ms_per_24_layer_step": ms_g, "rows_per_s": S / (ms_g * 1e-3),
                                  "algorithmic_gbs": b / (ms_g * 1e-3) / 1e9,
                                  "frac_hbm": b / (ms_g * 1e-3) / 1e9 / hbm},
+                       "graph_early_state": {"ms_per_24_layer_step": ms_e, "rows_per_s": S / (ms_e * 1e-3),
+                                             "algorithmic_gbs": b / (ms_e * 1e-3) / 1e9,
+                                             "frac_hbm": b / (ms_e * 1e-3) / 1e9 / hbm,
+                                             "call": "gdn_step_ex(..., GDN_STEP_EARLY_STATE): slot, state, tail "
+                                                     "and weights read while the previous layer's step finishes"},
                        "graph_no_l2_flush": {"ms_per_24_layer_step": ms_nf, "rows_per_s": S / (ms_nf * 1e-3),
                                              "note": "50 replays back to back, one event pair; the layers' "
                                                      "states stay in L2, so no HBM fraction is given"}}

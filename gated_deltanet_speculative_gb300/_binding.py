@@ -55,6 +55,8 @@ _I = ctypes.c_int32
 _SIGS = {
     "gdn_step": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _I,
                  ctypes.POINTER(c_rows), _P],
+    "gdn_step_ex": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _I,
+                    ctypes.POINTER(c_rows), ctypes.c_uint32, _P],
     "gdn_window": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _I, _I,
                    ctypes.POINTER(c_rows), _P, _P, _P],
     "gdn_tree": [ctypes.POINTER(c_dims), ctypes.POINTER(c_weights), ctypes.POINTER(c_cache), _P, _P, _P, _I, _I,
@@ -186,6 +188,21 @@ def step(dims: Dims, weights: dict, cache: dict, slot, rows: dict, stream=None):
     cw, cc, cr = _weights(dims, weights), _cache(dims, cache), _rows(dims, rows, S)
     _check("gdn_step", lib.gdn_step(ctypes.byref(dims.c()), ctypes.byref(cw), ctypes.byref(cc), _ptr(slot), S,
                                     ctypes.byref(cr), _stream_ptr(stream)))
+
+
+STEP_EARLY_STATE = 1
+
+
+def step_ex(dims: Dims, weights: dict, cache: dict, slot, rows: dict, flags: int = 0, stream=None):
+    """gdn_step with launch flags: STEP_EARLY_STATE promises that the kernel
+    queued just before on the stream writes none of slot, the cache or the
+    weights, so the step reads them while that kernel finishes."""
+    lib = load()
+    _need(slot, "slot", torch.int32)
+    S = slot.numel()
+    cw, cc, cr = _weights(dims, weights), _cache(dims, cache), _rows(dims, rows, S)
+    _check("gdn_step_ex", lib.gdn_step_ex(ctypes.byref(dims.c()), ctypes.byref(cw), ctypes.byref(cc), _ptr(slot), S,
+                                          ctypes.byref(cr), int(flags), _stream_ptr(stream)))
 
 
 def window(dims: Dims, weights: dict, cache: dict, slot, row_ptr, rows: dict, rec_state, rec_tail, stream=None):

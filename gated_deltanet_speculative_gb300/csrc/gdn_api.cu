@@ -177,7 +177,7 @@ int encode_row_maps(gdn::RowParams &p, int D, int n_rows) {
 int rows_entry(int mode, const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
                const int32_t *row_ptr, const int32_t *parent, int32_t n_streams, int32_t n_rows,
                const gdn_rows *rows, float *rec_state, void *rec_tail, void *stream, LogBuffers logs = {},
-               const int32_t *rec_slot = nullptr) {
+               const int32_t *rec_slot = nullptr, bool early_state = false) {
     GDN_TRY(check_dims(dims));
     GDN_TRY(check_weights(w));
     GDN_TRY(check_cache(cache));
@@ -210,6 +210,7 @@ int rows_entry(int mode, const gdn_dims *dims, const gdn_weights *w, const gdn_c
     p.log_a = logs.a;
     p.log_u = logs.u;
     p.log_k = logs.k;
+    p.early_state = early_state ? 1 : 0;
     if (mode != gdn::kStep && dims->d_k >= 64) GDN_TRY(encode_row_maps(p, dims->d_k, n_rows));
     return launch_rows(dims->d_k, mode, p, n_streams, stream);
 }
@@ -334,6 +335,13 @@ int gdn_step(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
              int32_t n_streams, const gdn_rows *rows, void *stream) {
     return rows_entry(gdn::kStep, dims, w, cache, slot, nullptr, nullptr, n_streams, n_streams, rows, nullptr,
                       nullptr, stream);
+}
+
+int gdn_step_ex(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,
+                int32_t n_streams, const gdn_rows *rows, uint32_t flags, void *stream) {
+    if (flags & ~(uint32_t)GDN_STEP_EARLY_STATE) return GDN_EINVAL;
+    return rows_entry(gdn::kStep, dims, w, cache, slot, nullptr, nullptr, n_streams, n_streams, rows, nullptr,
+                      nullptr, stream, LogBuffers{}, nullptr, (flags & GDN_STEP_EARLY_STATE) != 0);
 }
 
 int gdn_window(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache, const int32_t *slot,

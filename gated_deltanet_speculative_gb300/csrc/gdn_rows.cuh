@@ -73,6 +73,8 @@ struct RowParams {
     float *log_u;             // [R, Hv, D] write u = b (v - a S k) (logged modes)
     float *log_k;             // [R, Hk, D] normalised key (logged modes)
     int *err;                 // device error word
+    int early_state;          // steps: read slot, state, tail and weights before the wait (the kernel
+                              // before this one writes none of them)
     // d >= 64: tensor maps of the staged inputs (TMA), encoded per call on the host
     int box_rows;             // rows of one mixed / z box: 1 for steps, min(16, R) otherwise
     CUtensorMap map_mixed;    // [R rows][CH] bf16, box [box_rows][D]
@@ -233,34 +235,74 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kh = h / p.G;
     const size_t CH = (size_t)p.CH;
+    // The slot word, the conv and norm weights, and (steps) the state tile
+    // and the committed tail: issued by issue_state(), before the wait for a
+    // step launched with early_state, else after it.
+    int sl = 0;
+    float A_log = 0.0f, dt_bias = 0.0f;
+    float S[RPW][CPL];
+    const size_t tile = (size_t)D * D;
+    auto issue_state = [&](bool tile_and_tail) {
+        sl = __ldg(p.slot + s);
+        for (int i = tid; i < 3 * D / 2; i += kRowThreads) {   // two channels (16 bytes) per copy
+            const int part = i / (D / 2), e0 = (i - part * (D / 2)) * 2;
+            cp_async16(&sm.cw[part * D + e0][0], p.conv_w + (size_t)channel_of<D>(part, e0, p.Hk, kh, h) * 4);
+        }
+        if (tid < D / 8) cp_async16(&sm.nw[tid * 8], p.norm_w + tid * 8);
+        A_log = __ldg(p.A_log + h);
+        dt_bias = __ldg(p.dt_bias + h);
+        if (tile_and_tail && sl >= 0 && sl < p.n_slots) {
+            load_tile<D, RPW, CPL>(S, p.state + ((size_t)sl * p.Hv + h) * tile + (size_t)row0 * D, warp, lane);
+            const uint16_t *tl = p.tail + (size_t)sl * 3 * CH;
+            for (int i = tid; i < 3 * CHUNKS; i += kRowThreads) {   // the three committed tail rows
+                const int row = i / CHUNKS, ch = i - row * CHUNKS;
+                const int part = ch / SEG, off = (ch - part * SEG) * 8;
+                cp_async16(&sm.u.xin[part][row][off], tl + (size_t)row * CH + channel_of<D>(part, off, p.Hk, kh, h));
+            }
+        }
+    };
+    const bool early = MODE == kStep && p.early_state;   // uniform over the grid
     if constexpr (MODE == kStep) {
-        // While the kernel before this step finishes, ask L2 for what the step
-        // reads that no kernel of the layer loop writes: this slice of the
-        // committed state tile, the head's conv weights and tail, and the
-        // step's input row.  Prefetches only move lines into L2, which every
-        // write reaches, so they cannot change a result.  The slot word is
-        // read on the L2 path (no L1 line survives across the wait) and only
-        // chooses what to prefetch; the step reads it again after the wait.
-        if (warp == 0) {
-            const int sl0 = __ldcg(p.slot + s);
-            if (sl0 >= 0 && sl0 < p.n_slots) {
-                if (lane == 0)
-                    prefetch_l2_bulk(p.state + ((size_t)sl0 * p.Hv + h) * D * D + (size_t)row0 * D,
-                                     (uint32_t)(D / P * D * 4));
-                if (sli == 0 && lane >= 1 && lane <= 9) {   // tail rows x (q, k, v) segments
-                    const int m = (lane - 1) / 3, part = (lane - 1) % 3;
-                    prefetch_l2_bulk(p.tail + ((size_t)sl0 * 3 + m) * CH + channel_of<D>(part, 0, p.Hk, kh, h),
+        if (early) {
+            // The kernel before writes none of the slot words, the cache or
+            // the weights (the caller's promise): read them now, while it
+            // finishes; only the row's inputs wait.
+            issue_state(true);
+            if (warp == 0 && sli == 0) {   // ask L2 for the input row's q, k, v segments and z
+                if (lane >= 10 && lane <= 12)
+                    prefetch_l2_bulk(p.mixed + (size_t)s * CH + channel_of<D>(lane - 10, 0, p.Hk, kh, h),
                                      (uint32_t)(D * 2));
+                if (lane == 13) prefetch_l2_bulk(p.z + ((size_t)s * p.Hv + h) * D, (uint32_t)(D * 2));
+            }
+        } else {
+            // While the kernel before this step finishes, ask L2 for what the step
+            // reads that no kernel of the layer loop writes: this slice of the
+            // committed state tile, the head's conv weights and tail, and the
+            // step's input row.  Prefetches only move lines into L2, which every
+            // write reaches, so they cannot change a result.  The slot word is
+            // read on the L2 path (no L1 line survives across the wait) and only
+            // chooses what to prefetch; the step reads it again after the wait.
+            if (warp == 0) {
+                const int sl0 = __ldcg(p.slot + s);
+                if (sl0 >= 0 && sl0 < p.n_slots) {
+                    if (lane == 0)
+                        prefetch_l2_bulk(p.state + ((size_t)sl0 * p.Hv + h) * D * D + (size_t)row0 * D,
+                                         (uint32_t)(D / P * D * 4));
+                    if (sli == 0 && lane >= 1 && lane <= 9) {   // tail rows x (q, k, v) segments
+                        const int m = (lane - 1) / 3, part = (lane - 1) % 3;
+                        prefetch_l2_bulk(p.tail + ((size_t)sl0 * 3 + m) * CH + channel_of<D>(part, 0, p.Hk, kh, h),
+                                         (uint32_t)(D * 2));
+                    }
                 }
-            }
-            if (sli == 0 && lane >= 10 && lane <= 12) {   // the input row's q, k, v segments
-                const int part = lane - 10;
-                prefetch_l2_bulk(p.mixed + (size_t)s * CH + channel_of<D>(part, 0, p.Hk, kh, h), (uint32_t)(D * 2));
-            }
-            if (sli == 0 && lane == 13) prefetch_l2_bulk(p.z + ((size_t)s * p.Hv + h) * D, (uint32_t)(D * 2));
-            if (sli == 0 && lane >= 14 && lane <= 16) {   // conv weights of the three segments
-                const int part = lane - 14;
-                prefetch_l2_bulk(p.conv_w + (size_t)channel_of<D>(part, 0, p.Hk, kh, h) * 4, (uint32_t)(D * 8));
+                if (sli == 0 && lane >= 10 && lane <= 12) {   // the input row's q, k, v segments
+                    const int part = lane - 10;
+                    prefetch_l2_bulk(p.mixed + (size_t)s * CH + channel_of<D>(part, 0, p.Hk, kh, h), (uint32_t)(D * 2));
+                }
+                if (sli == 0 && lane == 13) prefetch_l2_bulk(p.z + ((size_t)s * p.Hv + h) * D, (uint32_t)(D * 2));
+                if (sli == 0 && lane >= 14 && lane <= 16) {   // conv weights of the three segments
+                    const int part = lane - 14;
+                    prefetch_l2_bulk(p.conv_w + (size_t)channel_of<D>(part, 0, p.Hk, kh, h) * 4, (uint32_t)(D * 8));
+                }
             }
         }
         asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -275,20 +317,14 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
     const bool lead = (h % p.G) == 0;    // this CTA writes the q/k channels shared by its key-head group
 
     // ---- a1: the stream's slot and rows (the same few words in every thread)
-    const int sl = __ldg(p.slot + s);
+    // While those words are in flight: the conv and norm weights (independent
+    // of every index), so that no later phase waits on a load of its own.
+    if (!early) issue_state(false);
     int r0 = s, n = 1;
     if (MODE != kStep) {
         r0 = __ldg(p.row_ptr + s);
         n = __ldg(p.row_ptr + s + 1) - r0;
     }
-    // While those words are in flight: the conv and norm weights (independent
-    // of every index), so that no later phase waits on a load of its own.
-    for (int i = tid; i < 3 * D / 2; i += kRowThreads) {   // two channels (16 bytes) per copy
-        const int part = i / (D / 2), e0 = (i - part * (D / 2)) * 2;
-        cp_async16(&sm.cw[part * D + e0][0], p.conv_w + (size_t)channel_of<D>(part, e0, p.Hk, kh, h) * 4);
-    }
-    if (tid < D / 8) cp_async16(&sm.nw[tid * 8], p.norm_w + tid * 8);
-    const float A_log = __ldg(p.A_log + h), dt_bias = __ldg(p.dt_bias + h);
     {
         int bad = (sl < 0 || sl >= p.n_slots) ? GDN_DERR_SLOT : 0;
         if (MODE != kStep && (r0 < 0 || n < 0 || n > kMaxRows || r0 > p.n_rows - n)) bad |= GDN_DERR_ROWS;
@@ -301,10 +337,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
 
     // The committed state tile goes to registers; the loads stay in flight
     // while the conv inputs are staged and processed.
-    const size_t tile = (size_t)D * D;
     float *slot_tile = p.state + ((size_t)sl * p.Hv + h) * tile;
-    float S[RPW][CPL];
-    load_tile<D, RPW, CPL>(S, slot_tile + (size_t)row0 * D, warp, lane);
+    if (!early) load_tile<D, RPW, CPL>(S, slot_tile + (size_t)row0 * D, warp, lane);
 
     // Stage the committed tail and the window's rows (this head's q, k and v
     // channels) and the z rows into shared memory.  d >= 64: seven TMA box
@@ -329,7 +363,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
             tc::tma_load_3d(&sm.z[0][0], &p.map_z, 0, h, r0, &stage_bar);
         }
     } else {
-        for (int i = tid; i < (n + 3) * CHUNKS; i += kRowThreads) {
+        for (int i = early ? 3 * CHUNKS + tid : tid; i < (n + 3) * CHUNKS; i += kRowThreads) {   // (early: tail staged)
             const int row = i / CHUNKS, ch = i - row * CHUNKS;
             const int part = ch / SEG, off = (ch - part * SEG) * 8;
             const int c = channel_of<D>(part, off, p.Hk, kh, h);

@@ -147,6 +147,30 @@ int gdn_step(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
              const int32_t *slot, int32_t n_streams, const gdn_rows *rows,
              void *stream);
 
+/* Flags of gdn_step_ex. */
+#define GDN_STEP_EARLY_STATE 1u
+
+/*
+ * gdn_step_ex -- gdn_step with launch flags (not in the pages: a latency
+ * option of the layer loop that [P932]'s note on capturing a forward's
+ * launches is about).
+ *   flags  0: exactly gdn_step.
+ *          GDN_STEP_EARLY_STATE: the caller promises that the kernel launched
+ *          just before this one on `stream` writes none of slot[],
+ *          cache->state, cache->tail and the weights (true, for example, of
+ *          a step of another layer, with its own cache).  The step's CTAs
+ *          then read the slot words, their rows of the state tile, the
+ *          committed tail and the weights while that kernel finishes, and
+ *          only the rows' inputs (mixed, z, a, b) after it; its writes (the
+ *          state and tail in place, y) still wait for it.  The results are
+ *          those of gdn_step, bit for bit.  A broken promise gives wrong
+ *          results (stale state), never a fault.
+ *          Any other bit: GDN_EINVAL.
+ */
+int gdn_step_ex(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
+                const int32_t *slot, int32_t n_streams, const gdn_rows *rows,
+                uint32_t flags, void *stream);
+
 /*
  * gdn_window -- chain verify windows (at most 16 rows a stream), recorded
  * row by row ([P932] MLX checkpoint note: every row's state and conv tail

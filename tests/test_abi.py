@@ -191,3 +191,18 @@ def test_commit_refuses_a_missing_or_misaligned_row_ptr():
     assert lib.gdn_commit(ctypes.byref(d), ctypes.byref(c), A16, A16 + 2, A16, 2, 4, A16, A16, None) == -3
     assert lib.gdn_prefill_workspace(ctypes.byref(d), 1, 4722, 64) == \
         lib.gdn_prefill_workspace_size(ctypes.byref(d), 1, 4722, 64) > 0
+
+
+def test_step_ex_refuses_unknown_flags_and_bad_arguments():
+    lib = gdn.load()
+    d, w, c, r = _args()
+    assert lib.gdn_step_ex(ctypes.byref(d), ctypes.byref(w), ctypes.byref(c), A16, 2, ctypes.byref(r), 2,
+                           None) == -1
+    assert lib.gdn_step_ex(ctypes.byref(d), ctypes.byref(w), ctypes.byref(c), A16, 2, ctypes.byref(r), 0x80000000,
+                           None) == -1
+    assert lib.gdn_step_ex(ctypes.byref(d), ctypes.byref(w), ctypes.byref(c), None, 2, ctypes.byref(r),
+                           B.STEP_EARLY_STATE, None) == -2
+    assert lib.gdn_step_ex(ctypes.byref(d), ctypes.byref(w), ctypes.byref(c), A16 + 2, 2, ctypes.byref(r),
+                           B.STEP_EARLY_STATE, None) == -3
+    assert lib.gdn_step_ex(ctypes.byref(d), ctypes.byref(w), ctypes.byref(c), A16, 0, ctypes.byref(r),
+                           B.STEP_EARLY_STATE, None) == -1

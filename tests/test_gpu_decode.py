@@ -88,3 +88,57 @@ def test_dependent_steps_captured_in_a_graph_equal_eager_bitwise(n_streams):
     torch.cuda.synchronize()
     assert np.array_equal(e_cache["state"].cpu().numpy().view(np.uint32), got_s)
     assert np.array_equal(host_bits(e_cache["tail"]), got_t)
+
+
+@pytest.mark.parametrize("n_streams", [1, 4, 16])
+def test_early_state_steps_of_24_layers_equal_plain_steps_bitwise(n_streams):
+    """gdn_step_ex with GDN_STEP_EARLY_STATE over 24 layers (each step's
+    previous kernel is the step of another layer, so the promise holds),
+    eager and captured in a graph, equals plain gdn_step calls bit for bit:
+    y, every layer's state and tail."""
+    cases = [Case(synth.LIKE_2B, [1] * n_streams, seed=7 + 100 * layer) for layer in range(LAYERS)]
+    dims = cases[0].dims_gpu()
+
+    def layers():
+        return [(c.dev_weights(), c.dev_cache(), c.dev_rows(), dev(c.slots)) for c in cases]
+
+    def results(ls):
+        torch.cuda.synchronize()
+        return [(host_bits(r["y"]), cache["state"].cpu().numpy().view(np.uint32), host_bits(cache["tail"]))
+                for _, cache, r, _ in ls]
+
+    plain = layers()
+    for w, cache, rows, slot in plain:
+        gdn.step(dims, w, cache, slot, rows)
+    want = results(plain)
+    early = layers()
+    for w, cache, rows, slot in early:
+        gdn.step_ex(dims, w, cache, slot, rows, gdn.STEP_EARLY_STATE)
+    assert gdn.get_device_error() == 0
+    for l, (a, b) in enumerate(zip(results(early), want)):
+        for x, y_, what in zip(a, b, ("y", "state", "tail")):
+            assert np.array_equal(x, y_), f"eager layer {l} {what}"
+    graphed = layers()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    warm = layers()
+    with torch.cuda.stream(side):
+        for w, cache, rows, slot in warm:   # warm, outside the capture
+            gdn.step_ex(dims, w, cache, slot, rows, gdn.STEP_EARLY_STATE, side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            for w, cache, rows, slot in graphed:
+                gdn.step_ex(dims, w, cache, slot, rows, gdn.STEP_EARLY_STATE, side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    fresh = layers()   # the capture did not run the steps: reset the graphed buffers to the start
+    for (_, c0, r0, _), (_, c1, r1, _) in zip(graphed, fresh):
+        c0["state"].copy_(c1["state"])
+        c0["tail"].copy_(c1["tail"])
+        r0["y"].copy_(r1["y"])
+    graph.replay()
+    assert gdn.get_device_error() == 0
+    for l, (a, b) in enumerate(zip(results(graphed), want)):
+        for x, y_, what in zip(a, b, ("y", "state", "tail")):
+            assert np.array_equal(x, y_), f"graphed layer {l} {what}"
