@@ -90,13 +90,17 @@ def test_dependent_steps_captured_in_a_graph_equal_eager_bitwise(n_streams):
     assert np.array_equal(host_bits(e_cache["tail"]), got_t)
 
 
-@pytest.mark.parametrize("n_streams", [1, 4, 16])
-def test_early_state_steps_of_24_layers_equal_plain_steps_bitwise(n_streams):
+@pytest.mark.parametrize("g,n_streams", [(synth.LIKE_2B, 1), (synth.LIKE_2B, 4), (synth.LIKE_2B, 16),
+                                         (synth.Geometry(2, 6, 128, 128), 1), (synth.Geometry(2, 6, 128, 128), 5),
+                                         (synth.Geometry(2, 4, 64, 64), 3), (synth.Geometry(2, 4, 32, 32), 2)],
+                         ids=["2b-1", "2b-4", "2b-16", "g3-1", "g3-5", "d64-3", "d32-2"])
+def test_early_state_steps_of_24_layers_equal_plain_steps_bitwise(g, n_streams):
     """gdn_step_ex with GDN_STEP_EARLY_STATE over 24 layers (each step's
     previous kernel is the step of another layer, so the promise holds),
     eager and captured in a graph, equals plain gdn_step calls bit for bit:
-    y, every layer's state and tail."""
-    cases = [Case(synth.LIKE_2B, [1] * n_streams, seed=7 + 100 * layer) for layer in range(LAYERS)]
+    y, every layer's state and tail (sliced and unsliced steps, clusters of
+    one and of three value heads, d = 32, 64 and 128)."""
+    cases = [Case(g, [1] * n_streams, seed=7 + 100 * layer) for layer in range(LAYERS)]
     dims = cases[0].dims_gpu()
 
     def layers():
