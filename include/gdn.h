@@ -156,9 +156,10 @@ int gdn_step(const gdn_dims *dims, const gdn_weights *w, const gdn_cache *cache,
  * launches is about).
  *   flags  0: exactly gdn_step.
  *          GDN_STEP_EARLY_STATE: the caller promises that the kernel launched
- *          just before this one on `stream` writes none of slot[],
- *          cache->state, cache->tail and the weights (true, for example, of
- *          a step of another layer, with its own cache).  The step's CTAs
+ *          just before this one on `stream` writes none of slot[], the
+ *          state and tail entries slot[] names, and the weights (true, for
+ *          example, of a step of another layer: its own cache, or other
+ *          entries of a shared one).  The step's CTAs
  *          then read the slot words, their rows of the state tile, the
  *          committed tail and the weights while that kernel finishes, and
  *          only the rows' inputs (mixed, z, a, b) after it; its writes (the
