@@ -90,9 +90,15 @@ def library_path() -> str:
     return _build.LIB
 
 
+_capture = threading.local()   # prepare(): the recorder that stands in for the library
+
+
 def load(build_if_missing: bool = True):
     """Load libgdn.so (building it first if it is missing or stale)."""
     global _lib
+    rec = getattr(_capture, "rec", None)
+    if rec is not None:
+        return rec
     with _lock:
         if _lib is None:
             path = _build.build() if build_if_missing else _build.LIB
@@ -107,6 +113,53 @@ def load(build_if_missing: bool = True):
                               "gdn_prefill_workspace": ctypes.c_size_t}.get(name, ctypes.c_int)
             _lib = lib
     return _lib
+
+
+class _Recorder:
+    """Records the library call a binding function makes instead of making it."""
+
+    def __init__(self, lib):
+        self._lib = lib
+        self.calls = []
+
+    def __getattr__(self, name):
+        fn = getattr(self._lib, name)
+
+        def record(*cargs):
+            self.calls.append((name, fn, cargs))
+            return 0
+        return record
+
+
+class PreparedCall:
+    """One entry point with its arguments checked and marshalled once.
+
+    Calling it enqueues the same C call on the given stream (default: the
+    current one) with a single ctypes call.  The tensors it was prepared
+    with must stay allocated and keep their shapes; their contents may
+    change between calls (new rows, new keep rows), as in a serving loop."""
+
+    def __init__(self, name, cfn, cargs, keep):
+        self.name, self._cfn, self._cargs, self._keep = name, cfn, cargs, keep
+
+    def __call__(self, stream=None):
+        _check(self.name, self._cfn(*self._cargs, _stream_ptr(stream)))
+
+
+def prepare(fn, *args, **kwargs) -> PreparedCall:
+    """Check and marshal the arguments of a compute call once, e.g.
+    ``prepare(step, dims, weights, cache, slot, rows)``; the result enqueues
+    that call when called (its stream is the C call's last argument)."""
+    rec = _Recorder(load())
+    _capture.rec = rec
+    try:
+        fn(*args, stream=0, **kwargs)
+    finally:
+        _capture.rec = None
+    if len(rec.calls) != 1:
+        raise ValueError(f"{getattr(fn, '__name__', fn)} is not a single compute call")
+    name, cfn, cargs = rec.calls[0]
+    return PreparedCall(name, cfn, cargs[:-1], (args, kwargs))
 
 
 class Dims:

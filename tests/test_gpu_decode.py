@@ -146,3 +146,35 @@ def test_early_state_steps_of_24_layers_equal_plain_steps_bitwise(g, n_streams):
     for l, (a, b) in enumerate(zip(results(graphed), want)):
         for x, y_, what in zip(a, b, ("y", "state", "tail")):
             assert np.array_equal(x, y_), f"graphed layer {l} {what}"
+
+
+def test_prepared_steps_equal_direct_calls_bitwise():
+    """gdn.prepare checks and marshals a call once; calling the prepared
+    steps of 24 layers (twice, the rows' contents changed in between) gives
+    what direct gdn_step / gdn_step_ex calls give, bit for bit."""
+    cases = [Case(synth.LIKE_2B, [1] * 2, seed=41 + 100 * layer) for layer in range(LAYERS)]
+    dims = cases[0].dims_gpu()
+    direct = [(c.dev_weights(), c.dev_cache(), c.dev_rows(), dev(c.slots)) for c in cases]
+    prep = [(c.dev_weights(), c.dev_cache(), c.dev_rows(), dev(c.slots)) for c in cases]
+    calls = [gdn.prepare(gdn.step_ex, dims, w, cache, slot, rows, gdn.STEP_EARLY_STATE) if i % 2
+             else gdn.prepare(gdn.step, dims, w, cache, slot, rows)
+             for i, (w, cache, rows, slot) in enumerate(prep)]
+    for rnd in range(2):
+        if rnd:   # new inputs in the same buffers
+            for (_, _, r0, _), (_, _, r1, _) in zip(direct, prep):
+                for k in ("mixed", "z", "a", "b"):
+                    r0[k].copy_(torch.roll(r0[k], 1, dims=-1))
+                    r1[k].copy_(r0[k])
+        for i, (w, cache, rows, slot) in enumerate(direct):
+            if i % 2:
+                gdn.step_ex(dims, w, cache, slot, rows, gdn.STEP_EARLY_STATE)
+            else:
+                gdn.step(dims, w, cache, slot, rows)
+        for call in calls:
+            call()
+        torch.cuda.synchronize()
+        assert gdn.get_device_error() == 0
+        for l, ((_, c0, r0, _), (_, c1, r1, _)) in enumerate(zip(direct, prep)):
+            assert np.array_equal(host_bits(r0["y"]), host_bits(r1["y"])), f"round {rnd} layer {l} y"
+            assert np.array_equal(c0["state"].cpu().numpy().view(np.uint32), c1["state"].cpu().numpy().view(np.uint32))
+            assert np.array_equal(host_bits(c0["tail"]), host_bits(c1["tail"]))

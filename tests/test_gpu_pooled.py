@@ -274,3 +274,47 @@ def test_pooled_round_swap_then_step_back_to_back_equals_copy_path():
     for s in range(c.S):
         assert np.array_equal(pst[cur[s]].view(np.uint32), st[c.slots[s]].view(np.uint32)), f"state {s}"
         assert np.array_equal(ptl[cur[s]], tl[c.slots[s]]), f"tail {s}"
+
+
+def test_prepared_pooled_rounds_equal_direct_calls_bitwise():
+    """Three pooled rounds (window + index commit) through prepared calls,
+    the rows, pool entries and keep rows refilled in the same buffers each
+    round, against the same rounds through direct calls."""
+    g = synth.Geometry(2, 6, 128, 128)
+    S, W = 4, 16
+    base = Case(g, [W] * S, seed=197, n_slots=S)
+    d = base.dims_gpu()
+    rng = np.random.default_rng(197)
+    sides = []
+    for _ in range(2):
+        pool, n_pool = pool_of(base, 3 * S * W)
+        sides.append({"w": base.dev_weights(), "pool": pool, "slot": dev(base.slots.copy()),
+                      "rp": dev(base.row_ptr), "rows": base.dev_rows(),
+                      "rec": torch.zeros(S * W, dtype=torch.int32, device="cuda"),
+                      "keep": torch.zeros(S, dtype=torch.int32, device="cuda")})
+    p = sides[1]
+    win = gdn.prepare(gdn.window_pooled, d, p["w"], p["pool"], p["slot"], p["rp"], p["rows"], p["rec"])
+    swap = gdn.prepare(gdn.commit_swap, d, p["pool"], p["slot"], p["rp"], p["keep"], p["rec"])
+    for rnd in range(3):
+        c = Case(g, [W] * S, seed=300 + rnd, n_slots=S)
+        acc = rng.integers(0, W + 1, size=S)
+        keep = np.where(acc > 0, c.row_ptr[:-1] + acc - 1, -1).astype(np.int32)
+        rec = (S + rnd * S * W + rng.permutation(S * W)).astype(np.int32)   # fresh entries each round
+        for side in sides:
+            for k, v in c.dev_rows().items():
+                side["rows"][k].copy_(v)
+            side["rec"].copy_(dev(rec))
+            side["keep"].copy_(dev(keep))
+        q = sides[0]
+        gdn.window_pooled(d, q["w"], q["pool"], q["slot"], q["rp"], q["rows"], q["rec"])
+        gdn.commit_swap(d, q["pool"], q["slot"], q["rp"], q["keep"], q["rec"])
+        win()
+        swap()
+        torch.cuda.synchronize()
+        assert gdn.get_device_error() == 0
+        assert np.array_equal(host_bits(q["rows"]["y"]), host_bits(p["rows"]["y"])), f"y round {rnd}"
+        assert np.array_equal(q["slot"].cpu().numpy(), p["slot"].cpu().numpy())
+        cur = p["slot"].cpu().numpy()
+        a, b = q["pool"]["state"].cpu().numpy(), p["pool"]["state"].cpu().numpy()
+        for s_ in range(S):
+            assert np.array_equal(a[cur[s_]].view(np.uint32), b[cur[s_]].view(np.uint32)), f"round {rnd} stream {s_}"
