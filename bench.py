@@ -900,6 +900,42 @@ def oracle_rounds(budget_s: float, min_rounds: int = 1, max_streams=None, thread
     return done_rows, t_total, threads, s
 
 
+def oracle_other_workloads():
+    """The oracle on the other rows' workloads, whole, on all host cores:
+    the 24-layer 2B-like decode step at one stream, and the two prefill
+    passes (the sequential recurrence, token by token)."""
+    import oracle
+
+    threads = os.cpu_count() or 1
+    out = {}
+    g2 = synth.LIKE_2B
+    od2 = oracle.Dims(g2.n_k_heads, g2.n_v_heads, g2.d_k, g2.d_v)
+    layers = [(synth.layer_weights(g2, 1 + 100 * l), synth.slot_cache(g2, 1, 1 + 100 * l),
+               synth.row_inputs(g2, 1, 1 + 100 * l)) for l in range(24)]
+    t = time.perf_counter()
+    for w2, c2, r2 in layers:
+        oracle.gdn_rows(od2, w2, c2["state"][0], c2["tail"][0], r2["mixed"], r2["z"], r2["a"], r2["b"],
+                        record=False, final=True, threads=threads)
+    dt = time.perf_counter() - t
+    out["decode_24_layers_2b_like_1_stream"] = {"ms_per_24_layer_step": dt * 1e3, "rows_per_s": 1 / dt}
+    g = GEOM
+    od = oracle.Dims(g.n_k_heads, g.n_v_heads, g.d_k, g.d_v)
+    for name, lengths in (("prefill_i_4722", [4722]), ("prefill_ii_512_1024_2048_4096", [512, 1024, 2048, 4096])):
+        w = synth.layer_weights(g, 4)
+        cache = synth.slot_cache(g, len(lengths), 4, zero=True)
+        rows = synth.row_inputs(g, sum(lengths), 4)
+        cu = synth.row_ptr(lengths)
+        t = time.perf_counter()
+        for s_ in range(len(lengths)):
+            lo, hi = int(cu[s_]), int(cu[s_ + 1])
+            oracle.gdn_rows(od, w, cache["state"][s_], cache["tail"][s_], rows["mixed"][lo:hi], rows["z"][lo:hi],
+                            rows["a"][lo:hi], rows["b"][lo:hi], record=False, final=True, threads=threads)
+        dt = time.perf_counter() - t
+        out[name] = {"ms": dt * 1e3, "tokens_per_s": sum(lengths) / dt}
+    out["cores"] = threads
+    return out
+
+
 def cpu_baseline():
     rows, secs, threads, streams = oracle_rounds(10.0)
     rows1, secs1, _, streams1 = oracle_rounds(3.0, threads=1)
@@ -908,7 +944,8 @@ def cpu_baseline():
                       f"{secs:.1f} s of oracle time, heads split over {threads} threads",
             "single_thread": {"value": rows1 / secs1, "unit": "rows/s", "cores": 1,
                               "sample": f"{streams1} stream windows of 16 rows, {secs1:.1f} s, one thread "
-                                        f"(the plain sequential definition)"}}
+                                        f"(the plain sequential definition)"},
+            "other_workloads": oracle_other_workloads()}
 
 
 def run_reference(args, rank, world):
