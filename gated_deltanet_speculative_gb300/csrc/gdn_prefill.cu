@@ -150,7 +150,7 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
     PrefillParams p = p0;
     p.c_lo = 0;
     p.c_hi = p.max_chunks;
-    const dim3 norm_grid(p.Hv, p.max_chunks);   // every chunk of the pass
+    const dim3 norm_grid(p.Hv * kNormSplit, p.max_chunks);   // every chunk of the pass
     cudaError_t e;
     if constexpr (TC) {
         e = cudaFuncSetAttribute(gdn_prefill_prep_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -213,7 +213,7 @@ cudaError_t launch(const PrefillParams &p0, cudaStream_t st, bool pipelined) {
             gdn_prefill_scan_tc_kernel<C><<<dim3(p.Hv, p.n_seqs), kScanTcThreads, kScanTcSmem, ss->stream>>>(p);
             if ((e = cudaEventRecord(ss->scanned, ss->stream)) != cudaSuccess) return e;
             if ((e = cudaStreamWaitEvent(ss->norm, ss->scanned, 0)) != cudaSuccess) return e;
-            gdn_prefill_norm_chunks_kernel<D, C><<<dim3(p.Hv, p.c_hi - p.c_lo), kNormThreads, 0, ss->norm>>>(p);
+            gdn_prefill_norm_chunks_kernel<D, C><<<dim3(p.Hv * kNormSplit, p.c_hi - p.c_lo), kNormThreads, 0, ss->norm>>>(p);
         }
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // ... and the caller's stream continues after all of it (the last

@@ -62,6 +62,7 @@ constexpr int kPrefillChunk = 64;
 constexpr uint32_t kPrepWaitLimit = 1u << 22;
 constexpr int kPrepThreads = 256;
 constexpr int kNormThreads = 256;
+constexpr int kNormSplit = 4;   // norm CTAs per (value head, chunk)
 
 // Floats of one (chunk, head) block of the workspace.
 template <int D, int C>
@@ -1567,7 +1568,9 @@ __device__ __forceinline__ void norm_item(const PrefillParams &p, size_t item, i
 template <int D, int C>
 __global__ void __launch_bounds__(kNormThreads) gdn_prefill_norm_chunks_kernel(const PrefillParams p) {
     __shared__ int info[2];
-    const int h = blockIdx.x, gc = p.c_lo + blockIdx.y;
+    // blockIdx.x = head * kNormSplit + part: each CTA takes C / kNormSplit of
+    // its chunk's tokens, so that a CTA is short and hands its SM back soon
+    const int h = blockIdx.x / kNormSplit, part = blockIdx.x % kNormSplit, gc = p.c_lo + blockIdx.y;
     if (threadIdx.x == 0) {
         int seq = -1, start = 0, n = 0, seq_start = 0, bad = 0;
         const bool ok = locate_chunk(p, C, gc, seq, start, n, seq_start, bad);
@@ -1577,7 +1580,9 @@ __global__ void __launch_bounds__(kNormThreads) gdn_prefill_norm_chunks_kernel(c
     }
     __syncthreads();
     const int n = info[0], start = info[1];
-    for (int t = threadIdx.x >> 5; t < n; t += kNormThreads / 32)
+    constexpr int TPC = C / kNormSplit;   // tokens of this CTA
+    const int t_end = min(n, (part + 1) * TPC);
+    for (int t = part * TPC + (threadIdx.x >> 5); t < t_end; t += kNormThreads / 32)
         norm_item<D>(p, (size_t)(start + t) * p.Hv + h, threadIdx.x & 31);
 }
 
