@@ -54,6 +54,16 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Sum over the 32 lanes with the xor butterfly 1, 2, 4, 8, 16: after the
+// first k levels every aligned group of 2^k lanes holds its own sum, so a
+// sum split into aligned lane groups (and finished from the groups' sums in
+// the same pairwise order) has the same bits as the whole.
+__device__ __forceinline__ float warp_sum_up(float v) {
+#pragma unroll
+    for (int off = 1; off <= 16; off <<= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, off));
+    return v;
+}
+
 // Reduce-scatter of N partial sums (N a power of two, 2..32) across the 32
 // lanes.  On return lane l holds the total of value (l >> (5 - log2 N)).
 // The association is the same xor butterfly as warp_sum (partners l^16,

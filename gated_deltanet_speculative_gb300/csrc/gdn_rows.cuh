@@ -209,12 +209,18 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
     static_assert(NV >= 2 && NV <= 32, "unsupported head width");
     constexpr bool TREE = MODE == kTree || MODE == kTreeLog;
     constexpr bool LOG = MODE == kWindowLog || MODE == kTreeLog;
+    // sliced RMSNorm: exchange per-slice partial sums (P >= 4) or gather the
+    // o rows (P = 2; measured faster there)
+    constexpr bool kPartials = P >= 4;
 
     __shared__ RowSmem<D> sm;
     __shared__ __align__(8) uint64_t stage_bar;   // TMA staging completes here
     __shared__ int stage_fail;                    // a staging wait gave up
     // the whole o vector of each row, gathered from the slices
+    // sliced: this slice's o rows (at their row index), and every slice's
+    // partial sum of o^2 per row, gathered through distributed shared memory
     __shared__ float o_all[P > 1 && MODE != kStep ? kMaxRows : 1][P > 1 ? D : 1];
+    __shared__ float part_all[P > 1 && MODE != kStep ? kMaxRows : 1][P];
     // logged trees: every row's write u (to rebuild a parent's state) and,
     // per node, the set of rows on its root-to-node path (bit m = row m)
     __shared__ float u_rows[MODE == kTreeLog ? kMaxRows : 1][MODE == kTreeLog ? D : 1];
@@ -635,10 +641,12 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
         if (lane >= 16 && (lane & ((1 << SHIFT) - 1)) == 0) {
             const int row = row0 + warp * RPW + vi - RPW;
             const float ov = __fmaf_rn(u_pair, sm.kq[t], __fmul_rn(dec, tot));
-            if constexpr (P > 1) {   // into every slice of this head (cluster ranks (h % G) * P + j)
+            if constexpr (P > 1 && !kPartials) {   // into every slice of this head (cluster ranks (h % G) * P + j)
 #pragma unroll
                 for (int j = 0; j < P; ++j)
                     st_cluster_f32(&o_all[MODE == kStep ? 0 : t][row], (uint32_t)(crank0 + j), ov);
+            } else if constexpr (P > 1) {
+                o_all[MODE == kStep ? 0 : t][row] = ov;
             } else {
                 sm.u.o[t][row] = ov;
             }
@@ -660,23 +668,73 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
         }
     }
     if (MODE == kStep) store_tile<D, RPW, CPL>(slot_tile + (size_t)row0 * D, S, warp, lane, false);
-    if constexpr (P > 1) {
+    if constexpr (P > 1 && !kPartials) {
         cluster_sync_all();   // every slice's o rows have landed in every slice
         if (MODE == kStep) shift_tail();   // and every slice has staged the old tail long ago
     } else {
-        __syncthreads();
+        __syncthreads();   // every warp's o rows are in shared memory
     }
 
     // ---- a7: gated RMSNorm, y in bf16 ----------------------------------------
-    for (int t = warp; t < n; t += kRowWarps) {
-        float ov[CPL];
-#pragma unroll
-        for (int c = 0; c < CPL; ++c)
-            ov[c] = P > 1 ? o_all[MODE == kStep ? 0 : t][lane * CPL + c] : sm.u.o[t][lane * CPL + c];
+    // Sum of o^2 over the row: lane l takes rows l*CPL .. l*CPL + CPL - 1,
+    // then the xor butterfly 1, 2, 4, .., 16.  Two slices gather each
+    // other's o rows and sum the whole row.  With more, a slice's rows are
+    // the aligned lane group [row0 / CPL, (row0 + D/P) / CPL): each slice
+    // sums its own group's levels, sends that partial to every slice of the
+    // head, and all finish the remaining levels from the P partials in the
+    // butterfly's pairwise order.  Either way the bits are the unsliced ones.
+    constexpr int GL = 32 / P;   // lanes of one slice's rows
+    auto lane_ss = [&](const float (&ov)[CPL]) {
         float ss = __fmul_rn(ov[0], ov[0]);
 #pragma unroll
         for (int c = 1; c < CPL; ++c) ss = __fmaf_rn(ov[c], ov[c], ss);
-        ss = warp_sum(ss);
+        return ss;
+    };
+    if constexpr (P > 1 && kPartials) {
+        for (int t = warp; t < n; t += kRowWarps) {
+            const bool mine = lane / GL == sli;
+            float ov[CPL];
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) ov[c] = mine ? o_all[MODE == kStep ? 0 : t][lane * CPL + c] : 0.0f;
+            float ss = lane_ss(ov);
+#pragma unroll
+            for (int off = 1; off < GL; off <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, off));
+            if (lane == sli * GL) {   // into every slice of this head (cluster ranks (h % G) * P + j)
+#pragma unroll
+                for (int j = 0; j < P; ++j)
+                    st_cluster_f32(&part_all[MODE == kStep ? 0 : t][sli], (uint32_t)(crank0 + j), ss);
+            }
+        }
+        cluster_sync_all();   // every slice's partials have landed in every slice
+        if (MODE == kStep) shift_tail();   // and every slice has staged the old tail long ago
+    }
+    for (int t = warp; t < n; t += kRowWarps) {
+        float ov[CPL];
+        float ss;
+        if constexpr (P > 1 && !kPartials) {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) ov[c] = o_all[MODE == kStep ? 0 : t][lane * CPL + c];
+            ss = warp_sum_up(lane_ss(ov));
+        } else if constexpr (P > 1) {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) ov[c] = o_all[MODE == kStep ? 0 : t][lane * CPL + c];   // own rows only
+            float v[P];
+#pragma unroll
+            for (int q = 0; q < P; ++q) v[q] = part_all[MODE == kStep ? 0 : t][q];
+#pragma unroll
+            for (int off = 1; off < P; off <<= 1) {
+                float w[P];
+#pragma unroll
+                for (int q = 0; q < P; ++q) w[q] = __fadd_rn(v[q], v[q ^ off]);
+#pragma unroll
+                for (int q = 0; q < P; ++q) v[q] = w[q];
+            }
+            ss = v[0];
+        } else {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) ov[c] = sm.u.o[t][lane * CPL + c];
+            ss = warp_sum_up(lane_ss(ov));
+        }
         const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.0f / D), p.eps_rms)));
         const size_t base = ((size_t)(r0 + t) * p.Hv + h) * D + lane * CPL;
 #pragma unroll
