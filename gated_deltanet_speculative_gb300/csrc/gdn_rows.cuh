@@ -384,6 +384,14 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
     if (TREE && tid < n) sm.parent[tid] = __ldg(p.parent + r0 + tid);
     // ---- a4: gates
     if (tid == 0) sm.bad = 0;
+    if (MODE == kStep && tid == 0) {   // the row follows the slot: its taps are the tail's rows 2, 1, 0
+        sm.parent[0] = -1;
+        sm.reused[0] = 0;
+        sm.order[0] = 0;
+        sm.anc[0][0] = -1;
+        sm.anc[0][1] = -2;
+        sm.anc[0][2] = -3;
+    }
     if (tid < n) {
         sm.recidx[tid] = p.rec_slot ? __ldg(p.rec_slot + r0 + tid) : r0 + tid;
         const size_t gi = (size_t)(r0 + tid) * p.Hv + h;
@@ -409,76 +417,79 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
     }
 
     // ---- each row's parent and conv ancestors along its branch -------------
-    // Each row's thread checks its own parent and record entry ...
-    if (tid < n) {
-        const int par = TREE ? sm.parent[tid] : tid - 1;
-        int bad = (par < -1 || par >= tid) ? GDN_DERR_PARENT : 0;
-        // a pooled record must be a pool entry other than the stream's slot
-        const int ri = sm.recidx[tid];
-        if (p.rec_slot && (ri < 0 || ri >= p.n_slots || ri == sl)) bad |= GDN_DERR_SLOT;
-        if (bad) atomicOr(&sm.bad, bad);
-        sm.parent[tid] = par;
-        sm.reused[tid] = 0;
-        sm.order[tid] = tid;
-    }
-    __syncthreads();
-    if (sm.bad) {   // uniform over the CTA and over its cluster (same stream)
-        if (h == 0 && tid == 0) raise_error(p.err, sm.bad);
-        return;
-    }
-    // ... then walks up to three parents for its conv ancestors
-    if (tid < n) {
-        int node = tid, tail_next = 2;
-        for (int m = 0; m < 3; ++m) {
-            if (node >= 0) node = sm.parent[node];
-            if (node >= 0) {
-                sm.anc[tid][m] = node;
-            } else {
-                sm.anc[tid][m] = tail_next - 3;
-                --tail_next;
+    // (a step's one row follows the slot: set with its gates, below)
+    if constexpr (MODE != kStep) {
+        // Each row's thread checks its own parent and record entry ...
+        if (tid < n) {
+            const int par = TREE ? sm.parent[tid] : tid - 1;
+            int bad = (par < -1 || par >= tid) ? GDN_DERR_PARENT : 0;
+            // a pooled record must be a pool entry other than the stream's slot
+            const int ri = sm.recidx[tid];
+            if (p.rec_slot && (ri < 0 || ri >= p.n_slots || ri == sl)) bad |= GDN_DERR_SLOT;
+            if (bad) atomicOr(&sm.bad, bad);
+            sm.parent[tid] = par;
+            sm.reused[tid] = 0;
+            sm.order[tid] = tid;
+        }
+        __syncthreads();
+        if (sm.bad) {   // uniform over the CTA and over its cluster (same stream)
+            if (h == 0 && tid == 0) raise_error(p.err, sm.bad);
+            return;
+        }
+        // ... then walks up to three parents for its conv ancestors
+        if (tid < n) {
+            int node = tid, tail_next = 2;
+            for (int m = 0; m < 3; ++m) {
+                if (node >= 0) node = sm.parent[node];
+                if (node >= 0) {
+                    sm.anc[tid][m] = node;
+                } else {
+                    sm.anc[tid][m] = tail_next - 3;
+                    --tail_next;
+                }
             }
         }
+        if (TREE && warp == 0) {
+            // Visit order: a tree depth first, children (and roots) in row order,
+            // so that a node follows its parent wherever it can and the parent's
+            // state is still in registers (only a node's later children reload
+            // it).  Lane t < n takes node t: its ancestor-or-self set by walking
+            // up, subtree sizes by ballot over those sets, and its preorder slot
+            // = its depth + the subtree sizes of the earlier siblings of every
+            // node on its root-to-node path.
+            const bool live = lane < n;
+            const int par = live ? sm.parent[lane] : -1;
+            uint32_t anc = live ? (1u << lane) : 0u;
+            for (int p_ = par, step = 0; step < kMaxRows; ++step) {
+                const bool up = p_ >= 0;
+                if (!__any_sync(kFull, up)) break;
+                if (up) anc |= 1u << p_;
+                const int pp = __shfl_sync(kFull, par, up ? p_ : 0);
+                p_ = up ? pp : -1;
+            }
+            int nsub = 0;
+            for (int b = 0; b < n; ++b) {
+                const uint32_t m = __ballot_sync(kFull, live && ((anc >> b) & 1u));
+                if (lane == b) nsub = __popc(m);
+            }
+            int before = 0;   // subtree sizes of the earlier siblings
+            for (int q = 0; q < n; ++q) {
+                const int pq = __shfl_sync(kFull, par, q), nq = __shfl_sync(kFull, nsub, q);
+                if (live && q < lane && pq == par) before += nq;
+            }
+            int pre = __popc(anc) - 1;
+            for (int a = 0; a < n; ++a) {
+                const int ba = __shfl_sync(kFull, before, a);
+                if ((anc >> a) & 1u) pre += ba;
+            }
+            if (live) sm.order[pre] = lane;
+            __syncwarp();
+            if (live && pre > 0 && par >= 0 && par != sm.order[pre - 1]) sm.reused[par] = 1;
+            if constexpr (MODE == kTreeLog)
+                if (live) path_mask[lane] = (int)anc;
+        }
+        __syncthreads();
     }
-    if (TREE && warp == 0) {
-        // Visit order: a tree depth first, children (and roots) in row order,
-        // so that a node follows its parent wherever it can and the parent's
-        // state is still in registers (only a node's later children reload
-        // it).  Lane t < n takes node t: its ancestor-or-self set by walking
-        // up, subtree sizes by ballot over those sets, and its preorder slot
-        // = its depth + the subtree sizes of the earlier siblings of every
-        // node on its root-to-node path.
-        const bool live = lane < n;
-        const int par = live ? sm.parent[lane] : -1;
-        uint32_t anc = live ? (1u << lane) : 0u;
-        for (int p_ = par, step = 0; step < kMaxRows; ++step) {
-            const bool up = p_ >= 0;
-            if (!__any_sync(kFull, up)) break;
-            if (up) anc |= 1u << p_;
-            const int pp = __shfl_sync(kFull, par, up ? p_ : 0);
-            p_ = up ? pp : -1;
-        }
-        int nsub = 0;
-        for (int b = 0; b < n; ++b) {
-            const uint32_t m = __ballot_sync(kFull, live && ((anc >> b) & 1u));
-            if (lane == b) nsub = __popc(m);
-        }
-        int before = 0;   // subtree sizes of the earlier siblings
-        for (int q = 0; q < n; ++q) {
-            const int pq = __shfl_sync(kFull, par, q), nq = __shfl_sync(kFull, nsub, q);
-            if (live && q < lane && pq == par) before += nq;
-        }
-        int pre = __popc(anc) - 1;
-        for (int a = 0; a < n; ++a) {
-            const int ba = __shfl_sync(kFull, before, a);
-            if ((anc >> a) & 1u) pre += ba;
-        }
-        if (live) sm.order[pre] = lane;
-        __syncwarp();
-        if (live && pre > 0 && par >= 0 && par != sm.order[pre - 1]) sm.reused[par] = 1;
-        if constexpr (MODE == kTreeLog)
-            if (live) path_mask[lane] = (int)anc;
-    }
-    __syncthreads();
 
     // ---- a2: conv over the branch's four taps, then SiLU (4 channels each) --
     for (int i = tid; i < n * (3 * D / 4); i += kRowThreads) {
