@@ -392,7 +392,17 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
         sm.anc[0][1] = -2;
         sm.anc[0][2] = -3;
     }
-    if (tid < n) {
+    // A step's gates are computed by the last thread while warps 0-2 convert
+    // the row (its a and b are loaded here, beside the row's inputs); the
+    // rows of a window or tree are computed here, one thread each.
+    constexpr int kGateThread = kRowThreads - 1;
+    uint16_t step_a = 0, step_b = 0;
+    if constexpr (MODE == kStep) {
+        if (tid == kGateThread) {
+            step_a = p.a[(size_t)r0 * p.Hv + h];
+            step_b = p.b[(size_t)r0 * p.Hv + h];
+        }
+    } else if (tid < n) {
         sm.recidx[tid] = p.rec_slot ? __ldg(p.rec_slot + r0 + tid) : r0 + tid;
         const size_t gi = (size_t)(r0 + tid) * p.Hv + h;
         const float ain = bf_bits(p.a[gi]);
@@ -491,7 +501,13 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
         __syncthreads();
     }
 
+    if (MODE == kStep && tid == kGateThread) {   // (no conv item falls to this thread)
+        const float g = -__fmul_rn(expf(A_log), softplusf_rn(__fadd_rn(bf_bits(step_a), dt_bias)));
+        sm.decay[0] = expf(g);
+        sm.beta[0] = sigmoidf_rn(bf_bits(step_b));
+    }
     // ---- a2: conv over the branch's four taps, then SiLU (4 channels each) --
+    static_assert(MODE != kStep || 3 * D / 4 <= kGateThread, "a step's conv items stop short of the gate thread");
     for (int i = tid; i < n * (3 * D / 4); i += kRowThreads) {
         const int t = i / (3 * D / 4);
         const int cc = (i - t * (3 * D / 4)) * 4;
