@@ -12,9 +12,9 @@
 // k, q and the gates alone), when the (stream, head) units alone would
 // leave SMs idle.  Each row's sums stay inside one warp with the same lane
 // layout, so a sliced step or window equals an unsliced one bit for bit; the
-// RMSNorm, the only step that mixes rows, gathers the whole o vector into
-// every slice through distributed shared memory and reduces it in the
-// unsliced order.
+// RMSNorm, the only step that mixes rows, sums o^2 in one order whatever the
+// slicing (a slice's rows are an aligned lane group of the butterfly), and
+// the slices complete that sum through distributed shared memory.
 //
 // Per row (TensorFold #932, Qwen3.5 CUDA engine note: gated delta rule and
 // causal convolution; tree note: taps and recurrence follow each row's
