@@ -762,7 +762,9 @@ __global__ void __launch_bounds__(kRowThreads, 2) gdn_rows_kernel(const __grid_c
             for (int c = 0; c < CPL; ++c) ov[c] = sm.u.o[t][lane * CPL + c];
             ss = warp_sum_up(lane_ss(ov));
         }
-        const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.0f / D), p.eps_rms)));
+        // (the fast reciprocal square root: within a few ulp, far below the
+        // output's bf16 rounding, and a short chain on the path to y)
+        const float inv = rsqrtf(__fadd_rn(__fmul_rn(ss, 1.0f / D), p.eps_rms));
         const size_t base = ((size_t)(r0 + t) * p.Hv + h) * D + lane * CPL;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
