@@ -247,7 +247,7 @@ def test_single_stream_prefill_with_several_items_per_cta_equals_pipelined_bitwi
 
 def test_prefill_long_prompt_many_chunk_groups():
     """A 16,384-token prompt with 27B-like heads: 256 chunks, which the
-    pipelined plan runs as 19 chunk groups (state handed from group to group
+    pipelined plan runs as 20 chunk groups (state handed from group to group
     through the slot), against the sequential oracle."""
     c = Case(synth.LIKE_27B, [16384], seed=233, zero_state=True)
     compare(c, run_prefill(c), threads=16)
