@@ -2,8 +2,10 @@
 //
 // Rounding discipline: every floating-point step of the recurrence, the conv
 // and the norms is written with explicit round-to-nearest intrinsics
-// (__fmul_rn / __fadd_rn / __fmaf_rn / __fdiv_rn / __fsqrt_rn), so no
-// compiler contraction can make two kernels that share these helpers round
+// (__fmul_rn / __fadd_rn / __fmaf_rn / __fdiv_rn / __fsqrt_rn) or with one
+// fixed fast intrinsic (SiLU's exponential and division, the RMSNorm's
+// reciprocal square root), the same call in every kernel, so no compiler
+// contraction can make two kernels that share these helpers round
 // differently.  That is what makes every row of a window identical, bit for
 // bit, to the same row run as a single step, and a tree node identical to
 // the chain along its path (TensorFold #932, note on the Qwen3.5 CUDA
