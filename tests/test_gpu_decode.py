@@ -178,3 +178,27 @@ def test_prepared_steps_equal_direct_calls_bitwise():
             assert np.array_equal(host_bits(r0["y"]), host_bits(r1["y"])), f"round {rnd} layer {l} y"
             assert np.array_equal(c0["state"].cpu().numpy().view(np.uint32), c1["state"].cpu().numpy().view(np.uint32))
             assert np.array_equal(host_bits(c0["tail"]), host_bits(c1["tail"]))
+
+
+def test_early_state_step_with_a_bad_slot_skips_only_that_stream():
+    """gdn_step_ex with GDN_STEP_EARLY_STATE reads slot[] before it waits;
+    a slot out of range still sets the slot bit of the error word, leaves
+    that stream's y unwritten, and the other streams equal plain steps."""
+    g = synth.LIKE_2B
+    c = Case(g, [1, 1, 1], seed=239, n_slots=3, slots=[0, 1, 2])
+    d = c.dims_gpu()
+    bad = np.array([0, 7, 2], np.int32)   # stream 1's slot is out of range
+    want_cache, want_rows = c.dev_cache(), c.dev_rows()
+    gdn.step(d, c.dev_weights(), want_cache, dev(np.array([0, 1, 2], np.int32)), want_rows)
+    assert gdn.get_device_error() == 0
+    cache, rows = c.dev_cache(), c.dev_rows()
+    gdn.step_ex(d, c.dev_weights(), cache, dev(bad), rows, gdn.STEP_EARLY_STATE)
+    assert gdn.get_device_error() & 1
+    y, wy = host_bits(rows["y"]), host_bits(want_rows["y"])
+    assert np.all(np.isnan(synth.bf16_bits_to_f32(y[1])))
+    for s in (0, 2):
+        assert np.array_equal(y[s], wy[s]), f"stream {s}"
+    st, wst = cache["state"].cpu().numpy(), want_cache["state"].cpu().numpy()
+    for sl in (0, 2):
+        assert np.array_equal(st[sl].view(np.uint32), wst[sl].view(np.uint32))
+    assert np.array_equal(st[1].view(np.uint32), c.cache["state"][1].view(np.uint32))
