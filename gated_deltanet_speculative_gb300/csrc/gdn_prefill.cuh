@@ -637,29 +637,34 @@ __global__ void __launch_bounds__(NT, 1) gdn_prefill_scan_kernel(const PrefillPa
 // (hi hi + hi lo + lo hi), accumulating in fp32.
 // ---------------------------------------------------------------------------
 constexpr int kPrepTcThreads = 512;
-constexpr int kPrepTcLD = 132;                 // fp32 row of q, k and the W stage
+constexpr int kPrepTcLD = 132;                 // fp32 row of q and k
 // Shared memory (bytes):
 constexpr int kPtQ = 0;                        // q fp32 [64][132], kept for every head
 constexpr int kPtK = 33792;                    // k fp32 [64][132], kept for every head
-constexpr int kPtR1 = 67584;                   // 65536: [K; Q] operand hi | lo; then per head
-                                               //   (diag(b) V)^T | (diag(b gamma) K)^T operands,
-                                               //   then the W fp32 stage [64][132]
-constexpr int kPtR2 = kPtR1 + 65536;           // 66304: q | k conv inputs [67][256] bf16; then per
-                                               //   head M, P, T fp32 [64][65] and the T operand
-                                               //   (at + 49920), then the U~^T fp32 stage [128][68]
+constexpr int kPtR1 = 67584;                   // 65536: per head the (diag(b) V)^T operand and
+                                               //   T' = T diag(b gamma)
+                                               //   (at + 32768), then the W fp32 stage [64][128] in
+                                               //   T''s place
+constexpr int kPtR2 = kPtR1 + 65536;           // 66304: q | k conv inputs [67][256] bf16, then the
+                                               //   [K; Q] operand hi | lo; then per head M, scratch,
+                                               //   T fp32 [64][65] and the T operand
+                                               //   (at + 49920), then the U~^T fp32 stage [128][64]
+                                               //   in the place of T and its operand (at + 33280)
 constexpr int kPtR3 = kPtR2 + 66304;           // 17152: v conv inputs [67][128] bf16 of one head
 constexpr int kPrepMaxG = 8;                   // value heads per key head (the ABI's limit)
-constexpr int kPtVec = kPtR3 + 17152;          // beta, G, eG, eGC [kPrepMaxG][64] each
-constexpr int kPtCw = kPtVec + 4 * kPrepMaxG * 64 * 4;   // conv weights: q | k channels [256][4], then one head's v [128][4]
+constexpr int kPtVec = kPtR3 + 17152;          // beta, G, eG, eGC, a [kPrepMaxG][64] each
+constexpr int kPtCw = kPtVec + 5 * kPrepMaxG * 64 * 4;   // conv weights: q | k channels [256][4], then one head's v [128][4]
 constexpr size_t kPrepTcSmem = kPtCw + 384 * 4 * 2;
+static_assert(kPrepTcSmem <= 227 * 1024, "the prep's shared memory fits one CTA's opt-in limit");
 
 template <int C>
 __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(const PrefillParams p) {
     constexpr int D = 128, LD = kPrepTcLD, AS = C + 1;   // odd row stride: column walks across rows hit distinct banks
-    constexpr int AU = C + 4;                            // U~^T stage row (16-byte aligned)
     static_assert(C == 64, "the tensor-core block layout is for C = 64");
     static_assert(kPrepTcThreads / 32 * 8 == 2 * C, "the norm step gives each warp eight of the 2C rows");
-    static_assert(3 * C * AS * 4 + 16384 <= 66304 && 128 * AU * 4 <= 66304, "region 2 holds M, scratch, T, T op / U~^T");
+    static_assert(3 * C * AS * 4 + 16384 <= 66304 && 2 * C * AS * 4 + D * C * 4 <= 66304,
+                  "region 2 holds M, scratch, T and the T operand, then the U~^T stage where T was");
+    static_assert(32768 + C * D * 4 <= 65536, "region 1 holds the W stage where T' was");
     static_assert(2 * D * C * 2 <= 64 * kPrepTcLD * 4, "q's region holds the K^T operand");
     extern __shared__ __align__(1024) unsigned char psm[];
     float *q = reinterpret_cast<float *>(psm + kPtQ);
@@ -675,12 +680,21 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     float *QK = A + C * AS;                                     // level-2 scratch [C][AS]
     float *T = QK + C * AS;                                     // T [C][AS]
     unsigned char *t_hi = R2 + 49920, *t_lo = t_hi + 8192;      // T operand [C][C]
-    float *Wf = reinterpret_cast<float *>(R1);                  // W [C][LD] after MMA 2
-    float *Uf = reinterpret_cast<float *>(R2);                  // U~^T [D][AU] after MMA 2
+    // The W and U~^T stages take the places of T' and T, which MMA 2 reads
+    // last: a head's W and U~^T leave from there while the next head's v conv
+    // writes its operand (region 1's first half), with no barrier between.
+    // Rows of 128 / 64 floats, 16-byte pieces XOR-swizzled
+    // by the row (bits 2..4 of the column), so that the TMEM readout's
+    // column writes and the row-wise reads of the stores both hit distinct
+    // banks.
+    float *Wf = reinterpret_cast<float *>(R1 + 32768);          // W [C][D]
+    float *Uf = reinterpret_cast<float *>(R2 + 2 * C * AS * 4); // U~^T [D][C]
+    auto swz = [](int row, int col) { return col ^ ((row & 7) << 2); };
     float *beta_all = reinterpret_cast<float *>(psm + kPtVec);      // [G][C], every head of the key head
     float *Gc_all = beta_all + kPrepMaxG * C;                        // log decays, then their prefix sums
     float *eG_all = Gc_all + kPrepMaxG * C;
     float *eGC_all = eG_all + kPrepMaxG * C;
+    float *dec_all = eGC_all + kPrepMaxG * C;                        // per-row decays a_t = exp(g_t)
     uint16_t *cw_qk = reinterpret_cast<uint16_t *>(psm + kPtCw);   // [2D][4]
     uint16_t *cw_v = cw_qk + 2 * D * 4;                              // [D][4] of the head in hand
     __shared__ int info[4];
@@ -756,6 +770,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         }
         Gc_all[gi * C + t] = gg;
         beta_all[gi * C + t] = bb;
+        dec_all[gi * C + t] = expf(gg);
     }
     cp_async_wait_all();
     __syncthreads();
@@ -889,17 +904,11 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
     // operands, the Q copy and K^T overlap it)
     const int quarter = warp & 3, part = warp >> 2;   // 16 warps: lane quarter x column part
 
-#pragma unroll 1
-    for (int gi = 0; gi < p.G; ++gi) {
-        const int h = kh * p.G + gi;
-        unsigned char *blk = reinterpret_cast<unsigned char *>(p.ws_chunks) + ((size_t)gc * p.Hv + h) * TcBlock::kBytes;
-        const float *beta = beta_all + gi * C, *Gc = Gc_all + gi * C, *eG = eG_all + gi * C, *eGC = eGC_all + gi * C;
-        if (gi > 0) {   // this head's v inputs and weights
-            cp_async_wait_all();
-            __syncthreads();
-        }
-        // conv + SiLU of h's v channels straight into (diag(b) V)^T
-        for (int it = tid; it < (C / PR) * D; it += kPrepTcThreads) {
+    // conv + SiLU of value head gi's v channels (staged in xv, weights in
+    // cw_v) straight into the (diag(b) V)^T operand
+    auto conv_v = [&](int gv, int first, int count) {   // on threads [first, first + count)
+        const float *bv = beta_all + gv * C;
+        for (int it = tid - first; it < (C / PR) * D; it += count) {
             const int e = it % D, t0 = (it / D) * PR;
             float act[PR];
             conv_piece(xv + (size_t)t0 * D + e, D, cw_v + e * 4, t0, act);
@@ -907,35 +916,49 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
             for (int h8 = 0; h8 < PR; h8 += 8) {
                 float vb[8];
 #pragma unroll
-                for (int e8 = 0; e8 < 8; ++e8) vb[e8] = __fmul_rn(beta[t0 + h8 + e8], act[h8 + e8]);
+                for (int e8 = 0; e8 < 8; ++e8) vb[e8] = __fmul_rn(bv[t0 + h8 + e8], act[h8 + e8]);
                 store_split8(v_hi, v_lo, e, t0 + h8, C, vb);
             }
         }
-        if (gi == 0) {   // MMA 1 done: [A; QK] in TMEM, region 2 free for M, T
-            ok = tc::mbar_wait(&bar_mma, ph, kPrepWaitLimit) && ok;
-            ph ^= 1;
-            tc::fence_after_sync();
-        }
-        __syncthreads();   // xv and cw_v consumed; the K^T operand is complete
+    };
+    conv_v(0, 0, kPrepTcThreads);
+    ok = tc::mbar_wait(&bar_mma, ph, kPrepWaitLimit) && ok;   // MMA 1: [A; QK] in TMEM, region 2 free
+    ph ^= 1;
+    tc::fence_after_sync();
+
+#pragma unroll 1
+    for (int gi = 0; gi < p.G; ++gi) {
+        const int h = kh * p.G + gi;
+        unsigned char *blk = reinterpret_cast<unsigned char *>(p.ws_chunks) + ((size_t)gc * p.Hv + h) * TcBlock::kBytes;
+        const float *beta = beta_all + gi * C, *Gc = Gc_all + gi * C, *eG = eG_all + gi * C, *eGC = eGC_all + gi * C;
+        const float *dec = dec_all + gi * C;
+        __syncthreads();   // xv and cw_v consumed; this head's v operand, the K^T operand and the
+                           // previous head's W and U~^T stores are complete
         if (gi + 1 < p.G) stage_v(h + 1);   // in flight while this head is worked on
         {   // lane r holds row r of [A; QK]; the four warps on a lane quarter take
             // 16 columns each and form M = strict_lower(diag(b) Gamma o A) (into
             // shared memory) and P = lower(Gamma o QK) (split and written to the
-            // chunk block from registers) with this head's gates
+            // chunk block from registers) with this head's gates.  Along a row,
+            // Gamma[t][s] = exp(G_t - G_s) takes one exponential, at the last of
+            // the 16 columns with s <= t; walking left, each next column is one
+            // product with a decay, Gamma[t][s - 1] = Gamma[t][s] * a_s (every
+            // factor is at most 1, so nothing overflows)
             const int r = quarter * 32 + lane;
             uint32_t v[16];
             tc::tmem_ld16_nowait(tmem_base + ((uint32_t)(quarter * 32) << 16) + part * 16, v);
-            tc::tmem_wait_ld();
             const bool isA = r < C;   // warp-uniform
             const int t = isA ? r : r - C;
+            const int c0 = part * 16, top = min(t, c0 + 15);   // top < c0: the whole piece is masked
             const float Gt = Gc[t], bt = isA ? beta[t] : 1.0f;
+            float gam = __expf(__fsub_rn(Gt, Gc[max(top, c0)]));
+            tc::tmem_wait_ld();
             float x[2][8];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int sc = part * 16 + e;
+            for (int e = 15; e >= 0; --e) {
+                const int sc = c0 + e;
                 const bool keep = t < n && sc < n && (isA ? sc < t : sc <= t);
-                const float gam = __expf(__fsub_rn(Gt, Gc[sc]));
                 x[e >> 3][e & 7] = keep ? __fmul_rn(__fmul_rn(bt, gam), __uint_as_float(v[e])) : 0.0f;
+                if (sc <= top) gam = __fmul_rn(gam, dec[sc]);
             }
             if (isA) {
                 float *dst = A + t * AS + part * 16;
@@ -950,8 +973,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
         // T = (I + M)^-1 by 16 x 16 blocks.  Threads < C solve the four diagonal
         // blocks (one column each), right-looking: once x_kk is final it is
         // folded into every later row, so each step is one FMA deep (the sums
-        // run in the same order as a row-by-row substitution).  The other
-        // threads meanwhile write K~^T = (diag(gamma_C / gamma) K)^T for the scan.
+        // run in the same order as a row-by-row substitution).
         if (tid < C) {
             const int b0 = (tid / 16) * 16, c = tid % 16;
             float x[16];
@@ -963,15 +985,6 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
                 for (int r = kk + 1; r < 16; ++r) x[r] = __fmaf_rn(-A[(b0 + r) * AS + b0 + kk], x[kk], x[r]);
 #pragma unroll
             for (int r = 0; r < 16; ++r) T[(b0 + r) * AS + b0 + c] = x[r];
-        } else {
-            for (int it = tid - C; it < D * (C / 8); it += kPrepTcThreads - C) {   // K~^T rows j, 8 t
-                const int j = it % D, t0 = (it / D) * 8;
-                float kt[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    kt[e] = (t0 + e) < n ? __fmul_rn(eGC[t0 + e], k[(t0 + e) * LD + j]) : 0.0f;
-                store_split8(blk + TcBlock::kPK, blk + TcBlock::kPK + TcBlock::kPKLo, C + j, t0, C, kt);
-            }
         }
         __syncthreads();
         // Off-diagonal blocks by doubling: for a block lower-triangular
@@ -1092,6 +1105,14 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
             tc::mma_bf16<C>(tmem_base + 128, vl, th, idn, true);
             tc::mma_commit(&bar_mma);
         }
+        // while MMA 2 runs: K~^T = (diag(gamma_C / gamma) K)^T for the scan
+        for (int it = tid; it < D * (C / 8); it += kPrepTcThreads) {   // K~^T rows j, 8 t
+            const int j = it % D, t0 = (it / D) * 8;
+            float kt[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) kt[e] = (t0 + e) < n ? __fmul_rn(eGC[t0 + e], k[(t0 + e) * LD + j]) : 0.0f;
+            store_split8(blk + TcBlock::kPK, blk + TcBlock::kPK + TcBlock::kPKLo, C + j, t0, C, kt);
+        }
         ok = tc::mbar_wait(&bar_mma, ph, kPrepWaitLimit) && ok;
         ph ^= 1;
         tc::fence_after_sync();
@@ -1107,39 +1128,51 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) gdn_prefill_prep_tc_kernel(
 #pragma unroll
             for (int q2 = 0; q2 < C / 32; ++q2) tc::tmem_ld16_nowait(taddr + q2 * 16, v[q2]);
             tc::tmem_wait_ld();
-            if (!isU) {   // column r of W: consecutive lanes, consecutive banks
+            if (!isU) {   // column r of W: the lanes' columns differ in their low five bits
 #pragma unroll
                 for (int q2 = 0; q2 < C / 32; ++q2)
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) Wf[(c0 + q2 * 16 + e) * LD + r] = __uint_as_float(v[q2][e]);
+                    for (int e = 0; e < 16; ++e) {
+                        const int t = c0 + q2 * 16 + e;
+                        Wf[t * D + swz(t, r)] = __uint_as_float(v[q2][e]);
+                    }
             } else {      // row r of U~^T as float4s (eight lanes cover the 32 banks)
-                float4 *ur = reinterpret_cast<float4 *>(Uf + r * AU + c0);
 #pragma unroll
                 for (int q2 = 0; q2 < C / 32; ++q2)
 #pragma unroll
                     for (int e = 0; e < 16; e += 4)
-                        ur[q2 * 4 + e / 4] = make_float4(__uint_as_float(v[q2][e]), __uint_as_float(v[q2][e + 1]),
-                                                         __uint_as_float(v[q2][e + 2]), __uint_as_float(v[q2][e + 3]));
+                        *reinterpret_cast<float4 *>(Uf + r * C + swz(r, c0 + q2 * 16 + e)) =
+                            make_float4(__uint_as_float(v[q2][e]), __uint_as_float(v[q2][e + 1]),
+                                        __uint_as_float(v[q2][e + 2]), __uint_as_float(v[q2][e + 3]));
             }
         }
-        __syncthreads();
-        {   // U~^T [128][64] fp32, row-major, coalesced 16-byte stores
-            float4 *dst = reinterpret_cast<float4 *>(blk + TcBlock::kUt);
-            for (int it = tid; it < D * C / 4; it += kPrepTcThreads) {
+        if (gi + 1 < p.G) cp_async_wait_all();   // the next head's v inputs and weights
+        __syncthreads();   // the W and U~^T stages are complete (and the next head's v inputs landed)
+        // The stores leave at the SM's store rate, and a thread waits on its
+        // own stores: with a next head, warps 0-7 store while warps 8-15 run
+        // its v conv (which writes the v operand in region 1's first half and
+        // touches neither stage); the next head's first barrier orders both
+        // before M and T reuse the stages.  The last head stores on every warp.
+        const bool more = gi + 1 < p.G;
+        const int n_st = more ? kPrepTcThreads / 2 : kPrepTcThreads;
+        if (tid < n_st) {
+            float4 *dst = reinterpret_cast<float4 *>(blk + TcBlock::kUt);   // U~^T [128][64] fp32, row-major
+            for (int it = tid; it < D * C / 4; it += n_st) {
                 const int i = it / (C / 4), t4 = it % (C / 4);
-                dst[it] = *reinterpret_cast<const float4 *>(Uf + i * AU + t4 * 4);
+                dst[it] = *reinterpret_cast<const float4 *>(Uf + i * C + swz(i, t4 * 4));
             }
+            for (int it = tid; it < C * (D / 8); it += n_st) {   // -W hi | lo, rows t, 8 columns j
+                const int t = it % C, j0 = (it / C) * 8;
+                const float4 a4 = *reinterpret_cast<const float4 *>(Wf + t * D + swz(t, j0));
+                const float4 b4 = *reinterpret_cast<const float4 *>(Wf + t * D + swz(t, j0 + 4));
+                const float x[8] = {-a4.x, -a4.y, -a4.z, -a4.w, -b4.x, -b4.y, -b4.z, -b4.w};
+                store_split8(blk + TcBlock::kWQ, blk + TcBlock::kWQ + TcBlock::kWQLo, t, j0, D, x);
+            }
+            if (tid == 0) *reinterpret_cast<float *>(blk + TcBlock::kMisc) = eG[n - 1];
+            if (tid < C) reinterpret_cast<float *>(blk + TcBlock::kGam)[tid] = eG[tid];   // gamma_t for O
+        } else {
+            conv_v(gi + 1, n_st, kPrepTcThreads - n_st);
         }
-        for (int it = tid; it < C * (D / 8); it += kPrepTcThreads) {   // -W hi | lo, rows t, 8 columns j
-            const int t = it % C, j0 = (it / C) * 8;
-            const float4 a4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0);
-            const float4 b4 = *reinterpret_cast<const float4 *>(Wf + t * LD + j0 + 4);
-            const float x[8] = {-a4.x, -a4.y, -a4.z, -a4.w, -b4.x, -b4.y, -b4.z, -b4.w};
-            store_split8(blk + TcBlock::kWQ, blk + TcBlock::kWQ + TcBlock::kWQLo, t, j0, D, x);
-        }
-        if (tid == 0) *reinterpret_cast<float *>(blk + TcBlock::kMisc) = eG[n - 1];
-        if (tid < C) reinterpret_cast<float *>(blk + TcBlock::kGam)[tid] = eG[tid];   // gamma_t for O
-        __syncthreads();   // the W stage is read; the next head reuses region 1
     }
     }   // items
     if (tid == 0) {
