@@ -619,20 +619,28 @@ __global__ void __launch_bounds__(NT, 1) gdn_prefill_scan_kernel(const PrefillPa
 // in turn (the grid may be held below the SM count so that a concurrent
 // scan finds free SMs).  An item writes the chunk block (TcBlock) of each
 // of the G value heads that share the key head.
-// Once per key head:
+// Once per key head (item):
+//   the gates of all G value heads (log decays, their prefix sums G_t,
+//   gamma_t = exp(G_t), gamma_C / gamma_t, beta_t and the decays a_t);
 //   conv + SiLU of the q and k channels (16-row pieces of one channel, no
 //   per-row branches); L2 norms, eight rows per warp in one reduce-scatter;
-//   MMA 1:  [K; Q] (128 x 128) * K^T -> K K^T and Q K^T, left in TMEM
+//   MMA 1:  [K; Q] (128 x 128) * K^T -> K K^T and Q K^T, left in TMEM;
+//   Q (shared by the value heads) out to the key head's first block, and
+//   the K^T operand, the A operand of every head's W product.
 // Then for each value head h of the group (its v inputs staged while the
 // previous head is worked on):
-//   gates of h; conv + SiLU of h's v channels straight into (diag(b) V)^T;
-//   (diag(b gamma) K)^T and K~^T (Q, shared by the value heads, goes out
-//   once per item, with gamma_t of each head for the scan);
+//   conv + SiLU of h's v channels straight into (diag(b) V)^T (the first
+//   head's while MMA 1 runs, each later one's beside the previous head's
+//   stores);
 //   M = strict_lower(diag(b) Gamma o A), P = lower(Gamma o Q K^T), formed
-//   from the TMEM readout of MMA 1 with h's gates;
+//   from the TMEM readout of MMA 1 with h's gates; along a row, Gamma is one
+//   exponential per 16 columns and products with the decays a_s;
 //   T = (I + M)^-1 on the CUDA cores (fp32): 16 x 16 diagonal blocks by
 //   forward substitution, the rest by two levels of block doubling;
-//   MMA 2:  (diag(b gamma) K)^T * T^T -> W^T,   (diag(b) V)^T * T^T -> U~^T
+//   MMA 2:  K^T * T'^T -> W^T with T' = T diag(b gamma) (W = T diag(b gamma) K),
+//           (diag(b) V)^T * T^T -> U~^T,
+//   while K~^T = (diag(gamma_C / gamma) K)^T goes out for the scan; W and
+//   U~^T leave TMEM into stages where T' and T were and go out from there.
 // Every MMA operand is split into bf16 hi + lo and multiplied three times
 // (hi hi + hi lo + lo hi), accumulating in fp32.
 // ---------------------------------------------------------------------------
